@@ -1,0 +1,275 @@
+"""GB300 (sm_103a) dense projection GEMMs -- Python binding of ``libdp_gb300.so``.
+
+The functions here marshal torch tensors into the C ABI of ``include/dp_gemm.h``
+(pointers, sizes, leading dimensions, the current CUDA stream) and return the
+output tensor.  Every step of the computation runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  If the library is not built, the
+first call raises.
+
+  dp_gemm_fwd(X, W)        Y  = X W^T       X[T,K], W[N,K]  (bf16)  -> Y[T,N]
+  dp_gemm_dgrad(dY, W)     dX = dY W        dY[T,N], W[N,K] (bf16)  -> dX[T,K]
+  dp_gemm_wgrad(dY, X)     dW = dY^T X      dY[T,N], X[T,K] (bf16)  -> dW[N,K]
+  router_fwd / router_dgrad / router_wgrad: the same on FP32 operands through
+  BF16x3 emulation, FP32 output.
+
+Outputs are bf16 (``out_dtype=torch.bfloat16``) or fp32 for the BF16 ops.  An
+``out=`` tensor may be a column slice of a wider buffer (padded row stride).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdp_gb300.so")
+
+DP_OUT_BF16, DP_OUT_F32 = 0, 1
+OP_FWD, OP_DGRAD, OP_WGRAD, OP_ROUTER_FWD, OP_ROUTER_DGRAD, OP_ROUTER_WGRAD = range(6)
+OP_NAMES = {"fwd": OP_FWD, "dgrad": OP_DGRAD, "wgrad": OP_WGRAD,
+            "router_fwd": OP_ROUTER_FWD, "router_dgrad": OP_ROUTER_DGRAD, "router_wgrad": OP_ROUTER_WGRAD}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DPError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "block_m", "block_n", "block_k", "stages", "splits", "raster_group", "grid",
+        "a_mn_major", "b_mn_major", "reserved")] + [(n, ctypes.c_int64) for n in (
+        "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units")] + [
+        ("workspace_bytes", ctypes.c_uint64)]
+
+
+def lib():
+    """Load libdp_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m fp32_dense_projection_gb300.build` (or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+        tail = [I, I, I, S, S, P, Z, P]          # T N K out deterministic ws ws_bytes stream
+        rtail = [I, I, I, S, P, Z, P]            # T N K deterministic ws ws_bytes stream
+        for name in ("dp_gemm_fwd", "dp_gemm_dgrad", "dp_gemm_wgrad"):
+            getattr(L, name).argtypes = [P, P, P] + tail
+            getattr(L, name + "_ex").argtypes = [P, I, P, I, P, I] + tail
+        for name in ("router_fwd", "router_dgrad", "router_wgrad"):
+            getattr(L, name).argtypes = [P, P, P] + rtail
+            getattr(L, name + "_ex").argtypes = [P, I, P, I, P, I] + rtail
+        L.dp_plan_query.argtypes = [S, I, I, I, S, S, ctypes.POINTER(PlanInfo)]
+        L.dp_workspace_size.argtypes = [S, I, I, I, S, S, ctypes.POINTER(ctypes.c_size_t)]
+        L.dp_init.argtypes = [S]
+        L.dp_device_error.argtypes = [S]
+        L.dp_status_string.argtypes = [S]
+        L.dp_status_string.restype = ctypes.c_char_p
+        L.dp_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().dp_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library missing
+        return f"status {status}"
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise DPError(status, what)
+
+
+def plan(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0) -> dict:
+    """The library's plan for a call (pure function of the shape and SM count)."""
+    op = OP_NAMES.get(op, op)
+    info = PlanInfo()
+    _check(lib().dp_plan_query(int(op), T, N, K, int(bool(out_f32)), int(sm_count), ctypes.byref(info)),
+           "dp_plan_query")
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
+
+
+def workspace_size(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0) -> int:
+    op = OP_NAMES.get(op, op)
+    n = ctypes.c_size_t(0)
+    _check(lib().dp_workspace_size(int(op), T, N, K, int(bool(out_f32)), int(sm_count), ctypes.byref(n)),
+           "dp_workspace_size")
+    return int(n.value)
+
+
+def init(device: int = -1):
+    _check(lib().dp_init(int(device)), "dp_init")
+
+
+def device_error(clear: bool = True) -> int:
+    """Synchronise and return the library's device fault status (0 = none)."""
+    return int(lib().dp_device_error(int(bool(clear))))
+
+
+# ------------------------------------------------------------------ workspace
+
+class Workspace:
+    """A caller-owned, zero-initialised device workspace that grows on demand.
+
+    The library needs the workspace zeroed before its first use only (its split
+    counters reset themselves); a grown buffer is a fresh zeroed tensor.
+    """
+
+    def __init__(self, device=None):
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        self.buf = None
+
+    def get(self, nbytes: int):
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_workspaces: dict = {}
+
+
+def _default_workspace(device: torch.device) -> Workspace:
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = _workspaces[key] = Workspace(device.index)
+    return ws
+
+
+# --------------------------------------------------------------- marshalling
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError("operands must be 2-D with unit column stride")
+    if t.size(0) <= 1:
+        return max(t.stride(0), t.size(1))
+    return t.stride(0)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device: torch.device, stream):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(op, T, N, K, out_f32, device, workspace):
+    need = workspace_size(op, T, N, K, out_f32)
+    if workspace is None:
+        buf = _default_workspace(device).get(need)
+    else:
+        buf = workspace
+    nbytes = 0 if buf is None else buf.numel() * buf.element_size()
+    return buf, nbytes
+
+
+def _gemm(op: int, name: str, a: torch.Tensor, b: torch.Tensor, out_shape, out, out_dtype, deterministic,
+          workspace, stream, T, N, K):
+    router = op >= OP_ROUTER_FWD
+    in_dtype = torch.float32 if router else torch.bfloat16
+    if a.dtype != in_dtype or b.dtype != in_dtype:
+        raise TypeError(f"{name}: operands must be {in_dtype}")
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError(f"{name}: operands must be CUDA tensors")
+    device = a.device
+    if router:
+        out_dtype = torch.float32
+    if out is None:
+        out = torch.empty(out_shape, dtype=out_dtype, device=device)
+    elif tuple(out.shape) != tuple(out_shape) or out.dtype != out_dtype:
+        raise ValueError(f"{name}: out must be {tuple(out_shape)} {out_dtype}")
+    out_f32 = out.dtype == torch.float32
+    buf, nbytes = _ws(op, T, N, K, out_f32, device, workspace)
+    L = lib()
+    with torch.cuda.device(device):
+        st = _stream(device, stream)
+        if router:
+            fn = getattr(L, name + "_ex")
+            status = fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K, int(bool(deterministic)),
+                        _ptr(buf), nbytes, st)
+        else:
+            fn = getattr(L, name + "_ex")
+            status = fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K,
+                        DP_OUT_F32 if out_f32 else DP_OUT_BF16, int(bool(deterministic)), _ptr(buf), nbytes, st)
+    _check(status, name)
+    return out
+
+
+def dp_gemm_fwd(X, W, out=None, out_dtype=torch.bfloat16, deterministic=True, workspace=None, stream=None):
+    """Y[T,N] = X[T,K] W[N,K]^T (bf16 in, FP32 accumulate, bf16 or fp32 out)."""
+    T, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("dp_gemm_fwd: W must be N x K")
+    return _gemm(OP_FWD, "dp_gemm_fwd", X, W, (T, N), out, out_dtype, deterministic, workspace, stream, T, N, K)
+
+
+def dp_gemm_dgrad(dY, W, out=None, out_dtype=torch.bfloat16, deterministic=True, workspace=None, stream=None):
+    """dX[T,K] = dY[T,N] W[N,K]."""
+    T, N = dY.shape
+    K = W.shape[1]
+    if W.shape[0] != N:
+        raise ValueError("dp_gemm_dgrad: W must be N x K")
+    return _gemm(OP_DGRAD, "dp_gemm_dgrad", dY, W, (T, K), out, out_dtype, deterministic, workspace, stream,
+                 T, N, K)
+
+
+def dp_gemm_wgrad(dY, X, out=None, out_dtype=torch.bfloat16, deterministic=True, workspace=None, stream=None):
+    """dW[N,K] = dY[T,N]^T X[T,K] (contraction over the T tokens)."""
+    T, N = dY.shape
+    K = X.shape[1]
+    if X.shape[0] != T:
+        raise ValueError("dp_gemm_wgrad: X must be T x K")
+    return _gemm(OP_WGRAD, "dp_gemm_wgrad", dY, X, (N, K), out, out_dtype, deterministic, workspace, stream,
+                 T, N, K)
+
+
+def router_fwd(X, W, out=None, deterministic=True, workspace=None, stream=None):
+    """FP32 router forward through BF16x3: Y[T,E] = X[T,H] W[E,H]^T."""
+    T, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("router_fwd: W must be E x H")
+    return _gemm(OP_ROUTER_FWD, "router_fwd", X, W, (T, N), out, torch.float32, deterministic, workspace,
+                 stream, T, N, K)
+
+
+def router_dgrad(dY, W, out=None, deterministic=True, workspace=None, stream=None):
+    """FP32 router input gradient through BF16x3: dX[T,H] = dY[T,E] W[E,H]."""
+    T, N = dY.shape
+    K = W.shape[1]
+    if W.shape[0] != N:
+        raise ValueError("router_dgrad: W must be E x H")
+    return _gemm(OP_ROUTER_DGRAD, "router_dgrad", dY, W, (T, K), out, torch.float32, deterministic, workspace,
+                 stream, T, N, K)
+
+
+def router_wgrad(dY, X, out=None, deterministic=True, workspace=None, stream=None):
+    """FP32 router weight gradient through BF16x3: dW[E,H] = dY[T,E]^T X[T,H]."""
+    T, N = dY.shape
+    K = X.shape[1]
+    if X.shape[0] != T:
+        raise ValueError("router_wgrad: X must be T x H")
+    return _gemm(OP_ROUTER_WGRAD, "router_wgrad", dY, X, (N, K), out, torch.float32, deterministic, workspace,
+                 stream, T, N, K)
+
+
+OPS = {"fwd": dp_gemm_fwd, "dgrad": dp_gemm_dgrad, "wgrad": dp_gemm_wgrad,
+       "router_fwd": router_fwd, "router_dgrad": router_dgrad, "router_wgrad": router_wgrad}

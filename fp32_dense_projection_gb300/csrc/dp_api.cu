@@ -1,0 +1,502 @@
+// C ABI of the dense projection GEMM library (declared in include/dp_gemm.h):
+// argument checks, the planner call, TMA tensor-map encoding, the BF16x3 operand
+// split of the router, and the kernel launches.  Nothing here allocates device
+// memory or synchronises, except the explicit debug read-out dp_device_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "dp_gemm.h"
+#include "gemm_kernel.cuh"
+#include "planner.h"
+
+namespace {
+
+using namespace dp;
+
+// Device status word: kernels OR fault bits into it when a bounded wait gives up.
+__device__ uint32_t g_fault_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool initialised = false;
+  dp_status status = DP_OK;
+  int sm_count = 0;
+  uint32_t* fault = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+dp_status init_device(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_devices[dev];
+  if (!d.initialised) {
+    int major = 0, minor = 0, sm = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return DP_ERR_LAUNCH;
+    }
+    d.sm_count = sm;
+    if (major != 10 || minor != 3) {
+      d.status = DP_ERR_ARCH;  // the library carries sm_103a code only
+    } else {
+      int cur = -1;
+      if (cudaGetDevice(&cur) != cudaSuccess) return DP_ERR_LAUNCH;
+      if (cur != dev && cudaSetDevice(dev) != cudaSuccess) return DP_ERR_LAUNCH;
+      void* fault = nullptr;
+      cudaError_t e = set_attributes_kk();
+      if (e == cudaSuccess) e = set_attributes_km();
+      if (e == cudaSuccess) e = set_attributes_mm();
+      if (e == cudaSuccess) e = cudaGetSymbolAddress(&fault, g_fault_word);
+      if (cur != dev) cudaSetDevice(cur);
+      if (e != cudaSuccess) return DP_ERR_LAUNCH;
+      d.fault = static_cast<uint32_t*>(fault);
+      d.status = DP_OK;
+    }
+    d.initialised = true;
+  }
+  *out = &d;
+  return d.status;
+}
+
+dp_status current_device(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DP_ERR_LAUNCH;
+  return init_device(dev, out);
+}
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 map over a row-major [rows][cols] matrix (leading dimension ld elements),
+// box = box_rows x 64 columns, 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ router split
+
+// BF16x3 operand split.  For each FP32 value x: hi = RNE(x), lo = RNE(x - hi)
+// (x - hi is exact in FP32).  Writes three bf16 segments of an R x C source,
+// either side by side (dst is R x 3C) or stacked (dst is 3R x C); bit i of
+// lo_mask selects lo for segment i.  The A operand uses (hi, hi, lo) and the B
+// operand (hi, lo, hi), so the contraction over the tripled axis is
+// sum hi*hi + hi*lo + lo*hi (FlashInfer page "perf(cake_dense_projection_gemm):
+// cache the router entry points' calls by their own tensors": FP32 router GEMM
+// through BF16x3 emulation).
+__global__ void __launch_bounds__(256) split_bf16x3_kernel(const float* __restrict__ src, int64_t R, int64_t C,
+                                                           int64_t lds, uint16_t* __restrict__ dst,
+                                                           int stacked, int lo_mask) {
+  const int64_t quads = C / 4;
+  const int64_t total = R * quads;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t r = i / quads;
+    const int64_t c = (i - r * quads) * 4;
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    const uint32_t h01 = pack_bf16x2(x.x, x.y);
+    const uint32_t h23 = pack_bf16x2(x.z, x.w);
+    const float hx = __uint_as_float(h01 << 16), hy = __uint_as_float(h01 & 0xFFFF0000u);
+    const float hz = __uint_as_float(h23 << 16), hw = __uint_as_float(h23 & 0xFFFF0000u);
+    const uint2 hi = make_uint2(h01, h23);
+    const uint2 lo = make_uint2(pack_bf16x2(x.x - hx, x.y - hy), pack_bf16x2(x.z - hz, x.w - hw));
+#pragma unroll
+    for (int seg = 0; seg < 3; ++seg) {
+      const uint2 v = ((lo_mask >> seg) & 1) ? lo : hi;
+      uint16_t* d = stacked ? dst + (seg * R + r) * C + c : dst + r * (3 * C) + seg * C + c;
+      *reinterpret_cast<uint2*>(d) = v;
+    }
+  }
+}
+
+cudaError_t launch_split(const float* src, int64_t R, int64_t C, int64_t lds, uint16_t* dst, bool stacked,
+                         int lo_mask, int sm, cudaStream_t stream) {
+  const int64_t total = R * (C / 4);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm) * 8;
+  if (blocks > cap) blocks = cap;
+  split_bf16x3_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, R, C, lds, dst, stacked ? 1 : 0,
+                                                                         lo_mask);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ argument checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A row-major rows x cols operand with leading dimension ld (0 = cols).
+dp_status check_matrix(const void* p, int64_t rows, int64_t cols, int64_t* ld, int esize) {
+  if (*ld == 0) *ld = cols;
+  if (*ld < cols) return DP_ERR_INVALID_ARG;
+  if (rows > 0 && p == nullptr) return DP_ERR_INVALID_ARG;
+  if (!aligned16(p)) return DP_ERR_ALIGNMENT;
+  if ((*ld * esize) % 16 != 0) return DP_ERR_ALIGNMENT;
+  if (*ld > (int64_t{1} << 36)) return DP_ERR_UNSUPPORTED;
+  return DP_OK;
+}
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+// Plan overrides for tuning and tests (DP_FORCE_BN, DP_FORCE_SPLITS); read once.
+void forced(int* bn, int* splits) {
+  static const int f_bn = env_int("DP_FORCE_BN");
+  static const int f_s = env_int("DP_FORCE_SPLITS");
+  *bn = f_bn;
+  *splits = f_s;
+}
+
+bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan) {
+  int fbn = 0, fs = 0;
+  forced(&fbn, &fs);
+  return make_plan(op, T, N, K, out_f32, sm, plan, fbn, fs);
+}
+
+dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
+  if (T < 0 || N < 1 || K < 1) return DP_ERR_INVALID_ARG;
+  if (N % 8 != 0 || K % 8 != 0) return DP_ERR_UNSUPPORTED;
+  const int64_t lim = 0x7FFFFFFF;
+  const int64_t mult = op >= kOpRouterFwd ? 3 : 1;  // the router triples the contraction axis
+  if (T * mult > lim || N * mult > lim || K * mult > lim) return DP_ERR_UNSUPPORTED;
+  return DP_OK;
+}
+
+// ------------------------------------------------------------ one GEMM launch
+
+// A: operand (m, k) -- K-major: [gm][gk] matrix; MN-major: [gk][gm] matrix.
+// B: operand (n, k) -- K-major: [gn][gk] matrix; MN-major: [gk][gn] matrix.
+dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, void* out, int64_t ldo, void* ws, cudaStream_t stream) {
+  if (p.units > 0x7FFFFFFF || p.tiles_m > 0x7FFFFFFF || p.tiles_n > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF)
+    return DP_ERR_UNSUPPORTED;
+  GemmLaunch l;
+  std::memset(&l, 0, sizeof(l));
+  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, 64) : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM);
+  const bool ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, 64)
+                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, static_cast<uint32_t>(p.bn));
+  if (!ok_a || !ok_b) return DP_ERR_LAUNCH;
+  GemmArgs& a = l.args;
+  a.gm = p.gm;
+  a.gn = p.gn;
+  a.nkb = static_cast<int32_t>(p.nkb);
+  a.splits = p.splits;
+  a.tiles_m = static_cast<int32_t>(p.tiles_m);
+  a.tiles_n = static_cast<int32_t>(p.tiles_n);
+  a.group = p.group;
+  a.units = static_cast<int32_t>(p.units);
+  a.out = out;
+  a.ldo = ldo;
+  a.out_f32 = p.out_f32;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
+  a.counters = p.splits > 1 ? reinterpret_cast<uint32_t*>(w + p.off_counters) : nullptr;
+  a.fault = dev.fault;
+  l.grid = p.grid;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (!p.a_mn && !p.b_mn)
+    e = launch_gemm_kk(p.bn, l, stream);
+  else if (!p.a_mn && p.b_mn)
+    e = launch_gemm_km(p.bn, l, stream);
+  else if (p.a_mn && p.b_mn)
+    e = launch_gemm_mm(p.bn, l, stream);
+  return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
+}
+
+dp_status zero_output(void* out, int64_t rows, int64_t cols, int64_t ld, int esize, cudaStream_t stream) {
+  if (rows == 0) return DP_OK;
+  const cudaError_t e = cudaMemset2DAsync(out, static_cast<size_t>(ld) * esize, 0, static_cast<size_t>(cols) * esize,
+                                          static_cast<size_t>(rows), stream);
+  return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
+}
+
+// Shapes of the three operands of each op: a [ra][ca], b [rb][cb], out [ro][co].
+void op_shapes(int op, int64_t T, int64_t N, int64_t K, int64_t* ra, int64_t* ca, int64_t* rb, int64_t* cb,
+               int64_t* ro, int64_t* co) {
+  switch (op % 3) {
+    case kOpFwd:  // X[T][K], W[N][K] -> Y[T][N]
+      *ra = T, *ca = K, *rb = N, *cb = K, *ro = T, *co = N;
+      break;
+    case kOpDgrad:  // dY[T][N], W[N][K] -> dX[T][K]
+      *ra = T, *ca = N, *rb = N, *cb = K, *ro = T, *co = K;
+      break;
+    default:  // dY[T][N], X[T][K] -> dW[N][K]
+      *ra = T, *ca = N, *rb = T, *cb = K, *ro = N, *co = K;
+      break;
+  }
+}
+
+dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb, void* out, int64_t ldo, int64_t T,
+                 int64_t N, int64_t K, int out_f32, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const bool router = op >= kOpRouterFwd;
+  if (!router && out_f32 != DP_OUT_BF16 && out_f32 != DP_OUT_F32) return DP_ERR_INVALID_ARG;
+  dp_status st = check_sizes(T, N, K, op);
+  if (st != DP_OK) return st;
+  int64_t ra, ca, rb, cb, ro, co;
+  op_shapes(op, T, N, K, &ra, &ca, &rb, &cb, &ro, &co);
+  const int in_size = router ? 4 : 2;
+  const int out_size = (router || out_f32) ? 4 : 2;
+  if ((st = check_matrix(a, ra, ca, &lda, in_size)) != DP_OK) return st;
+  if ((st = check_matrix(b, rb, cb, &ldb, in_size)) != DP_OK) return st;
+  if ((st = check_matrix(out, ro, co, &ldo, out_size)) != DP_OK) return st;
+  if (out == nullptr && ro > 0) return DP_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != DP_OK) return st;
+
+  if (T == 0) {  // empty token set: nothing to compute, the weight gradient is zero
+    if (op % 3 == kOpWgrad) return zero_output(out, ro, co, ldo, out_size, stream);
+    return DP_OK;
+  }
+  Plan p;
+  if (!plan_for(op, T, N, K, out_size == 4 ? 1 : 0, dev->sm_count, &p)) return DP_ERR_INVALID_ARG;
+  if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes)) return DP_ERR_WORKSPACE;
+  if (p.ws_bytes > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
+
+  if (!router) return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
+
+  // Router: split both FP32 operands into (hi, lo) bf16 segments along the
+  // contraction axis, then one BF16 GEMM over the tripled contraction.
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* a3 = reinterpret_cast<uint16_t*>(w + p.off_router_a);
+  uint16_t* b3 = reinterpret_cast<uint16_t*>(w + p.off_router_b);
+  const float* af = static_cast<const float*>(a);
+  const float* bf = static_cast<const float*>(b);
+  constexpr int kHiHiLo = 0b100, kHiLoHi = 0b010;
+  cudaError_t e = cudaSuccess;
+  int64_t ld3a = 0, ld3b = 0;
+  switch (op) {
+    case kOpRouterFwd:  // A' = X [T][3K], B' = W [N][3K]
+      e = launch_split(af, T, K, lda, a3, false, kHiHiLo, dev->sm_count, stream);
+      if (e == cudaSuccess) e = launch_split(bf, N, K, ldb, b3, false, kHiLoHi, dev->sm_count, stream);
+      ld3a = 3 * K;
+      ld3b = 3 * K;
+      break;
+    case kOpRouterDgrad:  // A' = dY [T][3N], B' = W stacked [3N][K]
+      e = launch_split(af, T, N, lda, a3, false, kHiHiLo, dev->sm_count, stream);
+      if (e == cudaSuccess) e = launch_split(bf, N, K, ldb, b3, true, kHiLoHi, dev->sm_count, stream);
+      ld3a = 3 * N;
+      ld3b = K;
+      break;
+    default:  // A' = dY stacked [3T][N], B' = X stacked [3T][K]
+      e = launch_split(af, T, N, lda, a3, true, kHiHiLo, dev->sm_count, stream);
+      if (e == cudaSuccess) e = launch_split(bf, T, K, ldb, b3, true, kHiLoHi, dev->sm_count, stream);
+      ld3a = N;
+      ld3b = K;
+      break;
+  }
+  if (e != cudaSuccess) return DP_ERR_LAUNCH;
+  return launch_view(p, *dev, a3, ld3a, b3, ld3b, out, ldo, ws, stream);
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+dp_status dp_gemm_fwd_ex(const void* X, int64_t ldx, const void* W, int64_t ldw, void* Y, int64_t ldy, int64_t T,
+                         int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                         size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpFwd, X, ldx, W, ldw, Y, ldy, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                      int deterministic, void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return dp_gemm_fwd_ex(X, 0, W, 0, Y, 0, T, N, K, out, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status dp_gemm_dgrad_ex(const void* dY, int64_t ldg, const void* W, int64_t ldw, void* dX, int64_t ldx, int64_t T,
+                           int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                           size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpDgrad, dY, ldg, W, ldw, dX, ldx, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                        int deterministic, void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return dp_gemm_dgrad_ex(dY, 0, W, 0, dX, 0, T, N, K, out, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status dp_gemm_wgrad_ex(const void* dY, int64_t ldg, const void* X, int64_t ldx, void* dW, int64_t ldw, int64_t T,
+                           int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                           size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpWgrad, dY, ldg, X, ldx, dW, ldw, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                        int deterministic, void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return dp_gemm_wgrad_ex(dY, 0, X, 0, dW, 0, T, N, K, out, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status router_fwd_ex(const float* X, int64_t ldx, const float* W, int64_t ldw, float* Y, int64_t ldy, int64_t T,
+                        int64_t N, int64_t K, int deterministic, void* workspace, size_t workspace_bytes,
+                        dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpRouterFwd, X, ldx, W, ldw, Y, ldy, T, N, K, 1, workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status router_fwd(const float* X, const float* W, float* Y, int64_t T, int64_t N, int64_t K, int deterministic,
+                     void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return router_fwd_ex(X, 0, W, 0, Y, 0, T, N, K, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status router_dgrad_ex(const float* dY, int64_t ldg, const float* W, int64_t ldw, float* dX, int64_t ldx,
+                          int64_t T, int64_t N, int64_t K, int deterministic, void* workspace,
+                          size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpRouterDgrad, dY, ldg, W, ldw, dX, ldx, T, N, K, 1, workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status router_dgrad(const float* dY, const float* W, float* dX, int64_t T, int64_t N, int64_t K,
+                       int deterministic, void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return router_dgrad_ex(dY, 0, W, 0, dX, 0, T, N, K, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t ldx, float* dW, int64_t ldw,
+                          int64_t T, int64_t N, int64_t K, int deterministic, void* workspace,
+                          size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_op(kOpRouterWgrad, dY, ldg, X, ldx, dW, ldw, T, N, K, 1, workspace, workspace_bytes,
+                static_cast<cudaStream_t>(stream));
+}
+
+dp_status router_wgrad(const float* dY, const float* X, float* dW, int64_t T, int64_t N, int64_t K,
+                       int deterministic, void* workspace, size_t workspace_bytes, dp_stream stream) {
+  return router_wgrad_ex(dY, 0, X, 0, dW, 0, T, N, K, deterministic, workspace, workspace_bytes, stream);
+}
+
+dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int sm_count,
+                        dp_plan_info* info) {
+  if (!info || static_cast<int>(op) < 0 || static_cast<int>(op) > kOpRouterWgrad) return DP_ERR_INVALID_ARG;
+  const dp_status st = check_sizes(T, N, K, static_cast<int>(op));
+  if (st != DP_OK) return st;
+  if (sm_count <= 0) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DP_ERR_LAUNCH;
+  }
+  const bool router = static_cast<int>(op) >= kOpRouterFwd;
+  Plan p;
+  if (!plan_for(static_cast<int>(op), T, N, K, (router || out == DP_OUT_F32) ? 1 : 0, sm_count, &p))
+    return DP_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  info->block_m = p.bm;
+  info->block_n = p.bn;
+  info->block_k = p.bk;
+  info->stages = p.stages;
+  info->splits = p.splits;
+  info->raster_group = p.group;
+  info->grid = p.grid;
+  info->a_mn_major = p.a_mn ? 1 : 0;
+  info->b_mn_major = p.b_mn ? 1 : 0;
+  info->gemm_m = p.gm;
+  info->gemm_n = p.gn;
+  info->gemm_k = p.gk;
+  info->tiles_m = p.tiles_m;
+  info->tiles_n = p.tiles_n;
+  info->k_blocks = p.nkb;
+  info->units = p.units;
+  info->workspace_bytes = T == 0 ? 0 : p.ws_bytes;
+  return DP_OK;
+}
+
+dp_status dp_workspace_size(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int sm_count,
+                            size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  dp_plan_info info;
+  const dp_status st = dp_plan_query(op, T, N, K, out, sm_count, &info);
+  if (st != DP_OK) return st;
+  *bytes = static_cast<size_t>(info.workspace_bytes);
+  return DP_OK;
+}
+
+dp_status dp_init(int device) {
+  if (device < 0 && cudaGetDevice(&device) != cudaSuccess) return DP_ERR_LAUNCH;
+  DeviceState* d = nullptr;
+  return init_device(device, &d);
+}
+
+dp_status dp_device_error(int clear) {
+  DeviceState* d = nullptr;
+  dp_status st = current_device(&d);
+  if (st != DP_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DP_ERR_LAUNCH;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fault_word, sizeof(word)) != cudaSuccess) return DP_ERR_LAUNCH;
+  if (clear) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero)) != cudaSuccess) return DP_ERR_LAUNCH;
+  }
+  return word ? DP_ERR_TIMEOUT : DP_OK;
+}
+
+const char* dp_status_string(dp_status status) {
+  switch (status) {
+    case DP_OK:
+      return "ok";
+    case DP_ERR_INVALID_ARG:
+      return "invalid argument";
+    case DP_ERR_ALIGNMENT:
+      return "pointer or row stride not 16-byte aligned";
+    case DP_ERR_UNSUPPORTED:
+      return "unsupported size (N and K must be multiples of 8; sizes below 2^31)";
+    case DP_ERR_WORKSPACE:
+      return "workspace missing or smaller than dp_workspace_size()";
+    case DP_ERR_ARCH:
+      return "current device is not sm_103a (compute capability 10.3)";
+    case DP_ERR_LAUNCH:
+      return "a CUDA call failed while enqueueing";
+    case DP_ERR_TIMEOUT:
+      return "a kernel gave up waiting on a barrier";
+    default:
+      return "unknown status";
+  }
+}
+
+int dp_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,401 @@
+// Persistent, warp-specialised BF16 GEMM for sm_103a:
+//     D[m][n] = sum_k A(m, k) * B(n, k)      (FP32 accumulation in TMEM)
+//
+// One CTA per SM walks a static list of work units (output tile x contraction
+// split).  Roles inside the 256-thread CTA:
+//   warp 0      TMA producer: loads 128x64 A and BNx64 B bf16 tiles (128-byte
+//               swizzle) into a STAGES-deep shared-memory ring;
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer (M=128,
+//               N=BN, K=16 per instruction), accumulating into one of two TMEM
+//               accumulators so the epilogue of a tile overlaps the next tile's
+//               main loop;
+//   warps 4..7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//               32*(w%4)...), BF16 round-to-nearest-even or FP32, 16-byte stores;
+//               for split units, FP32 partial tiles in the workspace and a
+//               last-arriver reduction in ascending split order.
+//
+// Operand "majorness" is a template parameter.  A K-major operand is a row-major
+// [rows][contraction] matrix (one TMA box of 64 contraction elements x rows);
+// an MN-major operand is a row-major [contraction][rows] matrix (boxes of 64
+// rows-direction elements x 64 contraction rows, placed 8 KB apart).  The
+// forward pass uses K-major A and B, the input gradient K-major A and MN-major B,
+// and the weight gradient MN-major A and B (FlashInfer page
+// "perf(cake_dense_projection_det_gemm): plan the 4096 -> 12288 input gradient
+// ...", PR body: "forward (K-major B)" and "input-gradient (MN-major B)" forms;
+// page "... restore the K1 weight-gradient routes ...": wgrad over 64-token K
+// blocks).  Ragged edges come from TMA zero fill on loads and bounds checks on
+// stores, so a partial 64-token block adds exactly its valid tokens.
+//
+// Every barrier wait is bounded (see mbar_wait): on a timeout the kernel records
+// a fault bit, unwinds, waits (bounded) for its own TMA loads and MMAs, and frees
+// its TMEM, so a broken pipeline cannot hang the GPU.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "planner.h"
+#include "ptx.cuh"
+
+namespace dp {
+
+struct GemmArgs {
+  int64_t gm, gn;      // output rows and columns of the contraction view
+  int32_t nkb;         // 64-wide contraction blocks in total
+  int32_t splits;      // contraction splits per tile
+  int32_t tiles_m, tiles_n;
+  int32_t group;       // raster group width, in output-column tiles
+  int32_t units;       // tiles_m * tiles_n * splits
+  void* out;
+  int64_t ldo;         // output leading dimension (elements)
+  int32_t out_f32;     // 1: FP32 output, 0: BF16 output
+  float4* partials;    // split partial tiles: [tile][split][BN/4][128] float4
+  uint32_t* counters;  // split arrival counters, one per tile (self-resetting)
+  uint32_t* fault;     // device status word
+};
+
+template <int BN>
+struct TileCfg {
+  static constexpr int BM = kBlockM;
+  static constexpr int BK = kBlockK;
+  static constexpr int STAGES = stages_for(BN);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full x2, tmem_empty x2, drain
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Work unit u -> (tile row, tile column, split, linear tile, k-block range).
+// Tiles are rastered in groups of `group` output-column tiles, columns fastest,
+// so the CTAs running at one time share A row-blocks and B column-blocks in L2.
+__device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& tm, int& tn, int& s,
+                                            int& tile, int& kb0, int& kb1) {
+  s = u % a.splits;
+  tile = u / a.splits;
+  const int per_group = a.group * a.tiles_m;
+  const int g = tile / per_group;
+  const int first_n = g * a.group;
+  const int width = min(a.group, a.tiles_n - first_n);
+  const int local = tile - g * per_group;
+  tn = first_n + local % width;
+  tm = local / width;
+  kb0 = static_cast<int>(static_cast<int64_t>(s) * a.nkb / a.splits);
+  kb1 = static_cast<int>(static_cast<int64_t>(s + 1) * a.nkb / a.splits);
+}
+
+// Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
+__device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_t col0,
+                                            const float (&v)[32]) {
+  if (m >= a.gm) return;
+  if (a.out_f32) {
+    float* dst = static_cast<float*>(a.out) + m * a.ldo + col0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (col0 + 4 * j < a.gn)
+        *reinterpret_cast<float4*>(dst + 4 * j) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+    uint16_t* dst = static_cast<uint16_t*>(a.out) + m * a.ldo + col0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (col0 + 8 * j < a.gn) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        *reinterpret_cast<uint4*>(dst + 8 * j) = w;
+      }
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(256, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args) {
+  using C = TileCfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t IDESC = idesc_bf16_f32(C::BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte alignment
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar0 = base + STAGES * C::STAGE_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + STAGES * C::STAGE_BYTES + C::NUM_BARS * 8);
+  volatile uint32_t* flag_wait = tmem_slot + 2;  // [2], double-buffered by unit parity
+  volatile uint32_t* flag_last = tmem_slot + 4;  // [2]
+
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+  const int lane = static_cast<int>(threadIdx.x) & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks, for the final drain
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+        int tm, tn, s, tile, kb0, kb1;
+        decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
+            atomicOr(args.fault, kFaultProducerWait);
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t fb = full_bar(stage);
+          mbar_expect_tx(fb, C::STAGE_BYTES);
+          if (A_MN) {
+            tma_load_2d(sa, &tmA, fb, tm * C::BM, kb * C::BK);
+            tma_load_2d(sa + 8192, &tmA, fb, tm * C::BM + 64, kb * C::BK);
+          } else {
+            tma_load_2d(sa, &tmA, fb, kb * C::BK, tm * C::BM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, tn * BN + 64 * j, kb * C::BK);
+          } else {
+            tma_load_2d(sb, &tmB, fb, kb * C::BK, tn * BN);
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load this thread issued has landed before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          if (!mbar_wait(full_bar(s), (issued_phase >> s) & 1u)) atomicOr(args.fault, kFaultDrainWait);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x, ++local) {
+        int tm, tn, s, tile, kb0, kb1;
+        decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
+        const int acc = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u)) {
+          atomicOr(args.fault, kFaultMmaWait);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase)) {
+            atomicOr(args.fault, kFaultMmaWait);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk) {
+            // K-major: step 16 elements (32 bytes) along the swizzled row;
+            // MN-major: step 16 contraction rows (16 x 128 bytes).
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+            mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));  // accumulator complete
+      }
+      // Every MMA this thread issued has finished before TMEM is freed.
+      mma_commit(drain_bar);
+      if (!mbar_wait(drain_bar, 0)) atomicOr(args.fault, kFaultDrainWait);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;          // TMEM sub-partition this warp may read
+    const int row = q * 32 + lane;   // accumulator row == TMEM lane
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const bool leader = threadIdx.x == 128;
+    int local = 0;
+    for (int u = blockIdx.x; u < args.units; u += gridDim.x, ++local) {
+      int tm, tn, s, tile, kb0, kb1;
+      decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
+      const int acc = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      // One thread waits; the outcome reaches the other 127 through a named barrier,
+      // so all of them leave together if the wait gives up.
+      if (leader) {
+        const bool ready = mbar_wait(tfull_bar(acc), aph);
+        if (!ready) atomicOr(args.fault, kFaultEpilogueWait);
+        flag_wait[local & 1] = ready ? 1u : 0u;
+      }
+      named_sync(1, 128);
+      if (flag_wait[local & 1] == 0u) break;
+      tc_fence_after();
+      const int64_t m = static_cast<int64_t>(tm) * C::BM + row;
+      const int64_t n0 = static_cast<int64_t>(tn) * BN;
+      const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
+      if (args.splits == 1) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tcol + c * 32, r);
+          tmem_wait_ld();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));  // accumulator may be reused
+          }
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          store_row32(args, m, n0 + c * 32, v);
+        }
+      } else {
+        // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
+        // 32 rows write 512 contiguous bytes.
+        float4* part = args.partials + (static_cast<size_t>(tile) * args.splits + s) * (C::BM * BN / 4);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tcol + c * 32, r);
+          tmem_wait_ld();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            __stcg(&part[(c * 8 + j) * C::BM + row],
+                   make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+        }
+        __threadfence();
+        named_sync(1, 128);
+        if (leader) {
+          const uint32_t before = atomicAdd(&args.counters[tile], 1u);
+          flag_last[local & 1] = (before == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
+        }
+        named_sync(1, 128);
+        if (flag_last[local & 1]) {
+          // Last split to arrive: sum all partials in ascending split order, round once.
+          __threadfence();
+          const float4* p0 = args.partials + static_cast<size_t>(tile) * args.splits * (C::BM * BN / 4);
+          if (m < args.gm) {
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+              if (n0 + c * 32 >= args.gn) break;
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 x = __ldcg(&p0[(c * 8 + j) * C::BM + row]);
+                v[4 * j] = x.x;
+                v[4 * j + 1] = x.y;
+                v[4 * j + 2] = x.z;
+                v[4 * j + 3] = x.w;
+              }
+#pragma unroll 1
+              for (int sp = 1; sp < args.splits; ++sp) {
+                const float4* ps = p0 + static_cast<size_t>(sp) * (C::BM * BN / 4);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 x = __ldcg(&ps[(c * 8 + j) * C::BM + row]);
+                  v[4 * j] += x.x;
+                  v[4 * j + 1] += x.y;
+                  v[4 * j + 2] += x.z;
+                  v[4 * j + 3] += x.w;
+                }
+              }
+              store_row32(args, m, n0 + c * 32, v);
+            }
+          }
+          if (leader) atomicExch(&args.counters[tile], 0u);  // ready for the next launch
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Host-side launch of one instantiation (defined in the per-view .cu files).
+struct GemmLaunch {
+  CUtensorMap tmA, tmB;
+  GemmArgs args;
+  int grid;
+};
+
+cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
+cudaError_t launch_gemm_km(int bn, const GemmLaunch& l, cudaStream_t stream);  // input gradient
+cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream);  // weight gradient
+// Dynamic shared memory limits of each instantiation, on the current device.
+cudaError_t set_attributes_kk();
+cudaError_t set_attributes_km();
+cudaError_t set_attributes_mm();
+
+template <int BN, bool A_MN, bool B_MN>
+cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
+  gemm_bf16_kernel<BN, A_MN, B_MN><<<l.grid, 256, TileCfg<BN>::SMEM_BYTES, stream>>>(l.tmA, l.tmB, l.args);
+  return cudaGetLastError();
+}
+
+template <int BN, bool A_MN, bool B_MN>
+cudaError_t set_attr_t() {
+  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<BN>::SMEM_BYTES);
+}
+
+}  // namespace dp

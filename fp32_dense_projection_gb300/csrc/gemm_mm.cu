@@ -1,0 +1,27 @@
+// Instantiations of the BF16 GEMM for the weight gradient: MN-major A (dY), MN-major B (X).
+// One translation unit per operand-major combination so the builds run in parallel.
+#include "gemm_kernel.cuh"
+
+namespace dp {
+
+cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream) {
+  switch (bn) {
+    case 64:
+      return launch_gemm_t<64, true, true>(l, stream);
+    case 128:
+      return launch_gemm_t<128, true, true>(l, stream);
+    case 256:
+      return launch_gemm_t<256, true, true>(l, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t set_attributes_mm() {
+  cudaError_t e = set_attr_t<64, true, true>();
+  if (e == cudaSuccess) e = set_attr_t<128, true, true>();
+  if (e == cudaSuccess) e = set_attr_t<256, true, true>();
+  return e;
+}
+
+}  // namespace dp

@@ -1,0 +1,187 @@
+// Per-shape planner (pure host code, no CUDA calls).
+//
+// The pages' deterministic package maps (arch, SM count, shape, T) to a program
+// through a table of measured row rules and keeps "the K split of the row's
+// previous plan (whole K per output tile)" so outputs stay bitwise identical
+// (FlashInfer page "perf(cake_dense_projection_det_gemm): plan the 4096 -> 12288
+// input gradient ...", PR body).  This planner replaces the table with a small
+// analytic cost model over the same decisions: output tile width, the number of
+// contraction splits (1 = whole K per tile), the raster group (16 output-column
+// tiles, as the pages' column-grouped raster), and a persistent grid no larger
+// than the SM count read at run time.
+#include "planner.h"
+
+#include <algorithm>
+
+namespace dp {
+
+namespace {
+
+constexpr double kFlopPerNsPerSm = 12500.0;  // dense BF16 tensor rate per SM
+constexpr double kL2BytesPerNsPerSm = 110.0;  // operand bytes an SM pulls from L2
+constexpr double kHbmBytesPerNs = 6500.0;     // whole-GPU DRAM bandwidth
+constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
+constexpr double kUnitOverheadNs = 600.0;     // prologue / epilogue drain per unit
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+struct View {
+  int64_t gm, gn, gk;
+  bool a_mn, b_mn;
+  int a_elem, b_elem;  // bytes per element as streamed by the GEMM (bf16 = 2)
+};
+
+bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
+  switch (op) {
+    case kOpFwd:  // Y[T,N] = X[T,K] W[N,K]^T : A = X (K-major), B = W (K-major)
+      *v = {T, N, K, false, false, 2, 2};
+      return true;
+    case kOpDgrad:  // dX[T,K] = dY[T,N] W[N,K] : A = dY (K-major), B = W (MN-major)
+      *v = {T, K, N, false, true, 2, 2};
+      return true;
+    case kOpWgrad:  // dW[N,K] = dY[T,N]^T X[T,K] : A = dY (MN-major), B = X (MN-major)
+      *v = {N, K, T, true, true, 2, 2};
+      return true;
+    // Router: the same views with the contraction tripled (hi|hi|lo against hi|lo|hi).
+    case kOpRouterFwd:
+      *v = {T, N, 3 * K, false, false, 2, 2};
+      return true;
+    case kOpRouterDgrad:
+      *v = {T, K, 3 * N, false, true, 2, 2};
+      return true;
+    case kOpRouterWgrad:
+      *v = {N, K, 3 * T, true, true, 2, 2};
+      return true;
+    default:
+      return false;
+  }
+}
+
+// Modelled time (ns) of one plan.  Each unit streams its k-blocks' operand tiles
+// and runs its MMAs; operand bytes come from L2 at a per-SM rate, but no faster in
+// total than the unique bytes can come from DRAM; split units also write and
+// re-read an FP32 partial tile.
+double model_ns(const View& v, int bn, int64_t splits, int sm, int out_bytes) {
+  const int64_t tiles_m = ceil_div(v.gm, kBlockM);
+  const int64_t tiles_n = ceil_div(v.gn, bn);
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, kBlockK));
+  const int64_t units = tiles * splits;
+  const int64_t active = std::min<int64_t>(units, sm);
+  const int64_t waves = ceil_div(units, sm);
+  const int64_t kb = ceil_div(nkb, splits);
+  // only rows/columns inside the matrix cost DRAM bytes; zero-filled boxes do not
+  const double a_rows = static_cast<double>(std::min<int64_t>(kBlockM, v.gm));
+  const double b_rows = static_cast<double>(std::min<int64_t>(bn, v.gn));
+  const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
+  const double flop_per_kb = 2.0 * kBlockM * bn * kBlockK;
+  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm;
+  const double per_sm_bw =
+      std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(active));
+  // L2 reuse: bytes loaded in total versus unique operand bytes
+  const double loaded = static_cast<double>(units) * kb * bytes_per_kb;
+  const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
+  const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
+  const double bw = 1.0 / ((1.0 / reuse) / per_sm_bw + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
+  const double t_load = kb * bytes_per_kb / bw;
+  const double tile_bytes = static_cast<double>(kBlockM) * bn;
+  double t_epi = tile_bytes * out_bytes / per_sm_bw;
+  if (splits > 1) t_epi += tile_bytes * 4.0 * (1.0 + 1.0) / per_sm_bw;  // partial out + last-arriver read share
+  const double t_unit = std::max(t_mma, t_load) + t_epi + kUnitOverheadNs;
+  return static_cast<double>(waves) * t_unit;
+}
+
+}  // namespace
+
+bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, int force_bn,
+               int force_splits) {
+  if (!p || sm < 1 || T < 0 || N < 1 || K < 1) return false;
+  View v;
+  if (!make_view(op, T, N, K, &v)) return false;
+  Plan plan;
+  plan.op = op;
+  plan.T = T;
+  plan.N = N;
+  plan.K = K;
+  plan.out_f32 = (op >= kOpRouterFwd) ? 1 : (out_f32 ? 1 : 0);
+  plan.gm = v.gm;
+  plan.gn = v.gn;
+  plan.gk = v.gk;
+  plan.a_mn = v.a_mn;
+  plan.b_mn = v.b_mn;
+  plan.nkb = ceil_div(v.gk, kBlockK);
+  const int out_bytes = plan.out_f32 ? 4 : 2;
+
+  int best_bn = 256;
+  int64_t best_s = 1;
+  if (v.gm > 0 && plan.nkb > 0) {
+    double best_t = 0.0;
+    bool have = false;
+    for (int bn : {256, 128, 64}) {
+      if (force_bn > 0 && bn != force_bn) continue;
+      if (force_bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
+      const int64_t tiles = ceil_div(v.gm, kBlockM) * ceil_div(v.gn, bn);
+      const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(plan.nkb, 64));
+      for (int64_t s = 1; s <= max_s; ++s) {
+        if (force_splits > 0 && s != std::min<int64_t>(force_splits, plan.nkb)) continue;
+        if (force_splits <= 0 && s > 1 && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
+        const double t = model_ns(v, bn, s, sm, out_bytes);
+        // prefer fewer splits and wider tiles on near-ties (less partial traffic)
+        if (!have || t < best_t * 0.97) {
+          have = true;
+          best_t = t;
+          best_bn = bn;
+          best_s = s;
+        }
+      }
+    }
+    if (!have) return false;
+  }
+  plan.bn = best_bn;
+  plan.splits = static_cast<int>(best_s);
+  plan.stages = stages_for(plan.bn);
+  plan.tiles_m = ceil_div(v.gm, kBlockM);
+  plan.tiles_n = ceil_div(v.gn, plan.bn);
+  plan.units = plan.tiles_m * plan.tiles_n * plan.splits;
+  plan.group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, plan.tiles_n)));
+  plan.grid = static_cast<int>(std::min<int64_t>(plan.units, sm));
+
+  // workspace layout
+  size_t off = 0;
+  const int64_t tiles = plan.tiles_m * plan.tiles_n;
+  if (plan.splits > 1) {
+    plan.off_counters = off;
+    plan.bytes_counters = round_up(static_cast<size_t>(tiles) * sizeof(uint32_t), 256);
+    off += plan.bytes_counters;
+    plan.off_partials = off;
+    plan.bytes_partials = static_cast<size_t>(tiles) * plan.splits * kBlockM * plan.bn * sizeof(float);
+    off += plan.bytes_partials;
+  }
+  if (op >= kOpRouterFwd && v.gm > 0) {
+    // hi/lo bf16 copies of both operands, concatenated along the contraction
+    int64_t a_elems = 0, b_elems = 0;
+    if (op == kOpRouterFwd) {
+      a_elems = T * 3 * K;
+      b_elems = N * 3 * K;
+    } else if (op == kOpRouterDgrad) {
+      a_elems = T * 3 * N;
+      b_elems = 3 * N * K;
+    } else {
+      a_elems = 3 * T * N;
+      b_elems = 3 * T * K;
+    }
+    off = round_up(off, 1024);
+    plan.off_router_a = off;
+    plan.bytes_router_a = static_cast<size_t>(a_elems) * 2;
+    off = round_up(off + plan.bytes_router_a, 1024);
+    plan.off_router_b = off;
+    plan.bytes_router_b = static_cast<size_t>(b_elems) * 2;
+    off += plan.bytes_router_b;
+  }
+  plan.ws_bytes = round_up(off, 256);
+  *p = plan;
+  return true;
+}
+
+}  // namespace dp

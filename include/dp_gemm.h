@@ -1,0 +1,222 @@
+/*
+ * dp_gemm.h -- C ABI of the GB300 (sm_103a) dense projection GEMM library.
+ *
+ * The library computes the projection GEMMs of one training step of a linear
+ * layer Y = X W^T, as described on the FlashInfer pull-request pages about the
+ * "Cake" dense projection GEMM packages:
+ *
+ *   forward          Y[T,N]  = X[T,K] . W[N,K]^T           (K-major B)
+ *   input gradient   dX[T,K] = dY[T,N] . W[N,K]            (MN-major B)
+ *   weight gradient  dW[N,K] = dY[T,N]^T . X[T,K]          (contraction over the
+ *                                                           T tokens, 64-token blocks)
+ *   router           the same three contractions on FP32 operands (hidden H -> 256
+ *                    experts) computed through BF16x3 emulation.
+ *
+ * Page references used below:
+ *   [det-dgrad]  "perf(cake_dense_projection_det_gemm): plan the 4096 -> 12288
+ *                input gradient with the row-half-release program at T-exact keys",
+ *                PR body: forward (K-major B) and input-gradient (MN-major B) forms;
+ *                whole K per output tile keeps outputs bitwise identical.
+ *   [k1-wgrad]   "perf(cake_dense_projection_gemm): restore the K1 weight-gradient
+ *                routes that meet the deterministic package's absolute FP64 budgets",
+ *                PR body: K1 has BF16 or FP32 output; wgrad contracts over 64-token
+ *                K blocks with one or two K splits; the FP64 error budgets.
+ *   [router]     "perf(cake_dense_projection_gemm): cache the router entry points'
+ *                calls by their own tensors", summary: FP32 router [T,H] x [256,H]^T,
+ *                BF16x3 emulation, router_forward / router_dgrad / router_wgrad,
+ *                deterministic=True is the default.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  All matrix pointers are DEVICE pointers on the current CUDA device,
+ *   row-major, 16-byte aligned.  BF16 operands are passed as raw 16-bit patterns
+ *   (`const void*`).  Leading dimensions (`ld*`, in elements) give the distance
+ *   between consecutive rows; 0 means "contiguous" (the row length).  Every
+ *   leading dimension times the element size must be a multiple of 16 bytes, and
+ *   the row lengths N and K must be multiples of 8 (16-byte rows).  An output
+ *   with a padded leading dimension is written only in its first N (or K) columns.
+ * Ownership.  The caller owns every buffer, the workspace and the stream.  The
+ *   library never allocates device memory, never synchronises and never frees.
+ * Workspace.  `workspace` is caller-provided device memory of at least
+ *   dp_workspace_size(...) bytes (may be NULL when that size is 0).  It must be
+ *   zero-filled once before its first use; the library leaves it reusable (the
+ *   split counters it holds reset themselves).  One workspace must not be used by
+ *   two calls that may run concurrently.
+ * Stream.  `stream` is a cudaStream_t (NULL = legacy default stream).  All work
+ *   is enqueued on it; calls return before the GPU finishes.  Calls are legal
+ *   inside CUDA stream capture after the first call on the device (which sets
+ *   kernel attributes; dp_init() does it explicitly).
+ * Determinism.  Every output is bitwise reproducible for the same inputs, shapes,
+ *   strides and SM count: each output tile's contraction is split into a fixed
+ *   partition chosen by a pure planner, and split partials are summed in split
+ *   order.  `deterministic` is accepted for interface parity with the pages'
+ *   entry points; 0 selects the same deterministic programs.
+ * Errors.  Arguments are checked before anything is enqueued; a non-DP_OK status
+ *   means nothing was launched (except DP_ERR_LAUNCH, reported by CUDA after the
+ *   attempt).  No exception crosses the ABI.
+ * Empty input.  T == 0 is legal: forward and input gradient enqueue nothing; the
+ *   weight gradient writes zeros (the sum over an empty token set).
+ */
+#ifndef DP_GEMM_H
+#define DP_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dp_status {
+    DP_OK = 0,
+    DP_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld smaller than the row */
+    DP_ERR_ALIGNMENT = 2,     /* pointer or row stride not 16-byte aligned */
+    DP_ERR_UNSUPPORTED = 3,   /* N or K not a multiple of 8, or a size beyond 2^31-1 */
+    DP_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than dp_workspace_size() */
+    DP_ERR_ARCH = 5,          /* current device is not compute capability 10.3 (sm_103a) */
+    DP_ERR_LAUNCH = 6,        /* a CUDA call failed while enqueueing */
+    DP_ERR_TIMEOUT = 7        /* a kernel gave up waiting on one of its barriers (debug read-out) */
+} dp_status;
+
+typedef enum dp_out_dtype {
+    DP_OUT_BF16 = 0,          /* FP32 accumulator rounded once to bf16, nearest-even */
+    DP_OUT_F32 = 1            /* FP32 accumulator stored as is */
+} dp_out_dtype;
+
+typedef enum dp_op {
+    DP_OP_FWD = 0,
+    DP_OP_DGRAD = 1,
+    DP_OP_WGRAD = 2,
+    DP_OP_ROUTER_FWD = 3,
+    DP_OP_ROUTER_DGRAD = 4,
+    DP_OP_ROUTER_WGRAD = 5
+} dp_op;
+
+/* A cudaStream_t, passed as a plain pointer. */
+typedef void* dp_stream;
+
+/* ------------------------------------------------------------------ BF16 ops */
+
+/* Forward, [det-dgrad] "forward (K-major B) form":
+ *   Y[t][n] = sum_k X[t][k] * W[n][k]
+ * X: T x K bf16 (ldx), W: N x K bf16 (ldw), Y: T x N (ldy) in `out` precision.
+ * FP32 accumulation; rows t >= T are never written. */
+dp_status dp_gemm_fwd(const void* X, const void* W, void* Y,
+                      int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                      void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status dp_gemm_fwd_ex(const void* X, int64_t ldx, const void* W, int64_t ldw,
+                         void* Y, int64_t ldy,
+                         int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                         void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* Input gradient, [det-dgrad] "input-gradient (MN-major B) form":
+ *   dX[t][k] = sum_n dY[t][n] * W[n][k]
+ * dY: T x N bf16 (ldg), W: N x K bf16 (ldw; read with the contraction N as its
+ * outer, MN-major dimension), dX: T x K (ldx) in `out` precision. */
+dp_status dp_gemm_dgrad(const void* dY, const void* W, void* dX,
+                        int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                        void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status dp_gemm_dgrad_ex(const void* dY, int64_t ldg, const void* W, int64_t ldw,
+                           void* dX, int64_t ldx,
+                           int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                           void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* Weight gradient, [k1-wgrad] (contraction over the tokens in 64-token K blocks):
+ *   dW[n][k] = sum_t dY[t][n] * X[t][k]
+ * dY: T x N bf16 (ldg), X: T x K bf16 (ldx), dW: N x K (ldw) in `out` precision.
+ * The token blocks of one output tile are summed by one CTA in order, or, for
+ * thin outputs, split into S contiguous block ranges whose FP32 partials are
+ * added in ascending split order before the single output rounding. */
+dp_status dp_gemm_wgrad(const void* dY, const void* X, void* dW,
+                        int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                        void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status dp_gemm_wgrad_ex(const void* dY, int64_t ldg, const void* X, int64_t ldx,
+                           void* dW, int64_t ldw,
+                           int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                           void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* ----------------------------------------------------------------- router ops */
+/* [router]: FP32 operands and FP32 output; N is the expert count (256 on the
+ * pages) and K the hidden size.  Each FP32 operand value x is split into bf16
+ * hi = RNE(x) and lo = RNE(x - hi); every product a*b is formed as
+ * hi_a*hi_b + hi_a*lo_b + lo_a*hi_b on the BF16 tensor cores with FP32
+ * accumulation (lo_a*lo_b is dropped). */
+
+/* Router forward: Y[t][n] = sum_k X[t][k] * W[n][k];  X: T x K, W: N x K, Y: T x N. */
+dp_status router_fwd(const float* X, const float* W, float* Y,
+                     int64_t T, int64_t N, int64_t K, int deterministic,
+                     void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status router_fwd_ex(const float* X, int64_t ldx, const float* W, int64_t ldw,
+                        float* Y, int64_t ldy, int64_t T, int64_t N, int64_t K, int deterministic,
+                        void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* Router input gradient: dX[t][k] = sum_n dY[t][n] * W[n][k];  dY: T x N, dX: T x K. */
+dp_status router_dgrad(const float* dY, const float* W, float* dX,
+                       int64_t T, int64_t N, int64_t K, int deterministic,
+                       void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status router_dgrad_ex(const float* dY, int64_t ldg, const float* W, int64_t ldw,
+                          float* dX, int64_t ldx, int64_t T, int64_t N, int64_t K, int deterministic,
+                          void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* Router weight gradient: dW[n][k] = sum_t dY[t][n] * X[t][k];  dW: N x K. */
+dp_status router_wgrad(const float* dY, const float* X, float* dW,
+                       int64_t T, int64_t N, int64_t K, int deterministic,
+                       void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t ldx,
+                          float* dW, int64_t ldw, int64_t T, int64_t N, int64_t K, int deterministic,
+                          void* workspace, size_t workspace_bytes, dp_stream stream);
+
+/* ------------------------------------------------------------ planning, misc */
+
+/* The plan the library uses for one call.  The planner is a pure function of
+ * (op, T, N, K, out, sm_count), so a workspace sized here fits the call. */
+typedef struct dp_plan_info {
+    int32_t block_m;          /* output tile rows (128) */
+    int32_t block_n;          /* output tile columns (64, 128 or 256) */
+    int32_t block_k;          /* contraction block (64 elements = 64 tokens for wgrad) */
+    int32_t stages;           /* shared-memory pipeline depth */
+    int32_t splits;           /* contraction splits per output tile (1 = whole K per tile) */
+    int32_t raster_group;     /* output-column tiles per raster group */
+    int32_t grid;             /* persistent CTAs launched (<= sm_count) */
+    int32_t a_mn_major;       /* A operand read MN-major (1) or K-major (0) */
+    int32_t b_mn_major;       /* B operand read MN-major (1) or K-major (0) */
+    int32_t reserved;
+    int64_t gemm_m;           /* output rows of the contraction */
+    int64_t gemm_n;           /* output columns */
+    int64_t gemm_k;           /* contraction length (3x for the router's BF16x3 terms) */
+    int64_t tiles_m;
+    int64_t tiles_n;
+    int64_t k_blocks;         /* ceil(gemm_k / block_k) */
+    int64_t units;            /* tiles_m * tiles_n * splits work units */
+    uint64_t workspace_bytes; /* == dp_workspace_size() */
+} dp_plan_info;
+
+/* Fill `info` with the plan for a call on a GPU with `sm_count` SMs
+ * (sm_count <= 0: query the current device).  Pure host function. */
+dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                        int sm_count, dp_plan_info* info);
+
+/* Workspace bytes a call needs (see dp_plan_query for sm_count). */
+dp_status dp_workspace_size(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                            int sm_count, size_t* bytes);
+
+/* Check the device's architecture and set kernel attributes on `device`
+ * (the current device if < 0).  Optional: the first call on a device does it. */
+dp_status dp_init(int device);
+
+/* Debug read-out: synchronise the current device and report whether any kernel
+ * of this library gave up waiting (DP_ERR_TIMEOUT) since the last clear.
+ * `clear` != 0 resets the flag.  Not for use inside stream capture. */
+dp_status dp_device_error(int clear);
+
+/* Static description of a status code. */
+const char* dp_status_string(dp_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int dp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DP_GEMM_H */

@@ -1,0 +1,148 @@
+"""The C ABI on a host without a GPU: the library builds, loads and exports every
+function include/dp_gemm.h declares; the planner, workspace sizing, status strings
+and argument checks work without touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp32_dense_projection_gb300 as dp
+from fp32_dense_projection_gb300 import build as dpbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dp_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    dpbuild.build()
+    return dp.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def test_header_declares_the_six_ops():
+    names = declared_functions()
+    for n in ("dp_gemm_fwd", "dp_gemm_dgrad", "dp_gemm_wgrad", "router_fwd", "router_dgrad", "router_wgrad",
+              "dp_workspace_size", "dp_plan_query", "dp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 18
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert dp.status_string(s) and "unknown" not in dp.status_string(s)
+    assert "unknown" in dp.status_string(99)
+    assert L.dp_version() >= 100
+
+
+SM = 152
+
+
+@pytest.mark.parametrize("op", list(dp.OP_NAMES))
+@pytest.mark.parametrize("T,N,K", [(64, 1024, 4096), (16384, 12288, 4096), (16231, 12288, 4096),
+                                   (65537, 64, 4096), (1025, 48, 5120), (1024, 256, 4096), (1, 8, 8)])
+def test_plan_is_valid(op, T, N, K):
+    p = dp.plan(op, T, N, K, out_f32=False, sm_count=SM)
+    assert p["block_m"] == 128 and p["block_k"] == 64
+    assert p["block_n"] in (64, 128, 256)
+    assert 1 <= p["grid"] <= SM
+    assert p["grid"] <= p["units"]
+    assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["splits"]
+    assert 1 <= p["splits"] <= max(1, p["k_blocks"])
+    assert p["tiles_m"] * 128 >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
+    assert p["k_blocks"] * 64 >= p["gemm_k"] > (p["k_blocks"] - 1) * 64
+    mult = 3 if op.startswith("router") else 1
+    if op.endswith("wgrad"):
+        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (N, K, mult * T)
+        assert p["a_mn_major"] == 1 and p["b_mn_major"] == 1
+    elif op.endswith("dgrad"):
+        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, K, mult * N)
+        assert p["a_mn_major"] == 0 and p["b_mn_major"] == 1
+    else:
+        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, N, mult * K)
+        assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
+    # pure function: same answer twice, and the workspace query agrees
+    assert dp.plan(op, T, N, K, sm_count=SM) == p
+    assert dp.workspace_size(op, T, N, K, sm_count=SM) == p["workspace_bytes"]
+
+
+def test_split_partition_covers_every_block_once():
+    # The kernel gives split s the k-blocks [floor(s*nb/S), floor((s+1)*nb/S)).
+    for nb in (1, 2, 17, 253, 254, 256, 1025):
+        for S in range(1, min(nb, 40) + 1):
+            bounds = [s * nb // S for s in range(S + 1)]
+            assert bounds[0] == 0 and bounds[-1] == nb
+            assert all(bounds[i + 1] > bounds[i] for i in range(S))  # no empty split while S <= nb
+
+
+def test_wide_projection_keeps_whole_k_per_tile():
+    # The pages' deterministic dgrad keeps whole K per output tile at 4096 -> 12288.
+    for op in ("fwd", "dgrad", "wgrad"):
+        for T in (16384, 16231):
+            p = dp.plan(op, T, 12288, 4096, sm_count=SM)
+            assert p["splits"] == 1, (op, T, p)
+
+
+def test_thin_wgrad_spreads_over_the_sms():
+    for (K, N) in ((4096, 64), (4096, 128), (5120, 48), (5120, 64)):
+        p = dp.plan("wgrad", 65537, N, K, sm_count=SM)
+        assert p["units"] >= SM * 0.6, p
+        assert p["splits"] > 1
+
+
+def test_plan_depends_on_sm_count_only_through_argument():
+    a = dp.plan("wgrad", 65537, 64, 4096, sm_count=148)
+    b = dp.plan("wgrad", 65537, 64, 4096, sm_count=152)
+    assert a["grid"] <= 148 and b["grid"] <= 152
+
+
+def test_empty_tokens_need_no_workspace():
+    for op in dp.OP_NAMES:
+        assert dp.workspace_size(op, 0, 64, 128, sm_count=SM) == 0
+
+
+@pytest.mark.parametrize("T,N,K,want", [(-1, 8, 8, 1), (8, 0, 8, 1), (8, 12, 8, 3), (8, 8, 20, 3),
+                                        (2**31, 8, 8, 3)])
+def test_size_checks(L, T, N, K, want):
+    info = dp.PlanInfo()
+    assert L.dp_plan_query(0, T, N, K, 0, SM, ctypes.byref(info)) == want
+
+
+def test_argument_checks_before_any_device_call(L):
+    P = ctypes.c_void_p
+    good = P(1 << 20)           # never dereferenced: every call below fails its checks first
+    odd = P((1 << 20) + 8)
+    # null operand
+    assert L.dp_gemm_fwd(None, good, good, 64, 64, 64, 0, 1, None, 0, None) == 1
+    # misaligned operand
+    assert L.dp_gemm_fwd(odd, good, good, 64, 64, 64, 0, 1, None, 0, None) == 2
+    # N not a multiple of 8
+    assert L.dp_gemm_dgrad(good, good, good, 64, 60, 64, 0, 1, None, 0, None) == 3
+    # leading dimension shorter than the row
+    assert L.dp_gemm_wgrad_ex(good, 32, good, 64, good, 64, 64, 64, 64, 0, 1, None, 0, None) == 1
+    # leading dimension that breaks the 16-byte row alignment
+    assert L.dp_gemm_fwd_ex(good, 68, good, 64, good, 64, 64, 64, 64, 0, 1, None, 0, None) == 2
+    # bad output dtype
+    assert L.dp_gemm_fwd(good, good, good, 64, 64, 64, 7, 1, None, 0, None) == 1
+    # router rows of fp32 must be 16-byte multiples too (ld 66 floats = 264 B is fine, 65 is not)
+    assert L.router_fwd_ex(good, 65, good, 64, good, 64, 8, 64, 64, 1, None, 0, None) == 2
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(dp, "_lib", None)
+    monkeypatch.setattr(dp, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        dp.lib()

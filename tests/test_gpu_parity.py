@@ -1,0 +1,159 @@
+"""GPU parity: every op through the C ABI against the FP64 oracle.
+
+* exact integer cases (bitwise equal to the oracle), over ragged T and several tiles;
+* the dense projection 4096 -> 1024 at T = 64, ten seeds, BF16 and FP32 output;
+* the FP32 router 4096 -> 256 experts at T in {64, 256, 1024};
+* the wide projection 4096 -> 12288 at T = 16384 and the ragged 16231, sampled;
+* the thin-N weight gradients at odd 64-token block counts, BF16 and FP32 output.
+
+Budgets (FlashInfer page "perf(cake_dense_projection_gemm): restore the K1
+weight-gradient routes ...", PR body): BF16 output atol = rtol = 1e-2 with zero
+violations; FP32 output rel_fro <= 5e-5 and max_abs <= 1e-3 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp32_dense_projection_gb300 as dp
+from fp32_dense_projection_gb300 import inputs
+from gpu_common import (DEV, as_f64, assert_budget, full_ref, gpu, no_device_fault, operands, out_shape,
+                        sample_points, sampled_ref)
+
+pytestmark = pytest.mark.gpu
+
+
+def to_dev(c):
+    return {k: v.to(DEV) for k, v in c.items()}
+
+
+# ------------------------------------------------------------ exact integers
+
+TS = [1, 2, 3, 5, 17, 64, 65, 129]
+NK = [(8, 16), (24, 64), (136, 8), (64, 136), (256, 200)]
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("N,K", NK)
+@pytest.mark.parametrize("T", TS)
+def test_integer_exact(op, T, N, K):
+    # FP32 output: values in [-3, 3] keep every partial sum an exact integer.
+    c = inputs.integer_case(T, N, K, seed=T + N + K)
+    a, b = operands(op, c)
+    ref = full_ref(op, a, b)
+    d = to_dev(c)
+    got = as_f64(gpu(op, *operands(op, d), out_dtype=torch.float32))
+    assert np.array_equal(got, ref), (op, T, N, K, np.abs(got - ref).max())
+    # BF16 output: values in [-1, 1] keep |sums| <= 256, exact in bf16.
+    c = inputs.integer_case(T, N, K, seed=1 + T + N + K, lo=-1, hi=1)
+    a, b = operands(op, c)
+    ref = full_ref(op, a, b)
+    d = to_dev(c)
+    got = as_f64(gpu(op, *operands(op, d), out_dtype=torch.bfloat16))
+    assert np.array_equal(got, ref), (op, T, N, K)
+
+
+@pytest.mark.parametrize("op", ["router_fwd", "router_dgrad", "router_wgrad"])
+@pytest.mark.parametrize("T,N,K", [(1, 8, 8), (17, 16, 72), (65, 256, 128), (129, 24, 264)])
+def test_router_integer_exact(op, T, N, K):
+    # integers are bf16-exact: lo = 0 and the BF16x3 result equals the exact sum
+    c = inputs.integer_case(T, N, K, seed=3 * T + N, dtype=torch.float32)
+    a, b = operands(op, c)
+    ref = full_ref(op, a, b)
+    got = as_f64(gpu(op, *operands(op, to_dev(c))))
+    assert np.array_equal(got, ref), (op, T, N, K)
+
+
+# ------------------------------------------ dense projection 4096 -> 1024, T = 64
+
+@pytest.mark.parametrize("seed", range(10))
+def test_dense_projection_t64(seed):
+    T, N, K = 64, 1024, 4096
+    c = inputs.dense_projection(T, N, K, seed=seed)
+    d = to_dev(c)
+    for op in ("fwd", "dgrad", "wgrad"):
+        ref = full_ref(op, *operands(op, c))
+        for out_dtype, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+            got = as_f64(gpu(op, *operands(op, d), out_dtype=out_dtype))
+            assert_budget(got, ref, name, f"{op} {name} seed {seed}")
+    no_device_fault()
+
+
+# ---------------------------------------------------- FP32 router 4096 -> 256
+
+@pytest.mark.parametrize("T", [64, 256, 1024])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_router(T, seed):
+    K, E = 4096, 256
+    c = inputs.router(T, K, seed=seed, experts=E)
+    d = to_dev(c)
+    for op in ("router_fwd", "router_dgrad", "router_wgrad"):
+        ref = full_ref(op, *operands(op, c))
+        got = as_f64(gpu(op, *operands(op, d)))
+        assert_budget(got, ref, "f32", f"{op} T={T} seed {seed}")
+    no_device_fault()
+
+
+def test_router_other_hidden_sizes():
+    for K in (5120, 6144):
+        c = inputs.router(256, K, seed=5)
+        d = to_dev(c)
+        for op in ("router_fwd", "router_dgrad", "router_wgrad"):
+            ref = full_ref(op, *operands(op, c))
+            assert_budget(as_f64(gpu(op, *operands(op, d))), ref, "f32", f"{op} H={K}")
+
+
+# ------------------------------------------- wide projection 4096 -> 12288
+
+@pytest.fixture(scope="module", params=[16384, 16231])
+def wide(request):
+    T = request.param
+    c = inputs.dense_projection(T, 12288, 4096, seed=0, w_scale=1.0 / 64)
+    return T, c, to_dev(c)
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_wide_projection_sampled(wide, op):
+    T, c, d = wide
+    got = gpu(op, *operands(op, d), out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    shape = tuple(got.shape)
+    rng = np.random.default_rng(T + len(op))
+    rows, cols = sample_points(shape, rng)
+    ref = sampled_ref(op, *operands(op, c), rows, cols)
+    g = got.float()[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
+    assert_budget(g, ref, "bf16", f"{op} T={T}")
+    assert torch.isfinite(got.float()).all()
+    no_device_fault()
+
+
+# ------------------------------------------------ thin-N weight gradient
+
+THIN = [(4096, 64), (4096, 128), (4096, 512), (5120, 48), (5120, 64)]
+
+
+@pytest.mark.parametrize("K,N", THIN)
+def test_thin_wgrad_t1025_full(K, N):
+    T = 1025
+    c = inputs.thin_wgrad(T, N, K, seed=1)
+    ref = full_ref("wgrad", c["dY"], c["X"])
+    d = to_dev(c)
+    for out_dtype, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+        got = as_f64(dp.dp_gemm_wgrad(d["dY"], d["X"], out_dtype=out_dtype))
+        assert_budget(got, ref, name, f"wgrad {K}->{N} T={T} {name}")
+
+
+@pytest.mark.parametrize("T", [16173, 65537])
+@pytest.mark.parametrize("K,N", THIN)
+def test_thin_wgrad_sampled(T, K, N):
+    c = inputs.thin_wgrad(T, N, K, seed=2)
+    d = to_dev(c)
+    rng = np.random.default_rng(T + K + N)
+    rows, cols = sample_points((N, K), rng, n_random=1024, full_rows=1, full_cols=1)
+    ref = sampled_ref("wgrad", c["dY"], c["X"], rows, cols)
+    ri, ci = torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)
+    for out_dtype, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+        got = dp.dp_gemm_wgrad(d["dY"], d["X"], out_dtype=out_dtype)
+        g = got.float()[ri, ci].double().cpu().numpy()
+        assert_budget(g, ref, name, f"wgrad {K}->{N} T={T} {name}")
+        assert torch.isfinite(got.float()).all()
+    no_device_fault()

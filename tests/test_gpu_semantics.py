@@ -1,0 +1,167 @@
+"""GPU behaviour beyond the numbers: bitwise determinism (repeats, CUDA graph
+replay versus eager launch), padded output rows with NaN canaries, operand views
+with padded strides, fresh tensors of the same shape, empty token sets, and the
+status codes of bad calls.
+
+The canary and fresh-tensor cases follow the test practice the FlashInfer pages
+describe for the deterministic package ("plan the 4096 -> 12288 input gradient
+...": write into a column slice of a wider NaN-filled buffer and check that the
+padding stays NaN; "cache the router entry points' calls ...": repeat a call with
+new tensors of the same shape and compare with a fresh reference).
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp32_dense_projection_gb300 as dp
+from fp32_dense_projection_gb300 import inputs
+from gpu_common import DEV, as_f64, assert_budget, full_ref, gpu, no_device_fault, operands
+
+pytestmark = pytest.mark.gpu
+
+CASES = [  # (op, T, N, K): whole-K tiles, split reductions, router
+    ("fwd", 300, 512, 1024),
+    ("dgrad", 300, 512, 1024),
+    ("wgrad", 300, 512, 1024),
+    ("wgrad", 16173, 64, 4096),   # split over tokens
+    ("fwd", 64, 1024, 4096),      # split over K
+    ("router_fwd", 256, 256, 4096),
+    ("router_dgrad", 256, 256, 4096),
+    ("router_wgrad", 1024, 256, 4096),
+]
+
+
+def case_tensors(op, T, N, K, seed=0):
+    if op.startswith("router"):
+        return inputs.router(T, K, seed=seed, experts=N)
+    return inputs.dense_projection(T, N, K, seed=seed)
+
+
+@pytest.mark.parametrize("op,T,N,K", CASES)
+def test_bitwise_repeatable(op, T, N, K):
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K).items()}
+    a, b = operands(op, c)
+    first = gpu(op, a, b, out_dtype=torch.float32)
+    for _ in range(9):
+        again = gpu(op, a, b, out_dtype=torch.float32)
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K", CASES)
+def test_graph_replay_matches_eager(op, T, N, K):
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K).items()}
+    a, b = operands(op, c)
+    kw = {} if op.startswith("router") else {"out_dtype": torch.bfloat16}
+    eager = gpu(op, a, b, **kw)
+    ws = torch.zeros(max(1, dp.workspace_size(op.replace("router_", "router_"), T, N, K,
+                                              out_f32=op.startswith("router"))), dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gpu(op, a, b, out=out, workspace=ws, **kw)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gpu(op, a, b, out=out, workspace=ws, **kw)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        bits = torch.int16 if out.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(out.view(bits), eager.view(bits))
+    no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K", [("fwd", 200, 256, 512), ("dgrad", 200, 256, 512), ("wgrad", 200, 256, 512),
+                                      ("wgrad", 4100, 64, 1024), ("router_fwd", 100, 256, 512),
+                                      ("router_dgrad", 100, 256, 512), ("router_wgrad", 100, 256, 512)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_padded_output_keeps_nan_canary(op, T, N, K, out_dtype):
+    if op.startswith("router"):
+        if out_dtype == torch.bfloat16:
+            pytest.skip("router output is FP32")
+    c = case_tensors(op, T, N, K, seed=3)
+    a, b = operands(op, c)
+    ref = full_ref(op, a, b)
+    R, C = ref.shape
+    pad = 24
+    wide = torch.full((R, C + pad), float("nan"), dtype=out_dtype, device=DEV)
+    view = wide[:, 8:8 + C]  # 8 elements in: keeps 16-byte alignment for both dtypes
+    d = {k: v.to(DEV) for k, v in c.items()}
+    kw = {} if op.startswith("router") else {"out_dtype": out_dtype}
+    gpu(op, *operands(op, d), out=view, **kw)
+    torch.cuda.synchronize()
+    got = as_f64(view)
+    assert_budget(got, ref, "bf16" if out_dtype == torch.bfloat16 else "f32", op)
+    assert torch.isnan(wide[:, :8].float()).all() and torch.isnan(wide[:, 8 + C:].float()).all()
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_padded_operand_strides(op):
+    T, N, K = 150, 128, 320
+    c = inputs.dense_projection(T, N, K, seed=4)
+    ref = full_ref(op, *operands(op, c))
+    # every operand becomes a column slice of a wider buffer
+    d = {}
+    for k, v in c.items():
+        big = torch.zeros(v.shape[0], v.shape[1] + 40, dtype=v.dtype, device=DEV)
+        big[:, 16:16 + v.shape[1]] = v.to(DEV)
+        d[k] = big[:, 16:16 + v.shape[1]]
+    got = as_f64(gpu(op, *operands(op, d), out_dtype=torch.float32))
+    assert_budget(got, ref, "f32", op)
+
+
+def test_fresh_tensors_same_shape():
+    T, N, K = 257, 256, 512
+    for seed in range(3):
+        c = inputs.dense_projection(T, N, K, seed=10 + seed)
+        d = {k: v.to(DEV) for k, v in c.items()}
+        for op in ("fwd", "dgrad", "wgrad"):
+            ref = full_ref(op, *operands(op, c))
+            assert_budget(as_f64(gpu(op, *operands(op, d), out_dtype=torch.float32)), ref, "f32", op)
+
+
+def test_empty_token_set():
+    N, K = 64, 128
+    X = torch.zeros(0, K, dtype=torch.bfloat16, device=DEV)
+    dY = torch.zeros(0, N, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(N, K, device=DEV).to(torch.bfloat16)
+    assert dp.dp_gemm_fwd(X, W).shape == (0, N)
+    assert dp.dp_gemm_dgrad(dY, W).shape == (0, K)
+    dW = torch.full((N, K), float("nan"), device=DEV)
+    dp.dp_gemm_wgrad(dY, X, out=dW, out_dtype=torch.float32)
+    assert torch.equal(dW, torch.zeros_like(dW))
+    Xr = torch.zeros(0, K, device=DEV)
+    dYr = torch.zeros(0, N, device=DEV)
+    dWr = torch.full((N, K), float("nan"), device=DEV)
+    dp.router_wgrad(dYr, Xr, out=dWr)
+    assert torch.equal(dWr, torch.zeros_like(dWr))
+
+
+def test_status_codes():
+    X = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    W = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    # misaligned: a view starting one element in
+    flat = torch.zeros(64 * 128 + 8, dtype=torch.bfloat16, device=DEV)
+    Xm = flat[1:1 + 64 * 128].view(64, 128)
+    with pytest.raises(dp.DPError) as e:
+        dp.dp_gemm_fwd(Xm, W)
+    assert e.value.status == 2
+    # K not a multiple of 8
+    with pytest.raises(dp.DPError) as e:
+        dp.dp_gemm_fwd(X[:, :100], W[:, :100])
+    assert e.value.status in (2, 3)
+    # workspace too small for a split plan
+    need = dp.workspace_size("fwd", 64, 1024, 4096)
+    assert need > 0
+    Xs = torch.randn(64, 4096, device=DEV).to(torch.bfloat16)
+    Ws = torch.randn(1024, 4096, device=DEV).to(torch.bfloat16)
+    small = torch.zeros(need // 2, dtype=torch.uint8, device=DEV)
+    with pytest.raises(dp.DPError) as e:
+        dp.dp_gemm_fwd(Xs, Ws, workspace=small)
+    assert e.value.status == 4
+    no_device_fault()

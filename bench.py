@@ -1,0 +1,434 @@
+"""Benchmark of the dense projection GEMM step on GB300.
+
+One step = forward, input gradient and weight gradient of the 4096 -> 12288
+projection at T = 16384 tokens (BF16 operands, BF16 output, whole K per output
+tile): Y = X W^T, dX = dY W, dW = dY^T X.  The metric is the step's BF16 TFLOP/s
+(3 x 2*T*N*K FLOP) with per-op microseconds and the dominant kernel's fraction of
+the measured dense BF16 peak.
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every step a buffer
+of twice the L2 size is zeroed (cold L2, as in the pages' protocol); CUDA events
+on the launching stream bracket each op, so the flush is not counted.  The timed
+region is bracketed by a barrier and a device synchronize on both sides; the
+reported time is the maximum over ranks.  With several GPUs each rank runs its
+own replica of the workload ("scaling": "weak"); no data crosses ranks.
+
+`--impl reference` times the FP64 CPU oracle (the slow plain definition) on the
+host cores on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BF16 TFLOP/s & % tensor peak, 4096→12288 T=16384 fwd/dgrad/wgrad (µs)"
+UNIT = "TFLOP/s"
+T_TOK, N_OUT, K_IN = 16384, 12288, 4096
+FLOP_OP = 2.0 * T_TOK * N_OUT * K_IN
+WORKLOAD = "wide projection 4096->12288, T=16384, bf16 in/out, fwd+dgrad+wgrad"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+        self.window = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = rows
+        if self.window:
+            t0, t1 = self.window
+            sel = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0]
+            inside = sel or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "samples": len(inside), "reasons": reasons}
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_profile_case(args, local):
+    """A small single-op case for ncu captures: one op, `--profile-T` tokens, a few GB."""
+    import fp32_dense_projection_gb300 as dp
+    from fp32_dense_projection_gb300 import build as dpbuild
+
+    dpbuild.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dp.init(local)
+    op, T = args.profile_op, args.profile_T
+    N, K = (args.profile_N or N_OUT), (args.profile_K or K_IN)
+    g = torch.Generator(device=device)
+    g.manual_seed(7)
+    X = torch.randn(T, K, generator=g, device=device).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device=device) / 64.0).to(torch.bfloat16)
+    dY = torch.randn(T, N, generator=g, device=device).to(torch.bfloat16)
+    a, b = {"fwd": (X, W), "dgrad": (dY, W), "wgrad": (dY, X)}[op]
+    fn = {"fwd": dp.dp_gemm_fwd, "dgrad": dp.dp_gemm_dgrad, "wgrad": dp.dp_gemm_wgrad}[op]
+    out_dtype = torch.float32 if args.profile_f32 else torch.bfloat16
+    out = fn(a, b, out_dtype=out_dtype)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    times = []
+    for _ in range(args.steps):
+        ev[0].record()
+        fn(a, b, out=out, out_dtype=out_dtype)
+        ev[1].record()
+        torch.cuda.synchronize()
+        times.append(ev[0].elapsed_time(ev[1]))
+    assert dp.device_error() == 0
+    flop = 2.0 * T * N * K
+    us = statistics.median(times) * 1e3
+    return {"profile_case": op, "T": T, "N": N, "K": K, "out": "f32" if args.profile_f32 else "bf16",
+            "us": round(us, 2), "tflops": round(flop / us / 1e6, 1), "plan": dp.plan(op, T, N, K, args.profile_f32)}
+
+
+def run_gpu(args, world, rank, local):
+    import fp32_dense_projection_gb300 as dp
+    from fp32_dense_projection_gb300 import build as dpbuild
+
+    dpbuild.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    dp.init(local)
+
+    # synthetic inputs generated on the device (seeded), same recipe shape as the tests
+    g = torch.Generator(device=device)
+    g.manual_seed(1234 + rank)
+    X = torch.randn(T_TOK, K_IN, generator=g, device=device).to(torch.bfloat16)
+    W = (torch.randn(N_OUT, K_IN, generator=g, device=device) / 64.0).to(torch.bfloat16)
+    dY = torch.randn(T_TOK, N_OUT, generator=g, device=device).to(torch.bfloat16)
+    Y = torch.empty(T_TOK, N_OUT, dtype=torch.bfloat16, device=device)
+    dX = torch.empty(T_TOK, K_IN, dtype=torch.bfloat16, device=device)
+    dW = torch.empty(N_OUT, K_IN, dtype=torch.bfloat16, device=device)
+    ws = dp.Workspace(local)
+    need = max(dp.workspace_size(op, T_TOK, N_OUT, K_IN) for op in ("fwd", "dgrad", "wgrad"))
+    wsbuf = ws.get(need)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    plans = {op: dp.plan(op, T_TOK, N_OUT, K_IN) for op in ("fwd", "dgrad", "wgrad")}
+    launches_per_step = 3  # one persistent GEMM launch per op (no split reduction at this size)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dp.dp_gemm_fwd(X, W, out=Y, workspace=wsbuf)
+        if ev is not None:
+            ev[1].record(stream)
+        dp.dp_gemm_dgrad(dY, W, out=dX, workspace=wsbuf)
+        if ev is not None:
+            ev[2].record(stream)
+        dp.dp_gemm_wgrad(dY, X, out=dW, workspace=wsbuf)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert dp.device_error() == 0, "kernel barrier timeout during warm-up"
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    sampler.mark(t0, t1)
+    clocks = sampler.stop()
+    per_op = {"fwd": [], "dgrad": [], "wgrad": []}
+    for ev in events:
+        per_op["fwd"].append(ev[0].elapsed_time(ev[1]))
+        per_op["dgrad"].append(ev[1].elapsed_time(ev[2]))
+        per_op["wgrad"].append(ev[2].elapsed_time(ev[3]))
+    step_ms = [sum(per_op[k][i] for k in per_op) for i in range(args.steps)]
+    ms_per_step = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = 3 * FLOP_OP * world / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the three ops, D2H of the three results, all timed
+    e2e = None
+    e2e_steps = max(1, min(args.steps, 5))
+    hX, hW, hdY = (t.cpu().pin_memory() for t in (X, W, dY))
+    hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
+    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
+
+    def e2e_step():
+        X.copy_(hX, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+        hdX.copy_(dX, non_blocking=True)
+        hdW.copy_(dW, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(3 * FLOP_OP * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps}
+    assert dp.device_error() == 0, "kernel barrier timeout during the timed region"
+
+    peaks, peak_src = load_peaks()
+    op_us = {k: statistics.median(v) * 1e3 for k, v in per_op.items()}
+    dom = max(op_us, key=op_us.get)
+    dom_mean_ms = statistics.mean(per_op[dom])
+    achieved = FLOP_OP / (dom_mean_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = load_traffic(dom)
+    roofline = {"bound": "tensor", "kernel": f"dp_gemm_{dom}", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (burst bf16)"}
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_TOK, "N": N_OUT, "K": K_IN, "out": "bf16",
+                   "l2": "2xL2 buffer zeroed before every step (not timed); inputs also exceed L2",
+                   "parallelism": f"replicas x{world}",
+                   "plans": {k: {kk: plans[k][kk] for kk in ("block_n", "splits", "grid", "units")} for k in plans}},
+        "per_op_us": {k: round(v, 2) for k, v in op_us.items()},
+        "per_op_tflops": {k: round(FLOP_OP / (v * 1e-6) / 1e12, 1) for k, v in op_us.items()},
+        "per_op_frac_of_peak": {k: round(FLOP_OP / (v * 1e-6) / 1e12 / peak, 4) for k, v in op_us.items()},
+        "pages_context": {"dgrad_gb300_t16384_us": 811.6, "note": "pages' own GB300 figure, context only"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(sample_rows=args.cpu_rows)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def load_traffic(op: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    entry = d.get("kernels", {}).get(op)
+    return entry.get("dram_bytes_per_launch") if entry else None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp32_dense_projection_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(rows: int, seed: int = 0):
+    """Time the FP64 oracle on `rows` output rows of each op of the workload."""
+    import numpy as np
+
+    import oracle
+    from fp32_dense_projection_gb300 import inputs
+
+    g = torch.Generator().manual_seed(seed)
+    # only the operand rows the sampled outputs need are drawn in full
+    X = inputs.normal((T_TOK, K_IN), seed, inputs.ROLE_X)
+    W = inputs.normal((N_OUT, K_IN), seed, inputs.ROLE_W, 1.0 / 64)
+    dY = inputs.normal((T_TOK, N_OUT), seed, inputs.ROLE_DY)
+    oracle.build()
+    rng = np.random.default_rng(seed)
+    macs = 0
+    t0 = time.perf_counter()
+    r = rng.integers(0, T_TOK, rows)
+    rr, cc = np.repeat(r, N_OUT), np.tile(np.arange(N_OUT), rows)
+    oracle.fwd_bf16_at(X, W, rr, cc)
+    macs += rr.size * K_IN
+    rr, cc = np.repeat(r, K_IN), np.tile(np.arange(K_IN), rows)
+    oracle.dgrad_bf16_at(dY, W, rr, cc)
+    macs += rr.size * N_OUT
+    rn = rng.integers(0, N_OUT, rows)
+    rr, cc = np.repeat(rn, K_IN), np.tile(np.arange(K_IN), rows)
+    oracle.wgrad_bf16_at(dY, X, rr, cc)
+    macs += rr.size * T_TOK
+    dt = time.perf_counter() - t0
+    del g
+    return 2.0 * macs / dt / 1e12, dt, oracle.num_threads()
+
+
+def cpu_baseline(sample_rows: int) -> dict:
+    tflops, dt, cores = oracle_sample(sample_rows)
+    return {"value": round(tflops, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{sample_rows} output rows of each of fwd/dgrad/wgrad at the full 4096->12288 T=16384 "
+                      f"shapes ({dt:.1f} s of FP64 CPU work)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    rows = max(1, args.cpu_rows // 4)
+    for _ in range(args.warmup):
+        oracle_sample(1, seed=1)
+    vals, times = [], []
+    for i in range(args.steps):
+        v, dt, cores = oracle_sample(rows, seed=2 + i)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    ms_equiv = 3 * FLOP_OP / (value * 1e12) * 1e3
+    sample = f"{rows} output rows of each op per step at the full shapes"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_equiv, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_TOK, "N": N_OUT, "K": K_IN,
+                   "reference": "FP64 CPU oracle (plain definition), no GPU; ms_per_step extrapolated"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": cores,
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-op", choices=["fwd", "dgrad", "wgrad"], default=None,
+                    help="run only a small single-op case (for ncu captures)")
+    ap.add_argument("--profile-T", type=int, default=4096)
+    ap.add_argument("--profile-N", type=int, default=0)
+    ap.add_argument("--profile-K", type=int, default=0)
+    ap.add_argument("--profile-f32", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.profile_op:
+        print(json.dumps(run_profile_case(args, local)), flush=True)
+        return
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        out = run_gpu(args, world, rank, local)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

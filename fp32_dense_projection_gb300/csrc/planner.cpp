@@ -126,6 +126,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
       for (int64_t s = 1; s <= max_s; ++s) {
         if (force_splits > 0 && s != std::min<int64_t>(force_splits, plan.nkb)) continue;
         if (force_splits <= 0 && s > 1 && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
+        if (s > 1 && tiles > kMaxSplitTiles) break;                         // one counter per tile
         const double t = model_ns(v, bn, s, sm, out_bytes);
         // prefer fewer splits and wider tiles on near-ties (less partial traffic)
         if (!have || t < best_t * 0.97) {
@@ -147,18 +148,20 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, plan.tiles_n)));
   plan.grid = static_cast<int>(std::min<int64_t>(plan.units, sm));
 
-  // workspace layout
-  size_t off = 0;
+  // workspace layout: [counters | split partials | router A' | router B']
+  size_t off = kCounterBytes;
   const int64_t tiles = plan.tiles_m * plan.tiles_n;
+  const bool router_copies = op >= kOpRouterFwd && v.gm > 0;
+  if (plan.splits > 1 || router_copies) {
+    plan.off_counters = 0;
+    plan.bytes_counters = kCounterBytes;
+  }
   if (plan.splits > 1) {
-    plan.off_counters = off;
-    plan.bytes_counters = round_up(static_cast<size_t>(tiles) * sizeof(uint32_t), 256);
-    off += plan.bytes_counters;
     plan.off_partials = off;
     plan.bytes_partials = static_cast<size_t>(tiles) * plan.splits * kBlockM * plan.bn * sizeof(float);
     off += plan.bytes_partials;
   }
-  if (op >= kOpRouterFwd && v.gm > 0) {
+  if (router_copies) {
     // hi/lo bf16 copies of both operands, concatenated along the contraction
     int64_t a_elems = 0, b_elems = 0;
     if (op == kOpRouterFwd) {
@@ -179,7 +182,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
     plan.bytes_router_b = static_cast<size_t>(b_elems) * 2;
     off += plan.bytes_router_b;
   }
-  plan.ws_bytes = round_up(off, 256);
+  plan.ws_bytes = (plan.splits > 1 || router_copies) ? round_up(off, 256) : 0;
   *p = plan;
   return true;
 }

@@ -24,6 +24,12 @@ enum Op : int {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
+// The first kCounterBytes of every non-empty workspace hold the split arrival
+// counters (one uint32 per output tile of a split plan).  Nothing else is ever
+// written there, so one zero-filled workspace can serve every op in turn: each
+// split launch returns its counters to zero.
+constexpr int kMaxSplitTiles = 4096;
+constexpr size_t kCounterBytes = kMaxSplitTiles * sizeof(uint32_t);
 
 struct Plan {
   int op = 0;
@@ -35,8 +41,8 @@ struct Plan {
   // tiling
   int bm = kBlockM, bn = 256, bk = kBlockK, stages = 4, splits = 1, group = 16, grid = 0;
   int64_t tiles_m = 0, tiles_n = 0, nkb = 0, units = 0;
-  // workspace layout (byte offsets from the workspace base); counters first so
-  // that a zero-filled workspace starts with zeroed counters
+  // workspace layout (byte offsets from the workspace base): counters first, in
+  // a fixed region of kCounterBytes, then split partials, then router operands
   size_t off_counters = 0, bytes_counters = 0;
   size_t off_partials = 0, bytes_partials = 0;
   size_t off_router_a = 0, bytes_router_a = 0;

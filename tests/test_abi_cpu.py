@@ -146,3 +146,11 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(dp, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         dp.lib()
+
+
+def test_workspace_keeps_a_fixed_counter_region():
+    # every non-empty workspace starts with the 16 KB split-counter region
+    for op in dp.OP_NAMES:
+        for T, N, K in ((64, 1024, 4096), (1024, 256, 4096), (65537, 64, 4096), (16384, 12288, 4096)):
+            n = dp.workspace_size(op, T, N, K, sm_count=SM)
+            assert n == 0 or n >= 16384

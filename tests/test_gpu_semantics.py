@@ -54,7 +54,7 @@ def test_graph_replay_matches_eager(op, T, N, K):
     a, b = operands(op, c)
     kw = {} if op.startswith("router") else {"out_dtype": torch.bfloat16}
     eager = gpu(op, a, b, **kw)
-    ws = torch.zeros(max(1, dp.workspace_size(op.replace("router_", "router_"), T, N, K,
+    ws = torch.zeros(max(1, dp.workspace_size(op, T, N, K,
                                               out_f32=op.startswith("router"))), dtype=torch.uint8, device=DEV)
     out = torch.empty_like(eager)
     s = torch.cuda.Stream()
@@ -164,4 +164,24 @@ def test_status_codes():
     with pytest.raises(dp.DPError) as e:
         dp.dp_gemm_fwd(Xs, Ws, workspace=small)
     assert e.value.status == 4
+    no_device_fault()
+
+
+def test_one_workspace_serves_every_op_in_turn():
+    # Non-split router calls write operand copies into the workspace; split calls keep
+    # arrival counters in its first bytes.  A sequence mixing them on one zeroed
+    # workspace must give the same bits as each call on a fresh workspace.
+    seq = [("router_dgrad", 1024, 256, 4096), ("router_wgrad", 1024, 256, 4096), ("fwd", 64, 1024, 4096),
+           ("router_fwd", 256, 256, 4096), ("wgrad", 16173, 64, 4096), ("router_wgrad", 1024, 256, 4096),
+           ("fwd", 64, 1024, 4096)]
+    need = max(dp.workspace_size(op, T, N, K, out_f32=True) for op, T, N, K in seq)
+    shared = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for i, (op, T, N, K) in enumerate(seq):
+        c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K, seed=i).items()}
+        a, b = operands(op, c)
+        kw = {} if op.startswith("router") else {"out_dtype": torch.float32}
+        got = gpu(op, a, b, workspace=shared, **kw)
+        fresh = torch.zeros(max(1, need), dtype=torch.uint8, device=DEV)
+        want = gpu(op, a, b, workspace=fresh, **kw)
+        assert torch.equal(got.view(torch.int32), want.view(torch.int32)), (i, op)
     no_device_fault()

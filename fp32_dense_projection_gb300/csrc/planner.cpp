@@ -122,10 +122,13 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
       if (force_bn > 0 && bn != force_bn) continue;
       if (force_bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
       const int64_t tiles = ceil_div(v.gm, kBlockM) * ceil_div(v.gn, bn);
-      const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(plan.nkb, 64));
-      for (int64_t s = 1; s <= max_s; ++s) {
+      // bounded accumulation length, unless the tiles are too many to split at all
+      // (then whole K per tile: a longer running sum, the only case without the bound)
+      const int64_t min_s = tiles > kMaxSplitTiles ? 1 : ceil_div(plan.nkb, kMaxAccumBlocks);
+      const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(plan.nkb, 64));
+      for (int64_t s = min_s; s <= max_s; ++s) {
         if (force_splits > 0 && s != std::min<int64_t>(force_splits, plan.nkb)) continue;
-        if (force_splits <= 0 && s > 1 && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
+        if (force_splits <= 0 && s > min_s && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
         if (s > 1 && tiles > kMaxSplitTiles) break;                         // one counter per tile
         const double t = model_ns(v, bn, s, sm, out_bytes);
         // prefer fewer splits and wider tiles on near-ties (less partial traffic)

@@ -29,6 +29,12 @@ constexpr int kBlockK = 64;
 // written there, so one zero-filled workspace can serve every op in turn: each
 // split launch returns its counters to zero.
 constexpr int kMaxSplitTiles = 4096;
+// Longest contraction one TMEM accumulator sums, in 64-wide blocks (16384 tokens).
+// The tensor core rounds each FP32 accumulate toward zero, so the error of a
+// running sum grows with its length; at 32768 tokens per accumulator a BF16
+// output of the 65537-token weight gradient fell outside the pages' budget.
+// Longer contractions are split (fixed partition, partials summed in order).
+constexpr int kMaxAccumBlocks = 256;
 constexpr size_t kCounterBytes = kMaxSplitTiles * sizeof(uint32_t);
 
 struct Plan {

@@ -154,3 +154,14 @@ def test_workspace_keeps_a_fixed_counter_region():
         for T, N, K in ((64, 1024, 4096), (1024, 256, 4096), (65537, 64, 4096), (16384, 12288, 4096)):
             n = dp.workspace_size(op, T, N, K, sm_count=SM)
             assert n == 0 or n >= 16384
+
+
+@pytest.mark.parametrize("op", list(dp.OP_NAMES))
+@pytest.mark.parametrize("T", [1025, 16173, 16384, 65537, 200000])
+def test_accumulation_length_is_bounded(op, T):
+    # no TMEM accumulator sums more than 256 contraction blocks (16384 tokens)
+    for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
+        p = dp.plan(op, T, N, K, sm_count=SM)
+        per_split = -(-p["k_blocks"] // p["splits"])
+        if p["tiles_m"] * p["tiles_n"] <= 4096:  # beyond that no split counters: whole K per tile
+            assert per_split <= 256, (op, T, N, K, p)

@@ -273,3 +273,30 @@ def router_wgrad(dY, X, out=None, deterministic=True, workspace=None, stream=Non
 
 OPS = {"fwd": dp_gemm_fwd, "dgrad": dp_gemm_dgrad, "wgrad": dp_gemm_wgrad,
        "router_fwd": router_fwd, "router_dgrad": router_dgrad, "router_wgrad": router_wgrad}
+
+
+def dp_gemm_wgrad_noalloc(dY, X, out, out_dtype=None, deterministic=True, stream=None):
+    """Weight gradient through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory (a frozen pool during graph
+    capture, a runtime that pre-reserves all memory, a host that forbids cudaMalloc
+    on its hot path): the split scratch lives in a 64 MiB array inside the library.
+    ``out`` must be given (the caller owns every buffer).  Calls on different streams
+    must not overlap: they share the one scratch array.
+    """
+    T, N = dY.shape
+    K = X.shape[1]
+    if X.shape[0] != T or tuple(out.shape) != (N, K):
+        raise ValueError("dp_gemm_wgrad_noalloc: dY[T,N], X[T,K], out[N,K]")
+    if dY.dtype != torch.bfloat16 or X.dtype != torch.bfloat16:
+        raise TypeError("dp_gemm_wgrad_noalloc: operands must be bf16")
+    L = lib()
+    fn = L.dp_gemm_wgrad_noalloc
+    P, I, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    fn.argtypes = [P, I, P, I, P, I, I, I, I, S, S, P]
+    out_f32 = out.dtype == torch.float32
+    with torch.cuda.device(dY.device):
+        status = fn(_ptr(dY), _ld(dY), _ptr(X), _ld(X), _ptr(out), _ld(out), T, N, K,
+                    DP_OUT_F32 if out_f32 else DP_OUT_BF16, int(bool(deterministic)), _stream(dY.device, stream))
+    _check(status, "dp_gemm_wgrad_noalloc")
+    return out

@@ -217,6 +217,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.gn = p.gn;
   a.nkb = static_cast<int32_t>(p.nkb);
   a.splits = p.splits;
+  a.full_units = static_cast<int32_t>(p.full_units);
   a.tiles_m = static_cast<int32_t>(p.tiles_m);
   a.tiles_n = static_cast<int32_t>(p.tiles_n);
   a.group = p.group;
@@ -440,6 +441,7 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
   info->tiles_n = p.tiles_n;
   info->k_blocks = p.nkb;
   info->units = p.units;
+  info->full_units = p.full_units;
   info->workspace_bytes = T == 0 ? 0 : p.ws_bytes;
   return DP_OK;
 }

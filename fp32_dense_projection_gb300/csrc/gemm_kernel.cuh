@@ -44,15 +44,16 @@ namespace dp {
 struct GemmArgs {
   int64_t gm, gn;      // output rows and columns of the contraction view
   int32_t nkb;         // 64-wide contraction blocks in total
-  int32_t splits;      // contraction splits per tile
+  int32_t splits;      // contraction splits of each split tile
+  int32_t full_units;  // units [0, full_units) are whole-K tiles; the rest split `splits` ways
   int32_t tiles_m, tiles_n;
   int32_t group;       // raster group width, in output-column tiles
-  int32_t units;       // tiles_m * tiles_n * splits
+  int32_t units;       // full_units + (tiles - full_units) * splits
   void* out;
   int64_t ldo;         // output leading dimension (elements)
   int32_t out_f32;     // 1: FP32 output, 0: BF16 output
-  float4* partials;    // split partial tiles: [tile][split][BN/4][128] float4
-  uint32_t* counters;  // split arrival counters, one per tile (self-resetting)
+  float4* partials;    // split partial tiles: [split tile][split][BN/4][128] float4
+  uint32_t* counters;  // split arrival counters, one per split tile (self-resetting)
   uint32_t* fault;     // device status word
 };
 
@@ -71,22 +72,51 @@ struct TileCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-// Work unit u -> (tile row, tile column, split, linear tile, k-block range).
-// Tiles are rastered in groups of `group` output-column tiles, columns fastest,
-// so the CTAs running at one time share A row-blocks and B column-blocks in L2.
-__device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& tm, int& tn, int& s,
-                                            int& tile, int& kb0, int& kb1) {
-  s = u % a.splits;
-  tile = u / a.splits;
+// Work unit u -> output tile, contraction range and, for split units, the split
+// index and the split tile's slot in the partial/counter arrays.
+//   u <  full_units: whole-K unit of tile u (all nkb blocks, one accumulator)
+//   u >= full_units: v = u - full_units; tile full_units + v / splits, split v % splits,
+//                    blocks [s*nkb/splits, (s+1)*nkb/splits)
+// A plan either splits every tile (full_units = 0), none (units = full_units), or
+// only the tiles of the last partial wave.  Tiles are rastered in groups of
+// `group` output-column tiles, columns fastest, so the CTAs running at one time
+// share A row-blocks and B column-blocks in L2.
+struct Unit {
+  int tm, tn;    // output tile coordinates
+  int s;         // split index (0 for whole-K units)
+  int ptile;     // slot of a split tile in the partial / counter arrays
+  int kb0, kb1;  // contraction blocks [kb0, kb1)
+  bool split;    // partial result: goes through the ordered reduction
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
+  Unit r;
+  int tile;
+  if (u < a.full_units) {
+    tile = u;
+    r.s = 0;
+    r.ptile = 0;
+    r.kb0 = 0;
+    r.kb1 = a.nkb;
+    r.split = false;
+  } else {
+    const int v = u - a.full_units;
+    const int q = v / a.splits;
+    r.s = v - q * a.splits;
+    r.ptile = q;
+    tile = a.full_units + q;
+    r.kb0 = static_cast<int>(static_cast<int64_t>(r.s) * a.nkb / a.splits);
+    r.kb1 = static_cast<int>(static_cast<int64_t>(r.s + 1) * a.nkb / a.splits);
+    r.split = a.splits > 1;
+  }
   const int per_group = a.group * a.tiles_m;
   const int g = tile / per_group;
   const int first_n = g * a.group;
   const int width = min(a.group, a.tiles_n - first_n);
   const int local = tile - g * per_group;
-  tn = first_n + local % width;
-  tm = local / width;
-  kb0 = static_cast<int>(static_cast<int64_t>(s) * a.nkb / a.splits);
-  kb1 = static_cast<int>(static_cast<int64_t>(s + 1) * a.nkb / a.splits);
+  r.tn = first_n + local % width;
+  r.tm = local / width;
+  return r;
 }
 
 // Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
@@ -172,9 +202,9 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks, for the final drain
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
-        int tm, tn, s, tile, kb0, kb1;
-        decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const Unit w = decode_unit(args, u);
+        const int tm = w.tm, tn = w.tn;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
@@ -217,8 +247,8 @@ __global__ void __launch_bounds__(256, 1)
       int local = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x, ++local) {
-        int tm, tn, s, tile, kb0, kb1;
-        decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
+        const Unit w = decode_unit(args, u);
+        const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u)) {
@@ -265,8 +295,8 @@ __global__ void __launch_bounds__(256, 1)
     const bool leader = threadIdx.x == 128;
     int local = 0;
     for (int u = blockIdx.x; u < args.units; u += gridDim.x, ++local) {
-      int tm, tn, s, tile, kb0, kb1;
-      decode_unit(args, u, tm, tn, s, tile, kb0, kb1);
+      const Unit w = decode_unit(args, u);
+      const int tm = w.tm, tn = w.tn;
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       // One thread waits; the outcome reaches the other 127 through a named barrier,
@@ -282,7 +312,7 @@ __global__ void __launch_bounds__(256, 1)
       const int64_t m = static_cast<int64_t>(tm) * C::BM + row;
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
-      if (args.splits == 1) {
+      if (!w.split) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -301,7 +331,7 @@ __global__ void __launch_bounds__(256, 1)
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
         // 32 rows write 512 contiguous bytes.
-        float4* part = args.partials + (static_cast<size_t>(tile) * args.splits + s) * (C::BM * BN / 4);
+        float4* part = args.partials + (static_cast<size_t>(w.ptile) * args.splits + w.s) * (C::BM * BN / 4);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -321,14 +351,14 @@ __global__ void __launch_bounds__(256, 1)
         __threadfence();
         named_sync(1, 128);
         if (leader) {
-          const uint32_t before = atomicAdd(&args.counters[tile], 1u);
+          const uint32_t before = atomicAdd(&args.counters[w.ptile], 1u);
           flag_last[local & 1] = (before == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
         }
         named_sync(1, 128);
         if (flag_last[local & 1]) {
           // Last split to arrive: sum all partials in ascending split order, round once.
           __threadfence();
-          const float4* p0 = args.partials + static_cast<size_t>(tile) * args.splits * (C::BM * BN / 4);
+          const float4* p0 = args.partials + static_cast<size_t>(w.ptile) * args.splits * (C::BM * BN / 4);
           if (m < args.gm) {
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -357,7 +387,7 @@ __global__ void __launch_bounds__(256, 1)
               store_row32(args, m, n0 + c * 32, v);
             }
           }
-          if (leader) atomicExch(&args.counters[tile], 0u);  // ready for the next launch
+          if (leader) atomicExch(&args.counters[w.ptile], 0u);  // ready for the next launch
         }
       }
     }

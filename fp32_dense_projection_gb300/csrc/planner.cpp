@@ -58,38 +58,46 @@ bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
   }
 }
 
-// Modelled time (ns) of one plan.  Each unit streams its k-blocks' operand tiles
-// and runs its MMAs; operand bytes come from L2 at a per-SM rate, but no faster in
-// total than the unique bytes can come from DRAM; split units also write and
-// re-read an FP32 partial tile.
-double model_ns(const View& v, int bn, int64_t splits, int sm, int out_bytes) {
-  const int64_t tiles_m = ceil_div(v.gm, kBlockM);
-  const int64_t tiles_n = ceil_div(v.gn, bn);
-  const int64_t tiles = tiles_m * tiles_n;
-  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, kBlockK));
-  const int64_t units = tiles * splits;
-  const int64_t active = std::min<int64_t>(units, sm);
-  const int64_t waves = ceil_div(units, sm);
-  const int64_t kb = ceil_div(nkb, splits);
-  // only rows/columns inside the matrix cost DRAM bytes; zero-filled boxes do not
+// Modelled time (ns) of one unit that sums `kb` contraction blocks of a
+// 128 x bn tile.  Operand bytes come from L2 at a per-SM rate, but no faster in
+// total than the unique bytes can come from DRAM with `active` SMs pulling; a
+// split unit also writes and re-reads an FP32 partial tile.
+double unit_ns(const View& v, int bn, int64_t kb, bool split, int64_t active, double reuse, int out_bytes) {
   const double a_rows = static_cast<double>(std::min<int64_t>(kBlockM, v.gm));
   const double b_rows = static_cast<double>(std::min<int64_t>(bn, v.gn));
   const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
   const double flop_per_kb = 2.0 * kBlockM * bn * kBlockK;
   const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm;
   const double per_sm_bw =
-      std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(active));
-  // L2 reuse: bytes loaded in total versus unique operand bytes
-  const double loaded = static_cast<double>(units) * kb * bytes_per_kb;
-  const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
-  const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
+      std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active)));
   const double bw = 1.0 / ((1.0 / reuse) / per_sm_bw + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
   const double t_load = kb * bytes_per_kb / bw;
   const double tile_bytes = static_cast<double>(kBlockM) * bn;
   double t_epi = tile_bytes * out_bytes / per_sm_bw;
-  if (splits > 1) t_epi += tile_bytes * 4.0 * (1.0 + 1.0) / per_sm_bw;  // partial out + last-arriver read share
-  const double t_unit = std::max(t_mma, t_load) + t_epi + kUnitOverheadNs;
-  return static_cast<double>(waves) * t_unit;
+  if (split) t_epi += tile_bytes * 4.0 * 2.0 / per_sm_bw;  // partial out + last-arriver read share
+  return std::max(t_mma, t_load) + t_epi + kUnitOverheadNs;
+}
+
+// Modelled time of a plan: `full` whole-K units followed by (tiles - full) tiles
+// split `splits` ways, run by min(units, sm) persistent CTAs.
+double model_ns(const View& v, int bn, int64_t full, int64_t splits, int sm, int out_bytes) {
+  const int64_t tiles = ceil_div(v.gm, kBlockM) * ceil_div(v.gn, bn);
+  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, kBlockK));
+  const int64_t split_units = (tiles - full) * splits;
+  const int64_t units = full + split_units;
+  const int64_t active = std::min<int64_t>(units, sm);
+  const double bytes_per_kb = (static_cast<double>(std::min<int64_t>(kBlockM, v.gm)) * v.a_elem +
+                               static_cast<double>(std::min<int64_t>(bn, v.gn)) * v.b_elem) *
+                              kBlockK;
+  const double loaded = static_cast<double>(tiles) * nkb * bytes_per_kb;
+  const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
+  const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
+  double t = 0.0;
+  if (full > 0) t += static_cast<double>(ceil_div(full, sm)) * unit_ns(v, bn, nkb, false, active, reuse, out_bytes);
+  if (split_units > 0)  // full is 0 or a whole number of waves when any tile is split
+    t += static_cast<double>(ceil_div(split_units, sm)) *
+         unit_ns(v, bn, ceil_div(nkb, splits), splits > 1, active, reuse, out_bytes);
+  return t;
 }
 
 }  // namespace
@@ -114,10 +122,20 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   const int out_bytes = plan.out_f32 ? 4 : 2;
 
   int best_bn = 256;
-  int64_t best_s = 1;
+  int64_t best_s = 1, best_full = 0;
   if (v.gm > 0 && plan.nkb > 0) {
     double best_t = 0.0;
     bool have = false;
+    auto consider = [&](int bn, int64_t full, int64_t s, double t) {
+      // prefer fewer split units and wider tiles on near-ties (less partial traffic)
+      if (!have || t < best_t * 0.97) {
+        have = true;
+        best_t = t;
+        best_bn = bn;
+        best_s = s;
+        best_full = full;
+      }
+    };
     for (int bn : {256, 128, 64}) {
       if (force_bn > 0 && bn != force_bn) continue;
       if (force_bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
@@ -126,17 +144,20 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
       // (then whole K per tile: a longer running sum, the only case without the bound)
       const int64_t min_s = tiles > kMaxSplitTiles ? 1 : ceil_div(plan.nkb, kMaxAccumBlocks);
       const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(plan.nkb, 64));
+      // every tile split the same way (s = 1: whole K per tile)
       for (int64_t s = min_s; s <= max_s; ++s) {
         if (force_splits > 0 && s != std::min<int64_t>(force_splits, plan.nkb)) continue;
         if (force_splits <= 0 && s > min_s && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
         if (s > 1 && tiles > kMaxSplitTiles) break;                         // one counter per tile
-        const double t = model_ns(v, bn, s, sm, out_bytes);
-        // prefer fewer splits and wider tiles on near-ties (less partial traffic)
-        if (!have || t < best_t * 0.97) {
-          have = true;
-          best_t = t;
-          best_bn = bn;
-          best_s = s;
+        consider(bn, s == 1 ? tiles : 0, s, model_ns(v, bn, s == 1 ? tiles : 0, s, sm, out_bytes));
+      }
+      // whole-K tiles for the full waves, the last partial wave's tiles split
+      if (min_s == 1 && force_splits <= 0 && tiles > sm && tiles % sm != 0) {
+        const int64_t full = tiles / sm * sm;
+        const int64_t tail = tiles - full;
+        if (tail <= kMaxSplitTiles) {
+          for (int64_t s = 2; s <= std::min<int64_t>(plan.nkb, 16); ++s)
+            consider(bn, full, s, model_ns(v, bn, full, s, sm, out_bytes));
         }
       }
     }
@@ -147,7 +168,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.stages = stages_for(plan.bn);
   plan.tiles_m = ceil_div(v.gm, kBlockM);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
-  plan.units = plan.tiles_m * plan.tiles_n * plan.splits;
+  plan.full_units = best_full;
+  plan.units = best_full + (plan.tiles_m * plan.tiles_n - best_full) * plan.splits;
   plan.group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, plan.tiles_n)));
   plan.grid = static_cast<int>(std::min<int64_t>(plan.units, sm));
 
@@ -161,7 +183,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   }
   if (plan.splits > 1) {
     plan.off_partials = off;
-    plan.bytes_partials = static_cast<size_t>(tiles) * plan.splits * kBlockM * plan.bn * sizeof(float);
+    plan.bytes_partials =
+        static_cast<size_t>(tiles - plan.full_units) * plan.splits * kBlockM * plan.bn * sizeof(float);
     off += plan.bytes_partials;
   }
   if (router_copies) {

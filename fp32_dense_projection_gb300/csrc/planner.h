@@ -47,6 +47,9 @@ struct Plan {
   // tiling
   int bm = kBlockM, bn = 256, bk = kBlockK, stages = 4, splits = 1, group = 16, grid = 0;
   int64_t tiles_m = 0, tiles_n = 0, nkb = 0, units = 0;
+  // units [0, full_units) are whole-K tiles; the remaining tiles are split
+  // `splits` ways (all tiles when full_units = 0, the last partial wave otherwise)
+  int64_t full_units = 0;
   // workspace layout (byte offsets from the workspace base): counters first, in
   // a fixed region of kCounterBytes, then split partials, then router operands
   size_t off_counters = 0, bytes_counters = 0;

@@ -209,7 +209,8 @@ typedef struct dp_plan_info {
     int64_t tiles_m;
     int64_t tiles_n;
     int64_t k_blocks;         /* ceil(gemm_k / block_k) */
-    int64_t units;            /* tiles_m * tiles_n * splits work units */
+    int64_t units;            /* full_units + (tiles_m * tiles_n - full_units) * splits */
+    int64_t full_units;       /* leading whole-K units; the remaining tiles are split */
     uint64_t workspace_bytes; /* == dp_workspace_size() */
 } dp_plan_info;
 

@@ -60,7 +60,11 @@ def test_plan_is_valid(op, T, N, K):
     assert p["block_n"] in (64, 128, 256)
     assert 1 <= p["grid"] <= SM
     assert p["grid"] <= p["units"]
-    assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["splits"]
+    tiles = p["tiles_m"] * p["tiles_n"]
+    assert p["units"] == p["full_units"] + (tiles - p["full_units"]) * p["splits"]
+    assert 0 <= p["full_units"] <= tiles
+    # either no tile is split, every tile is, or only the last partial wave's tiles are
+    assert p["full_units"] in (0, tiles) or (p["full_units"] % SM == 0 and tiles - p["full_units"] < SM)
     assert 1 <= p["splits"] <= max(1, p["k_blocks"])
     assert p["tiles_m"] * 128 >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
     assert p["k_blocks"] * 64 >= p["gemm_k"] > (p["k_blocks"] - 1) * 64
@@ -88,12 +92,14 @@ def test_split_partition_covers_every_block_once():
             assert all(bounds[i + 1] > bounds[i] for i in range(S))  # no empty split while S <= nb
 
 
-def test_wide_projection_keeps_whole_k_per_tile():
-    # The pages' deterministic dgrad keeps whole K per output tile at 4096 -> 12288.
+def test_wide_projection_keeps_whole_k_in_full_waves():
+    # The pages' deterministic dgrad keeps whole K per output tile at 4096 -> 12288; here every
+    # tile of the full waves keeps whole K and only the last partial wave may be split.
     for op in ("fwd", "dgrad", "wgrad"):
         for T in (16384, 16231):
             p = dp.plan(op, T, 12288, 4096, sm_count=SM)
-            assert p["splits"] == 1, (op, T, p)
+            tiles = p["tiles_m"] * p["tiles_n"]
+            assert p["full_units"] >= tiles - SM, (op, T, p)
 
 
 def test_thin_wgrad_spreads_over_the_sms():

@@ -157,3 +157,35 @@ def test_thin_wgrad_sampled(T, K, N):
         assert_budget(g, ref, name, f"wgrad {K}->{N} T={T} {name}")
         assert torch.isfinite(got.float()).all()
     no_device_fault()
+
+
+# ------------------------------------- split tail: whole-K full waves + split last wave
+
+TAIL_CASES = [("fwd", 2048, 2560, 2048), ("dgrad", 2048, 2048, 2560), ("wgrad", 4096, 2048, 2560)]
+
+
+@pytest.mark.parametrize("op,T,N,K", TAIL_CASES)
+def test_split_tail_plan(op, T, N, K):
+    p = dp.plan(op, T, N, K)
+    tiles = p["tiles_m"] * p["tiles_n"]
+    if not (0 < p["full_units"] < tiles):
+        pytest.skip(f"plan on this device has no split tail: {p}")
+    c = inputs.dense_projection(T, N, K, seed=8)
+    d = to_dev(c)
+    a, b = operands(op, c)
+    got32 = gpu(op, *operands(op, d), out_dtype=torch.float32)
+    got16 = gpu(op, *operands(op, d), out_dtype=torch.bfloat16)
+    R, C = got32.shape
+    rng = np.random.default_rng(1)
+    # the tail tiles are the last ones in raster order: check the last tile row in full
+    last = np.arange(max(0, R - 128), R)
+    rows = np.concatenate([np.repeat(last, C), rng.integers(0, R, 4096)])
+    cols = np.concatenate([np.tile(np.arange(C), last.size), rng.integers(0, C, 4096)])
+    ref = sampled_ref(op, a, b, rows, cols)
+    ri, ci = torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)
+    assert_budget(got32[ri, ci].double().cpu().numpy(), ref, "f32", f"{op} split tail f32")
+    assert_budget(got16.float()[ri, ci].double().cpu().numpy(), ref, "bf16", f"{op} split tail bf16")
+    for _ in range(3):
+        again = gpu(op, *operands(op, d), out_dtype=torch.float32)
+        assert torch.equal(again.view(torch.int32), got32.view(torch.int32))
+    no_device_fault()

@@ -44,7 +44,7 @@ class DPError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "splits", "raster_group", "grid",
-        "a_mn_major", "b_mn_major", "reserved")] + [(n, ctypes.c_int64) for n in (
+        "a_mn_major", "b_mn_major", "swap_ab", "cta_pair", "raster_rows", "reserved")] + [(n, ctypes.c_int64) for n in (
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
         ("workspace_bytes", ctypes.c_uint64)]
 

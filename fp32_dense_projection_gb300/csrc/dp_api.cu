@@ -175,18 +175,20 @@ int env_int(const char* name) {
   return v ? std::atoi(v) : 0;
 }
 
-// Plan overrides for tuning and tests (DP_FORCE_BN, DP_FORCE_SPLITS); read once.
-void forced(int* bn, int* splits) {
-  static const int f_bn = env_int("DP_FORCE_BN");
-  static const int f_s = env_int("DP_FORCE_SPLITS");
-  *bn = f_bn;
-  *splits = f_s;
-}
-
+// Plan overrides for tuning and tests, read on every call: DP_FORCE_BN,
+// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS (> 0 forces), DP_FORCE_SWAP (0 or 1: the
+// weight-gradient orientation) and DP_FORCE_PAIR (0 or 1: single-CTA or CTA-pair
+// tiles).  Unset in normal use.
 bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan) {
-  int fbn = 0, fs = 0;
-  forced(&fbn, &fs);
-  return make_plan(op, T, N, K, out_f32, sm, plan, fbn, fs);
+  const char* sw = std::getenv("DP_FORCE_SWAP");
+  const char* pr = std::getenv("DP_FORCE_PAIR");
+  Overrides o;
+  o.bn = env_int("DP_FORCE_BN");
+  o.splits = env_int("DP_FORCE_SPLITS");
+  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
+  o.swap = sw ? std::atoi(sw) : -1;
+  o.pair = pr ? std::atoi(pr) : -1;
+  return make_plan(op, T, N, K, out_f32, sm, plan, o);
 }
 
 dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
@@ -210,7 +212,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   std::memset(&l, 0, sizeof(l));
   const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, 64) : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM);
   const bool ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, 64)
-                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, static_cast<uint32_t>(p.bn));
+                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn));
   if (!ok_a || !ok_b) return DP_ERR_LAUNCH;
   GemmArgs& a = l.args;
   a.gm = p.gm;
@@ -221,15 +223,18 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.tiles_m = static_cast<int32_t>(p.tiles_m);
   a.tiles_n = static_cast<int32_t>(p.tiles_n);
   a.group = p.group;
+  a.raster_m = p.raster_m ? 1 : 0;
   a.units = static_cast<int32_t>(p.units);
   a.out = out;
   a.ldo = ldo;
   a.out_f32 = p.out_f32;
+  a.out_trans = p.swap ? 1 : 0;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.counters = p.splits > 1 ? reinterpret_cast<uint32_t*>(w + p.off_counters) : nullptr;
   a.fault = dev.fault;
   l.grid = p.grid;
+  l.pair = p.pair;
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);
@@ -289,7 +294,10 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
   if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes)) return DP_ERR_WORKSPACE;
   if (p.ws_bytes > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
 
-  if (!router) return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
+  if (!router) {
+    if (p.swap) return launch_view(p, *dev, b, ldb, a, lda, out, ldo, ws, stream);  // A = X, B = dY
+    return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
+  }
 
   // Router: split both FP32 operands into (hi, lo) bf16 segments along the
   // contraction axis, then one BF16 GEMM over the tripled contraction.
@@ -434,6 +442,9 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
   info->grid = p.grid;
   info->a_mn_major = p.a_mn ? 1 : 0;
   info->b_mn_major = p.b_mn ? 1 : 0;
+  info->swap_ab = p.swap ? 1 : 0;
+  info->cta_pair = p.pair ? 1 : 0;
+  info->raster_rows = p.raster_m ? 1 : 0;
   info->gemm_m = p.gm;
   info->gemm_n = p.gn;
   info->gemm_k = p.gk;

@@ -47,23 +47,27 @@ struct GemmArgs {
   int32_t splits;      // contraction splits of each split tile
   int32_t full_units;  // units [0, full_units) are whole-K tiles; the rest split `splits` ways
   int32_t tiles_m, tiles_n;
-  int32_t group;       // raster group width, in output-column tiles
+  int32_t group;       // raster group width, in tiles of the grouped raster dimension
+  int32_t raster_m;    // 1: row tiles fastest inside a group (B column blocks shared)
   int32_t units;       // full_units + (tiles - full_units) * splits
   void* out;
   int64_t ldo;         // output leading dimension (elements)
   int32_t out_f32;     // 1: FP32 output, 0: BF16 output
+  int32_t out_trans;   // 1: D[m][n] is stored at out[n * ldo + m] (swapped weight gradient)
   float4* partials;    // split partial tiles: [split tile][split][BN/4][128] float4
   uint32_t* counters;  // split arrival counters, one per split tile (self-resetting)
   uint32_t* fault;     // device status word
 };
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct TileCfg {
-  static constexpr int BM = kBlockM;
+  static constexpr int BM = kBlockM;             // accumulator rows per CTA
+  static constexpr int TM = PAIR ? 2 * BM : BM;  // output tile rows (a CTA pair splits them)
+  static constexpr int BNH = PAIR ? BN / 2 : BN; // B rows each CTA loads
   static constexpr int BK = kBlockK;
-  static constexpr int STAGES = stages_for(BN);
+  static constexpr int STAGES = stages_for(BN, PAIR);
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BNH * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full x2, tmem_empty x2, drain
@@ -79,8 +83,10 @@ struct TileCfg {
 //                    blocks [s*nkb/splits, (s+1)*nkb/splits)
 // A plan either splits every tile (full_units = 0), none (units = full_units), or
 // only the tiles of the last partial wave.  Tiles are rastered in groups of
-// `group` output-column tiles, columns fastest, so the CTAs running at one time
-// share A row-blocks and B column-blocks in L2.
+// `group` tiles along one dimension with that dimension fastest, so the CTAs
+// running at one time share operand blocks in L2: by default groups of output
+// columns (A row-blocks shared); with raster_m, groups of output rows (B
+// column-blocks shared), which the planner picks when B is the larger operand.
 struct Unit {
   int tm, tn;    // output tile coordinates
   int s;         // split index (0 for whole-K units)
@@ -109,13 +115,17 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
     r.kb1 = static_cast<int>(static_cast<int64_t>(r.s + 1) * a.nkb / a.splits);
     r.split = a.splits > 1;
   }
-  const int per_group = a.group * a.tiles_m;
+  const int fast_tiles = a.raster_m ? a.tiles_m : a.tiles_n;  // dimension grouped, fastest
+  const int slow_tiles = a.raster_m ? a.tiles_n : a.tiles_m;
+  const int per_group = a.group * slow_tiles;
   const int g = tile / per_group;
-  const int first_n = g * a.group;
-  const int width = min(a.group, a.tiles_n - first_n);
+  const int first = g * a.group;
+  const int width = min(a.group, fast_tiles - first);
   const int local = tile - g * per_group;
-  r.tn = first_n + local % width;
-  r.tm = local / width;
+  const int fast = first + local % width;
+  const int slow = local / width;
+  r.tm = a.raster_m ? fast : slow;
+  r.tn = a.raster_m ? slow : fast;
   return r;
 }
 
@@ -123,6 +133,20 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
 __device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_t col0,
                                             const float (&v)[32]) {
   if (m >= a.gm) return;
+  if (a.out_trans) {
+    // D[m][n] goes to out[n][m]: the 32 lanes of a warp hold 32 consecutive m, so
+    // each of these stores writes 32 consecutive output elements.
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j >= a.gn) break;
+      const int64_t o = (col0 + j) * a.ldo + m;
+      if (a.out_f32)
+        static_cast<float*>(a.out)[o] = v[j];
+      else
+        static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
+    }
+    return;
+  }
   if (a.out_f32) {
     float* dst = static_cast<float*>(a.out) + m * a.ldo + col0;
 #pragma unroll
@@ -145,13 +169,20 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_
   }
 }
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs args) {
-  using C = TileCfg<BN>;
+  using C = TileCfg<BN, PAIR>;
   constexpr int STAGES = C::STAGES;
-  constexpr uint32_t IDESC = idesc_bf16_f32(C::BM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = idesc_bf16_f32(C::TM, BN, A_MN, B_MN);
+  // With PAIR, a cluster of two CTAs computes one TM x BN tile: rank r loads A rows
+  // [r*128, r*128+128) and B rows [r*BN/2, (r+1)*BN/2) of the tile into the same
+  // shared-memory offsets, the leader (rank 0) issues the 2-CTA MMAs, and rank r's
+  // TMEM receives accumulator rows [r*128, r*128+128).
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int unit_step = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -178,17 +209,25 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // both CTAs' barriers are initialised before either signals the other
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -201,30 +240,38 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks, for the final drain
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x) {
+      for (int u = unit0; ok && u < args.units; u += unit_step) {
         const Unit w = decode_unit(args, u);
-        const int tm = w.tm, tn = w.tn;
+        const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
+        const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
+          if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
             break;
           }
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
-          const uint32_t fb = full_bar(stage);
-          mbar_expect_tx(fb, C::STAGE_BYTES);
+          // a pair's loads all complete on the leader's full barrier
+          const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
+          if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES);
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+            if (PAIR)
+              tma_load_2d_pair(dst, map, fb, x, y);
+            else
+              tma_load_2d(dst, map, fb, x, y);
+          };
           if (A_MN) {
-            tma_load_2d(sa, &tmA, fb, tm * C::BM, kb * C::BK);
-            tma_load_2d(sa + 8192, &tmA, fb, tm * C::BM + 64, kb * C::BK);
+            load(sa, &tmA, a_row0, kb * C::BK);
+            load(sa + 8192, &tmA, a_row0 + 64, kb * C::BK);
           } else {
-            tma_load_2d(sa, &tmA, fb, kb * C::BK, tm * C::BM);
+            load(sa, &tmA, kb * C::BK, a_row0);
           }
           if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, tn * BN + 64 * j, kb * C::BK);
+            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, &tmB, b_row0 + 64 * j, kb * C::BK);
           } else {
-            tma_load_2d(sb, &tmB, fb, kb * C::BK, tn * BN);
+            load(sb, &tmB, kb * C::BK, b_row0);
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -234,31 +281,36 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
       }
-      // Every load this thread issued has landed before the CTA may exit.
+      // Every load this thread issued has landed before the CTA may exit: on the
+      // stage's full barrier, or for a pair (whose loads complete on the leader's
+      // barrier) on the empty barrier the leader's MMAs release after reading it.
       for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u)
-          if (!mbar_wait(full_bar(s), (issued_phase >> s) & 1u)) atomicOr(args.fault, kFaultDrainWait);
+        if ((issued >> s) & 1u) {
+          const uint32_t par = (issued_phase >> s) & 1u;
+          if (!(PAIR ? mbar_wait<true>(empty_bar(s), par) : mbar_wait(full_bar(s), par)))
+            atomicOr(args.fault, kFaultDrainWait);
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < args.units; u += gridDim.x, ++local) {
+      for (int u = unit0; ok && u < args.units; u += unit_step, ++local) {
         const Unit w = decode_unit(args, u);
         const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u)) {
+        if (!mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u)) {
           atomicOr(args.fault, kFaultMmaWait);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase)) {
+          if (!mbar_wait<PAIR>(full_bar(stage), phase)) {
             atomicOr(args.fault, kFaultMmaWait);
             ok = false;
             break;
@@ -272,19 +324,33 @@ __global__ void __launch_bounds__(256, 1)
             // MN-major: step 16 contraction rows (16 x 128 bytes).
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            if (PAIR)
+              mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+            else
+              mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));  // frees the stage once these MMAs have read it
+          // frees the stage (in both CTAs of a pair) once these MMAs have read it
+          if (PAIR)
+            mma_commit_pair_multicast(empty_bar(stage), 0x3);
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));  // accumulator complete
+        // accumulator complete (in both CTAs' TMEM for a pair)
+        if (PAIR)
+          mma_commit_pair_multicast(tfull_bar(acc), 0x3);
+        else
+          mma_commit(tfull_bar(acc));
       }
       // Every MMA this thread issued has finished before TMEM is freed.
-      mma_commit(drain_bar);
+      if (PAIR)
+        mma_commit_pair(drain_bar);
+      else
+        mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) atomicOr(args.fault, kFaultDrainWait);
     }
   } else if (warp >= 4) {
@@ -294,22 +360,35 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const bool leader = threadIdx.x == 128;
     int local = 0;
-    for (int u = blockIdx.x; u < args.units; u += gridDim.x, ++local) {
+    // the epilogue warps (of both CTAs of a pair) release the accumulator on the
+    // leader's barrier
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(map_shared_rank(tempty_bar(a), 0));
+        else
+          mbar_arrive(tempty_bar(a));
+      }
+    };
+    for (int u = unit0; u < args.units; u += unit_step, ++local) {
       const Unit w = decode_unit(args, u);
       const int tm = w.tm, tn = w.tn;
+      const int slot = w.ptile * (PAIR ? 2 : 1) + static_cast<int>(rank);  // this CTA's partial slot
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       // One thread waits; the outcome reaches the other 127 through a named barrier,
       // so all of them leave together if the wait gives up.
       if (leader) {
-        const bool ready = mbar_wait(tfull_bar(acc), aph);
+        const bool ready = mbar_wait<PAIR>(tfull_bar(acc), aph);
         if (!ready) atomicOr(args.fault, kFaultEpilogueWait);
         flag_wait[local & 1] = ready ? 1u : 0u;
       }
       named_sync(1, 128);
       if (flag_wait[local & 1] == 0u) break;
       tc_fence_after();
-      const int64_t m = static_cast<int64_t>(tm) * C::BM + row;
+      const int64_t m = static_cast<int64_t>(tm) * C::TM + static_cast<int64_t>(rank) * C::BM + row;
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
       if (!w.split) {
@@ -318,11 +397,7 @@ __global__ void __launch_bounds__(256, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(tcol + c * 32, r);
           tmem_wait_ld();
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));  // accumulator may be reused
-          }
+          if (c == BN / 32 - 1) release_acc(acc);  // accumulator may be reused
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -331,73 +406,108 @@ __global__ void __launch_bounds__(256, 1)
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
         // 32 rows write 512 contiguous bytes.
-        float4* part = args.partials + (static_cast<size_t>(w.ptile) * args.splits + w.s) * (C::BM * BN / 4);
+        float4* part = args.partials + (static_cast<size_t>(slot) * args.splits + w.s) * (C::BM * BN / 4);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tcol + c * 32, r);
           tmem_wait_ld();
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
-          }
+          if (c == BN / 32 - 1) release_acc(acc);
+          if (m < args.gm) {  // padding rows of a thin tile are never read back
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            __stcg(&part[(c * 8 + j) * C::BM + row],
-                   make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+            for (int j = 0; j < 8; ++j)
+              __stcg(&part[(c * 8 + j) * C::BM + row],
+                     make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+          }
         }
         __threadfence();
         named_sync(1, 128);
         if (leader) {
-          const uint32_t before = atomicAdd(&args.counters[w.ptile], 1u);
+          const uint32_t before = atomicAdd(&args.counters[slot], 1u);
           flag_last[local & 1] = (before == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
         }
         named_sync(1, 128);
         if (flag_last[local & 1]) {
           // Last split to arrive: sum all partials in ascending split order, round once.
           __threadfence();
-          const float4* p0 = args.partials + static_cast<size_t>(w.ptile) * args.splits * (C::BM * BN / 4);
+          const float4* p0 = args.partials + static_cast<size_t>(slot) * args.splits * (C::BM * BN / 4);
           if (m < args.gm) {
+            // Walk (chunk, split) pairs q = c * splits + sp in order, two at a time,
+            // with the next two pairs' loads issued before the current ones are
+            // added: partials of one 32-column chunk are summed in ascending split
+            // order, and four chunk-splits of loads are in flight per thread.
+            const int S = args.splits;
+            int nch = BN / 32;
+            while (nch > 0 && n0 + (nch - 1) * 32 >= args.gn) --nch;
+            const int total = nch * S;
+            const size_t pstride = static_cast<size_t>(C::BM) * BN / 4;
+            float4 cur0[8], cur1[8], nxt0[8], nxt1[8];
+            auto load = [&](float4(&dst)[8], int q) {
+              if (q < total) {
+                const int c = q / S, sp = q - (q / S) * S;
+                const float4* src = p0 + sp * pstride + static_cast<size_t>(c * 8) * C::BM + row;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = __ldcg(src + j * C::BM);
+              }
+            };
+            float v[32];
+            auto consume = [&](const float4(&x)[8], int q) {
+              if (q < total) {
+                const int c = q / S, sp = q - (q / S) * S;
+                if (sp == 0) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    v[4 * j] = x[j].x;
+                    v[4 * j + 1] = x[j].y;
+                    v[4 * j + 2] = x[j].z;
+                    v[4 * j + 3] = x[j].w;
+                  }
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    v[4 * j] += x[j].x;
+                    v[4 * j + 1] += x[j].y;
+                    v[4 * j + 2] += x[j].z;
+                    v[4 * j + 3] += x[j].w;
+                  }
+                }
+                if (sp == S - 1) store_row32(args, m, n0 + c * 32, v);
+              }
+            };
+            load(cur0, 0);
+            load(cur1, 1);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-              if (n0 + c * 32 >= args.gn) break;
-              float v[32];
+            for (int q = 0; q < total; q += 2) {
+              load(nxt0, q + 2);
+              load(nxt1, q + 3);
+              consume(cur0, q);
+              consume(cur1, q + 1);
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float4 x = __ldcg(&p0[(c * 8 + j) * C::BM + row]);
-                v[4 * j] = x.x;
-                v[4 * j + 1] = x.y;
-                v[4 * j + 2] = x.z;
-                v[4 * j + 3] = x.w;
+                cur0[j] = nxt0[j];
+                cur1[j] = nxt1[j];
               }
-#pragma unroll 1
-              for (int sp = 1; sp < args.splits; ++sp) {
-                const float4* ps = p0 + static_cast<size_t>(sp) * (C::BM * BN / 4);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 x = __ldcg(&ps[(c * 8 + j) * C::BM + row]);
-                  v[4 * j] += x.x;
-                  v[4 * j + 1] += x.y;
-                  v[4 * j + 2] += x.z;
-                  v[4 * j + 3] += x.w;
-                }
-              }
-              store_row32(args, m, n0 + c * 32, v);
             }
           }
-          if (leader) atomicExch(&args.counters[w.ptile], 0u);  // ready for the next launch
+          if (leader) atomicExch(&args.counters[slot], 0u);  // ready for the next launch
         }
       }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (PAIR)
+    cluster_sync();  // neither CTA leaves while the leader's MMAs may still use the peer
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -405,7 +515,8 @@ __global__ void __launch_bounds__(256, 1)
 struct GemmLaunch {
   CUtensorMap tmA, tmB;
   GemmArgs args;
-  int grid;
+  int grid;   // CTAs (twice the number of pairs for a paired plan)
+  bool pair;  // clusters of two CTAs share each tile
 };
 
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
@@ -416,16 +527,27 @@ cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();
 cudaError_t set_attributes_mm();
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
-  gemm_bf16_kernel<BN, A_MN, B_MN><<<l.grid, 256, TileCfg<BN>::SMEM_BYTES, stream>>>(l.tmA, l.tmB, l.args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<BN, PAIR>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;  // single-CTA tiles launch without a cluster
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR>, l.tmA, l.tmB, l.args);
 }
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, bool PAIR>
 cudaError_t set_attr_t() {
-  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TileCfg<BN>::SMEM_BYTES);
+  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<BN, PAIR>::SMEM_BYTES);
 }
 
 }  // namespace dp

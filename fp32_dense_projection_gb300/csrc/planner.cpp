@@ -1,14 +1,17 @@
 // Per-shape planner (pure host code, no CUDA calls).
 //
 // The pages' deterministic package maps (arch, SM count, shape, T) to a program
-// through a table of measured row rules and keeps "the K split of the row's
-// previous plan (whole K per output tile)" so outputs stay bitwise identical
-// (FlashInfer page "perf(cake_dense_projection_det_gemm): plan the 4096 -> 12288
-// input gradient ...", PR body).  This planner replaces the table with a small
-// analytic cost model over the same decisions: output tile width, the number of
-// contraction splits (1 = whole K per tile), the raster group (16 output-column
-// tiles, as the pages' column-grouped raster), and a persistent grid no larger
-// than the SM count read at run time.
+// through a table of measured row rules and keeps whole K per output tile so
+// outputs stay bitwise identical (FlashInfer page
+// "perf(cake_dense_projection_det_gemm): plan the 4096 -> 12288 input gradient
+// ...", PR body).  This planner replaces the table with a small analytic cost
+// model over the same decisions: tile shape (one CTA or a CTA pair, output tile
+// width), the contraction split (whole K per tile, every tile split, or only the
+// last partial wave's tiles), the weight gradient's orientation, the raster order
+// (groups of 16 tiles, as the pages' column-grouped raster) and a persistent grid
+// no larger than the SM count read at run time.  The plan is a pure function of
+// its arguments, so every launch of a shape partitions every tile's contraction
+// the same way.
 #include "planner.h"
 
 #include <algorithm>
@@ -17,11 +20,14 @@ namespace dp {
 
 namespace {
 
-constexpr double kFlopPerNsPerSm = 12500.0;  // dense BF16 tensor rate per SM
-constexpr double kL2BytesPerNsPerSm = 110.0;  // operand bytes an SM pulls from L2
-constexpr double kHbmBytesPerNs = 6500.0;     // whole-GPU DRAM bandwidth
+// Rates calibrated on GB300 measurements of this kernel (cold L2).
+constexpr double kFlopPerNsPerSm = 12500.0;   // dense BF16 tensor rate per SM
+constexpr double kL2BytesPerNsPerSm = 160.0;  // operand bytes an SM pulls when they hit in L2
+constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
-constexpr double kUnitOverheadNs = 600.0;     // prologue / epilogue drain per unit
+constexpr double kReduceBytesPerNs = 50.0;    // last-arriver read of the split partials (one SM)
+constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
+constexpr bool kAutoPair = false;             // CTA-pair tiles chosen automatically (else only when forced)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -58,52 +64,120 @@ bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
   }
 }
 
-// Modelled time (ns) of one unit that sums `kb` contraction blocks of a
-// 128 x bn tile.  Operand bytes come from L2 at a per-SM rate, but no faster in
-// total than the unique bytes can come from DRAM with `active` SMs pulling; a
-// split unit also writes and re-reads an FP32 partial tile.
-double unit_ns(const View& v, int bn, int64_t kb, bool split, int64_t active, double reuse, int out_bytes) {
+// A tiling: tile = rows x bn, rows = 128 (one CTA) or 256 (a CTA pair).
+struct Tiling {
+  int bn;
+  bool pair;
+  int64_t rows() const { return pair ? 2 * kBlockM : kBlockM; }
+};
+
+// Modelled time (ns) of one unit that sums `kb` contraction blocks of a tile,
+// per SM.  Operand bytes come at a rate between the per-SM DRAM share and the L2
+// rate, weighted by how often the plan re-reads each operand byte (`reuse`); the
+// output or the FP32 partial is written at the per-SM DRAM share.
+double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t active_sms, double reuse,
+               int out_bytes) {
   const double a_rows = static_cast<double>(std::min<int64_t>(kBlockM, v.gm));
-  const double b_rows = static_cast<double>(std::min<int64_t>(bn, v.gn));
+  const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn)) / (t.pair ? 2.0 : 1.0);
   const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
-  const double flop_per_kb = 2.0 * kBlockM * bn * kBlockK;
-  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm;
-  const double per_sm_bw =
-      std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active)));
-  const double bw = 1.0 / ((1.0 / reuse) / per_sm_bw + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
+  const double flop_per_kb = 2.0 * kBlockM * t.bn * kBlockK;  // per SM
+  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0);
+  const double dram =
+      std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
+  const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
   const double t_load = kb * bytes_per_kb / bw;
-  const double tile_bytes = static_cast<double>(kBlockM) * bn;
-  double t_epi = tile_bytes * out_bytes / per_sm_bw;
-  if (split) t_epi += tile_bytes * 4.0 * 2.0 / per_sm_bw;  // partial out + last-arriver read share
-  return std::max(t_mma, t_load) + t_epi + kUnitOverheadNs;
+  const double out_tile = a_rows * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * (split ? 4.0 : out_bytes);
+  return std::max(t_mma, t_load) + out_tile / dram;
 }
 
 // Modelled time of a plan: `full` whole-K units followed by (tiles - full) tiles
-// split `splits` ways, run by min(units, sm) persistent CTAs.
-double model_ns(const View& v, int bn, int64_t full, int64_t splits, int sm, int out_bytes) {
-  const int64_t tiles = ceil_div(v.gm, kBlockM) * ceil_div(v.gn, bn);
+// split `splits` ways, run by min(units, slots) persistent CTAs (or pairs); never
+// faster than the unique operand bytes cross from DRAM; split tiles end with one
+// CTA per (half) tile reading all of its partials.
+double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes) {
+  const int64_t slots = t.pair ? sm / 2 : sm;
+  const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
   const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, kBlockK));
   const int64_t split_units = (tiles - full) * splits;
   const int64_t units = full + split_units;
-  const int64_t active = std::min<int64_t>(units, sm);
-  const double bytes_per_kb = (static_cast<double>(std::min<int64_t>(kBlockM, v.gm)) * v.a_elem +
-                               static_cast<double>(std::min<int64_t>(bn, v.gn)) * v.b_elem) *
-                              kBlockK;
-  const double loaded = static_cast<double>(tiles) * nkb * bytes_per_kb;
+  const int64_t active_sms = std::min<int64_t>(units, slots) * (t.pair ? 2 : 1);
+  const double a_rows = static_cast<double>(std::min<int64_t>(t.rows(), v.gm));
+  const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn));
+  const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
   const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
   const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
-  double t = 0.0;
-  if (full > 0) t += static_cast<double>(ceil_div(full, sm)) * unit_ns(v, bn, nkb, false, active, reuse, out_bytes);
+  double time = 0.0;
+  if (full > 0)
+    time += static_cast<double>(ceil_div(full, slots)) * unit_ns(v, t, nkb, false, active_sms, reuse, out_bytes);
   if (split_units > 0)  // full is 0 or a whole number of waves when any tile is split
-    t += static_cast<double>(ceil_div(split_units, sm)) *
-         unit_ns(v, bn, ceil_div(nkb, splits), splits > 1, active, reuse, out_bytes);
-  return t;
+    time += static_cast<double>(ceil_div(split_units, slots)) *
+            unit_ns(v, t, ceil_div(nkb, splits), splits > 1, active_sms, reuse, out_bytes);
+  const double t_dram = (unique + static_cast<double>(v.gm) * v.gn * out_bytes) / kHbmBytesPerNs;
+  time = std::max(time, t_dram);
+  if (splits > 1 && split_units > 0)
+    time += splits * std::min<double>(kBlockM, a_rows) * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0 /
+            kReduceBytesPerNs;
+  return time;
+}
+
+struct Choice {
+  bool have = false;
+  double t = 0.0;
+  Tiling tiling = {256, false};
+  int64_t splits = 1, full = 0;
+};
+
+// Best (tiling, split count, whole-K prefix) for one contraction view.
+void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& o, Choice* best) {
+  auto consider = [&](const Tiling& t, int64_t full, int64_t s, double time) {
+    // prefer earlier candidates (single CTA, wider tiles, fewer splits) on near-ties
+    if (!best->have || time < best->t * 0.99) {
+      best->have = true;
+      best->t = time;
+      best->tiling = t;
+      best->splits = s;
+      best->full = full;
+    }
+  };
+  for (int pair = 0; pair < 2; ++pair) {
+    if (o.pair >= 0 && pair != o.pair) continue;
+    if (pair && !kAutoPair && o.pair != 1) continue;
+    if (pair && (sm < 2 || v.gm <= kBlockM)) continue;  // a pair needs two row blocks of work
+    const int64_t slots = pair ? sm / 2 : sm;
+    for (int bn : {256, 128, 64}) {
+      if (pair && bn < 128) continue;  // each CTA of a pair holds bn / 2 >= 64 columns of B
+      if (o.bn > 0 && bn != o.bn) continue;
+      if (o.bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
+      const Tiling t = {bn, pair != 0};
+      const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, bn);
+      const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // counters / partial slots: one per CTA tile
+      // bounded accumulation length, unless the tiles are too many to split at all
+      // (then whole K per tile: a longer running sum, the only case without the bound)
+      const int64_t min_s = cta_tiles > kMaxSplitTiles ? 1 : ceil_div(nkb, kMaxAccumBlocks);
+      const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(nkb, 64));
+      // every tile split the same way (s = 1: whole K per tile)
+      for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0; ++s) {
+        if (o.splits > 0 && s != std::min<int64_t>(o.splits, nkb)) continue;
+        if (o.splits <= 0 && s > min_s && tiles * s > 4LL * slots) break;  // beyond 4 waves never pays
+        if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // one counter per CTA tile
+        consider(t, s == 1 ? tiles : 0, s, model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes));
+      }
+      // whole-K tiles for the full waves, the last partial wave's tiles split
+      if (min_s == 1 && o.splits <= 0 && tiles > slots && tiles % slots != 0) {
+        const int64_t full = tiles / slots * slots;
+        if ((tiles - full) * (pair ? 2 : 1) <= kMaxSplitTiles) {
+          for (int64_t s = 2; s <= std::min<int64_t>(nkb, 16); ++s)
+            if (o.tail_splits <= 0 || s == o.tail_splits)
+              consider(t, full, s, model_ns(v, t, full, s, sm, out_bytes));
+        }
+      }
+    }
+  }
 }
 
 }  // namespace
 
-bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, int force_bn,
-               int force_splits) {
+bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, const Overrides& o) {
   if (!p || sm < 1 || T < 0 || N < 1 || K < 1) return false;
   View v;
   if (!make_view(op, T, N, K, &v)) return false;
@@ -113,78 +187,62 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.N = N;
   plan.K = K;
   plan.out_f32 = (op >= kOpRouterFwd) ? 1 : (out_f32 ? 1 : 0);
-  plan.gm = v.gm;
-  plan.gn = v.gn;
-  plan.gk = v.gk;
   plan.a_mn = v.a_mn;
   plan.b_mn = v.b_mn;
   plan.nkb = ceil_div(v.gk, kBlockK);
   const int out_bytes = plan.out_f32 ? 4 : 2;
 
-  int best_bn = 256;
-  int64_t best_s = 1, best_full = 0;
+  Choice c;
+  c.have = true;  // empty problems: any tiling, no work units
   if (v.gm > 0 && plan.nkb > 0) {
-    double best_t = 0.0;
-    bool have = false;
-    auto consider = [&](int bn, int64_t full, int64_t s, double t) {
-      // prefer fewer split units and wider tiles on near-ties (less partial traffic)
-      if (!have || t < best_t * 0.97) {
-        have = true;
-        best_t = t;
-        best_bn = bn;
-        best_s = s;
-        best_full = full;
-      }
-    };
-    for (int bn : {256, 128, 64}) {
-      if (force_bn > 0 && bn != force_bn) continue;
-      if (force_bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
-      const int64_t tiles = ceil_div(v.gm, kBlockM) * ceil_div(v.gn, bn);
-      // bounded accumulation length, unless the tiles are too many to split at all
-      // (then whole K per tile: a longer running sum, the only case without the bound)
-      const int64_t min_s = tiles > kMaxSplitTiles ? 1 : ceil_div(plan.nkb, kMaxAccumBlocks);
-      const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(plan.nkb, 64));
-      // every tile split the same way (s = 1: whole K per tile)
-      for (int64_t s = min_s; s <= max_s; ++s) {
-        if (force_splits > 0 && s != std::min<int64_t>(force_splits, plan.nkb)) continue;
-        if (force_splits <= 0 && s > min_s && tiles * s > 4LL * sm) break;  // splitting beyond 4 waves never pays
-        if (s > 1 && tiles > kMaxSplitTiles) break;                         // one counter per tile
-        consider(bn, s == 1 ? tiles : 0, s, model_ns(v, bn, s == 1 ? tiles : 0, s, sm, out_bytes));
-      }
-      // whole-K tiles for the full waves, the last partial wave's tiles split
-      if (min_s == 1 && force_splits <= 0 && tiles > sm && tiles % sm != 0) {
-        const int64_t full = tiles / sm * sm;
-        const int64_t tail = tiles - full;
-        if (tail <= kMaxSplitTiles) {
-          for (int64_t s = 2; s <= std::min<int64_t>(plan.nkb, 16); ++s)
-            consider(bn, full, s, model_ns(v, bn, full, s, sm, out_bytes));
-        }
+    c.have = false;
+    if (o.swap != 1) search(v, plan.nkb, sm, out_bytes, o, &c);
+    if (op == kOpWgrad && o.swap != 0) {
+      // thin outputs: let K fill the 128-row tile side and N be the MMA's N
+      const View sv = {K, N, T, true, true, 2, 2};
+      Choice cs;
+      search(sv, plan.nkb, sm, out_bytes, o, &cs);
+      if (cs.have && (!c.have || cs.t < c.t * 0.97 || o.swap == 1)) {
+        c = cs;
+        plan.swap = true;
+        v = sv;
       }
     }
-    if (!have) return false;
+    if (!c.have) return false;
   }
-  plan.bn = best_bn;
-  plan.splits = static_cast<int>(best_s);
-  plan.stages = stages_for(plan.bn);
-  plan.tiles_m = ceil_div(v.gm, kBlockM);
+  plan.gm = v.gm;
+  plan.gn = v.gn;
+  plan.gk = v.gk;
+  plan.pair = c.tiling.pair;
+  plan.bm = static_cast<int>(c.tiling.rows());
+  plan.bn = c.tiling.bn;
+  plan.splits = static_cast<int>(c.splits);
+  plan.stages = stages_for(plan.bn, plan.pair);
+  plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
-  plan.full_units = best_full;
-  plan.units = best_full + (plan.tiles_m * plan.tiles_n - best_full) * plan.splits;
-  plan.group = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, plan.tiles_n)));
-  plan.grid = static_cast<int>(std::min<int64_t>(plan.units, sm));
+  const int64_t tiles = plan.tiles_m * plan.tiles_n;
+  plan.full_units = (v.gm > 0 && plan.nkb > 0) ? c.full : tiles;
+  plan.units = plan.full_units + (tiles - plan.full_units) * plan.splits;
+  // Group along the dimension whose operand is larger, so the tiles that share
+  // its blocks run in the same wave and it crosses from DRAM about once.
+  plan.raster_m = v.gn > v.gm;
+  plan.group = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(16, plan.raster_m ? plan.tiles_m : plan.tiles_n)));
+  const int64_t slots = plan.pair ? sm / 2 : sm;
+  plan.grid = static_cast<int>(std::min<int64_t>(plan.units, slots) * (plan.pair ? 2 : 1));
 
   // workspace layout: [counters | split partials | router A' | router B']
   size_t off = kCounterBytes;
-  const int64_t tiles = plan.tiles_m * plan.tiles_n;
   const bool router_copies = op >= kOpRouterFwd && v.gm > 0;
   if (plan.splits > 1 || router_copies) {
     plan.off_counters = 0;
     plan.bytes_counters = kCounterBytes;
   }
   if (plan.splits > 1) {
+    // one FP32 partial per split of every split tile, per CTA of the tile
     plan.off_partials = off;
-    plan.bytes_partials =
-        static_cast<size_t>(tiles - plan.full_units) * plan.splits * kBlockM * plan.bn * sizeof(float);
+    plan.bytes_partials = static_cast<size_t>(tiles - plan.full_units) * (plan.pair ? 2 : 1) * plan.splits *
+                          kBlockM * plan.bn * sizeof(float);
     off += plan.bytes_partials;
   }
   if (router_copies) {

@@ -44,6 +44,11 @@ struct Plan {
   // contraction view
   int64_t gm = 0, gn = 0, gk = 0;
   bool a_mn = false, b_mn = false;
+  // weight gradient computed as D[k][n] = sum_t X[t][k] dY[t][n] (A = X, B = dY) and
+  // stored transposed into dW[n][k]: thin N becomes the MMA's N, K fills the tile rows
+  bool swap = false;
+  bool raster_m = false;  // raster groups of row tiles, rows fastest (B is the larger operand)
+  bool pair = false;      // tiles of 256 rows computed by a cluster of two CTAs (bm = 256)
   // tiling
   int bm = kBlockM, bn = 256, bk = kBlockK, stages = 4, splits = 1, group = 16, grid = 0;
   int64_t tiles_m = 0, tiles_n = 0, nkb = 0, units = 0;
@@ -59,18 +64,31 @@ struct Plan {
   size_t ws_bytes = 0;
 };
 
-// Shared-memory pipeline depth for a tile width: as many 128 x 64 + bn x 64 bf16
-// stages as fit in 192 KB (4 for bn = 256, 6 for 128, 8 for 64).
-constexpr int stages_for(int bn) {
-  return (192 * 1024) / (kBlockM * kBlockK * 2 + bn * kBlockK * 2) < 8
-             ? (192 * 1024) / (kBlockM * kBlockK * 2 + bn * kBlockK * 2)
+// Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows
+// x 64 B tile (bf16) as fit in 192 KB, at most 8.  b_rows is the tile width, or
+// half of it when a CTA pair shares the tile (each CTA holds half of B).
+constexpr int stages_for_rows(int b_rows) {
+  return (192 * 1024) / (kBlockM * kBlockK * 2 + b_rows * kBlockK * 2) < 8
+             ? (192 * 1024) / (kBlockM * kBlockK * 2 + b_rows * kBlockK * 2)
              : 8;
 }
+constexpr int stages_for(int bn, bool pair = false) { return stages_for_rows(pair ? bn / 2 : bn); }
+
+// Overrides of the planner's choices, for tests and tuning (all unset in normal
+// use): > 0 forces the tile width / uniform split count / last-wave split count;
+// >= 0 forces the weight-gradient orientation (swap) or single-CTA (0) versus
+// CTA-pair (1) tiles.
+struct Overrides {
+  int bn = 0;
+  int splits = 0;
+  int tail_splits = 0;
+  int swap = -1;
+  int pair = -1;
+};
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,
-// sm_count < 1, unknown op).  `force_bn` / `force_splits` > 0 override the
-// planner's choice (used by tests and tuning).
+// sm_count < 1, unknown op, or overrides that admit no plan).
 bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm_count, Plan* plan,
-               int force_bn = 0, int force_splits = 0);
+               const Overrides& overrides = Overrides());
 
 }  // namespace dp

@@ -193,15 +193,19 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
 /* The plan the library uses for one call.  The planner is a pure function of
  * (op, T, N, K, out, sm_count), so a workspace sized here fits the call. */
 typedef struct dp_plan_info {
-    int32_t block_m;          /* output tile rows (128) */
+    int32_t block_m;          /* output tile rows (128, or 256 for a CTA pair) */
     int32_t block_n;          /* output tile columns (64, 128 or 256) */
     int32_t block_k;          /* contraction block (64 elements = 64 tokens for wgrad) */
     int32_t stages;           /* shared-memory pipeline depth */
     int32_t splits;           /* contraction splits per output tile (1 = whole K per tile) */
-    int32_t raster_group;     /* output-column tiles per raster group */
-    int32_t grid;             /* persistent CTAs launched (<= sm_count) */
+    int32_t raster_group;     /* tiles per raster group (columns, or rows if raster_rows) */
+    int32_t grid;             /* persistent CTAs launched (<= sm_count; even for a pair) */
     int32_t a_mn_major;       /* A operand read MN-major (1) or K-major (0) */
     int32_t b_mn_major;       /* B operand read MN-major (1) or K-major (0) */
+    int32_t swap_ab;          /* weight gradient as dW^T = X^T dY (thin N as the MMA's N),
+                                 stored transposed into dW */
+    int32_t cta_pair;         /* 1: tiles of 256 rows shared by a cluster of two CTAs */
+    int32_t raster_rows;      /* 1: raster groups of row tiles, rows fastest */
     int32_t reserved;
     int64_t gemm_m;           /* output rows of the contraction */
     int64_t gemm_n;           /* output columns */

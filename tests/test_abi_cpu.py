@@ -56,21 +56,27 @@ SM = 152
                                    (65537, 64, 4096), (1025, 48, 5120), (1024, 256, 4096), (1, 8, 8)])
 def test_plan_is_valid(op, T, N, K):
     p = dp.plan(op, T, N, K, out_f32=False, sm_count=SM)
-    assert p["block_m"] == 128 and p["block_k"] == 64
-    assert p["block_n"] in (64, 128, 256)
-    assert 1 <= p["grid"] <= SM
-    assert p["grid"] <= p["units"]
+    pair = bool(p["cta_pair"])
+    assert p["block_m"] == (256 if pair else 128) and p["block_k"] == 64
+    assert p["block_n"] in ((128, 256) if pair else (64, 128, 256))
+    slots = SM // 2 if pair else SM
+    ctas_per_tile = 2 if pair else 1
+    assert 1 <= p["grid"] <= SM and p["grid"] % ctas_per_tile == 0
+    assert p["grid"] // ctas_per_tile <= p["units"]
     tiles = p["tiles_m"] * p["tiles_n"]
     assert p["units"] == p["full_units"] + (tiles - p["full_units"]) * p["splits"]
     assert 0 <= p["full_units"] <= tiles
     # either no tile is split, every tile is, or only the last partial wave's tiles are
-    assert p["full_units"] in (0, tiles) or (p["full_units"] % SM == 0 and tiles - p["full_units"] < SM)
+    assert p["full_units"] in (0, tiles) or (p["full_units"] % slots == 0 and tiles - p["full_units"] < slots)
     assert 1 <= p["splits"] <= max(1, p["k_blocks"])
-    assert p["tiles_m"] * 128 >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
+    assert p["tiles_m"] * p["block_m"] >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
     assert p["k_blocks"] * 64 >= p["gemm_k"] > (p["k_blocks"] - 1) * 64
     mult = 3 if op.startswith("router") else 1
     if op.endswith("wgrad"):
-        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (N, K, mult * T)
+        if p["swap_ab"]:
+            assert op == "wgrad" and (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (K, N, T)
+        else:
+            assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (N, K, mult * T)
         assert p["a_mn_major"] == 1 and p["b_mn_major"] == 1
     elif op.endswith("dgrad"):
         assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, K, mult * N)
@@ -99,7 +105,8 @@ def test_wide_projection_keeps_whole_k_in_full_waves():
         for T in (16384, 16231):
             p = dp.plan(op, T, 12288, 4096, sm_count=SM)
             tiles = p["tiles_m"] * p["tiles_n"]
-            assert p["full_units"] >= tiles - SM, (op, T, p)
+            slots = SM // 2 if p["cta_pair"] else SM
+            assert p["full_units"] >= tiles - slots, (op, T, p)
 
 
 def test_thin_wgrad_spreads_over_the_sms():
@@ -113,6 +120,37 @@ def test_plan_depends_on_sm_count_only_through_argument():
     a = dp.plan("wgrad", 65537, 64, 4096, sm_count=148)
     b = dp.plan("wgrad", 65537, 64, 4096, sm_count=152)
     assert a["grid"] <= 148 and b["grid"] <= 152
+    for sm in (2, 3, 148, 152):  # odd SM counts still give whole CTA pairs
+        p = dp.plan("fwd", 16384, 12288, 4096, sm_count=sm)
+        assert p["grid"] <= sm and (not p["cta_pair"] or p["grid"] % 2 == 0)
+
+
+def test_plan_overrides_are_read_per_call(monkeypatch):
+    monkeypatch.setenv("DP_FORCE_SWAP", "1")
+    assert dp.plan("wgrad", 16173, 64, 4096, sm_count=SM)["swap_ab"] == 1
+    monkeypatch.setenv("DP_FORCE_SWAP", "0")
+    assert dp.plan("wgrad", 16173, 64, 4096, sm_count=SM)["swap_ab"] == 0
+    monkeypatch.setenv("DP_FORCE_PAIR", "0")
+    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["cta_pair"] == 0
+    monkeypatch.setenv("DP_FORCE_PAIR", "1")
+    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["cta_pair"] == 1
+    for sm in (2, 3, 148, 152):  # odd SM counts still give whole CTA pairs
+        p = dp.plan("fwd", 16384, 12288, 4096, sm_count=sm)
+        assert p["grid"] <= sm and p["grid"] % 2 == 0
+    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["cta_pair"] == 1
+
+
+def test_raster_groups_the_larger_operand():
+    # thin wgrad 4096 -> 512 not swapped: B (X, 4096 columns) is larger than A (dY, 512):
+    # row tiles fastest, so the row tiles sharing an X column block run together
+    import os
+    os.environ["DP_FORCE_SWAP"] = "0"
+    try:
+        p = dp.plan("wgrad", 65537, 512, 4096, sm_count=SM)
+    finally:
+        del os.environ["DP_FORCE_SWAP"]
+    assert p["raster_rows"] == 1
+    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["raster_rows"] == 0
 
 
 def test_empty_tokens_need_no_workspace():
@@ -169,5 +207,5 @@ def test_accumulation_length_is_bounded(op, T):
     for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
         p = dp.plan(op, T, N, K, sm_count=SM)
         per_split = -(-p["k_blocks"] // p["splits"])
-        if p["tiles_m"] * p["tiles_n"] <= 4096:  # beyond that no split counters: whole K per tile
+        if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else no counters: whole K
             assert per_split <= 256, (op, T, N, K, p)

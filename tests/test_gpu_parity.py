@@ -189,3 +189,69 @@ def test_split_tail_plan(op, T, N, K):
         again = gpu(op, *operands(op, d), out_dtype=torch.float32)
         assert torch.equal(again.view(torch.int32), got32.view(torch.int32))
     no_device_fault()
+
+
+@pytest.mark.parametrize("swap", [0, 1])
+@pytest.mark.parametrize("T,K,N", [(1025, 4096, 64), (1025, 5120, 48), (4100, 4096, 128), (300, 1024, 200)])
+def test_thin_wgrad_both_orientations(monkeypatch, swap, T, K, N):
+    # dW = dY^T X (tile rows over N) and dW^T = X^T dY stored transposed (tile rows over K)
+    monkeypatch.setenv("DP_FORCE_SWAP", str(swap))
+    p = dp.plan("wgrad", T, N, K)
+    assert p["swap_ab"] == swap
+    c = inputs.thin_wgrad(T, N, K, seed=4)
+    ref = full_ref("wgrad", c["dY"], c["X"])
+    d = to_dev(c)
+    for out_dtype, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+        wide = torch.full((N, K + 16), float("nan"), dtype=out_dtype, device=DEV)
+        view = wide[:, 8:8 + K]
+        dp.dp_gemm_wgrad(d["dY"], d["X"], out=view, out_dtype=out_dtype)
+        assert_budget(as_f64(view), ref, name, f"wgrad swap={swap} {K}->{N} T={T} {name}")
+        assert torch.isnan(wide[:, :8].float()).all() and torch.isnan(wide[:, 8 + K:].float()).all()
+    no_device_fault()
+
+
+# --------------------------------- CTA-pair tiles (256 rows over a cluster of two CTAs)
+
+PAIR_SHAPES = [("fwd", 257, 256, 192), ("fwd", 600, 384, 512), ("dgrad", 300, 136, 256), ("dgrad", 513, 512, 384),
+               ("wgrad", 129, 264, 512), ("wgrad", 1000, 512, 256)]
+
+
+@pytest.mark.parametrize("op,T,N,K", PAIR_SHAPES)
+@pytest.mark.parametrize("bn", [128, 256])
+def test_pair_integer_exact(monkeypatch, op, T, N, K, bn):
+    monkeypatch.setenv("DP_FORCE_PAIR", "1")
+    monkeypatch.setenv("DP_FORCE_BN", str(bn))
+    monkeypatch.setenv("DP_FORCE_SWAP", "0")
+    p = dp.plan(op, T, N, K)
+    if not p["cta_pair"]:
+        pytest.skip(f"no pair plan for this shape: {p}")
+    c = inputs.integer_case(T, N, K, seed=T + N + K + bn)
+    ref = full_ref(op, *operands(op, c))
+    got = as_f64(gpu(op, *operands(op, to_dev(c)), out_dtype=torch.float32))
+    assert np.array_equal(got, ref), (op, T, N, K, bn, p)
+    no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K,tail", [("fwd", 2048, 2560, 2048, 2), ("dgrad", 2048, 2048, 2560, 3),
+                                           ("wgrad", 4096, 2048, 2560, 0), ("wgrad", 16173, 512, 1024, 0)])
+def test_pair_split_plans(monkeypatch, op, T, N, K, tail):
+    # pairs with split tails or split-everything plans: ordered reduction per CTA half
+    monkeypatch.setenv("DP_FORCE_PAIR", "1")
+    if tail:
+        monkeypatch.setenv("DP_FORCE_TAIL_SPLITS", str(tail))
+    p = dp.plan(op, T, N, K)
+    assert p["cta_pair"] and p["splits"] > 1, p
+    c = inputs.dense_projection(T, N, K, seed=9)
+    d = to_dev(c)
+    got = gpu(op, *operands(op, d), out_dtype=torch.float32)
+    R, C = got.shape
+    rng = np.random.default_rng(3)
+    last = np.arange(max(0, R - 256), R)
+    rows = np.concatenate([np.repeat(last, C), rng.integers(0, R, 4096)])
+    cols = np.concatenate([np.tile(np.arange(C), last.size), rng.integers(0, C, 4096)])
+    ref = sampled_ref(op, *operands(op, c), rows, cols)
+    ri, ci = torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)
+    assert_budget(got[ri, ci].double().cpu().numpy(), ref, "f32", f"pair {op} {p}")
+    again = gpu(op, *operands(op, d), out_dtype=torch.float32)
+    assert torch.equal(again.view(torch.int32), got.view(torch.int32))
+    no_device_fault()

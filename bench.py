@@ -53,6 +53,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(value: float) -> float:
+    """The largest `value` over all ranks (the slowest rank sets a step's time)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(ms_per_step: float, world: int, flop_per_rank_step: float) -> float:
+    """Whole-job throughput: every rank's FLOP over the slowest rank's step time."""
+    return flop_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -231,12 +247,8 @@ def run_gpu(args, world, rank, local):
         per_op["dgrad"].append(ev[1].elapsed_time(ev[2]))
         per_op["wgrad"].append(ev[2].elapsed_time(ev[3]))
     step_ms = [sum(per_op[k][i] for k in per_op) for i in range(args.steps)]
-    ms_per_step = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = 3 * FLOP_OP * world / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(statistics.mean(step_ms))
+    value = job_tflops(ms_per_step, world, 3 * FLOP_OP)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, the three ops, D2H of the three results, all timed
@@ -266,12 +278,8 @@ def run_gpu(args, world, rank, local):
         e2e_step()
     eb.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(3 * FLOP_OP * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+    e2e_ms = max_over_ranks(ea.elapsed_time(eb) / e2e_steps)
+    e2e = {"value": round(job_tflops(e2e_ms, world, 3 * FLOP_OP), 2), "unit": UNIT,
            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": e2e_steps}
     assert dp.device_error() == 0, "kernel barrier timeout during the timed region"

@@ -27,7 +27,7 @@ constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceBytesPerNs = 50.0;    // last-arriver read of the split partials (one SM)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
-constexpr bool kAutoPair = false;             // CTA-pair tiles chosen automatically (else only when forced)
+constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }

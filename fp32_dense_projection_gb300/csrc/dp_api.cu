@@ -94,65 +94,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 map over a row-major [rows][cols] matrix (leading dimension ld elements),
-// box = box_rows x 64 columns, 128-byte swizzle, zero fill outside the matrix.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+// Map over a row-major [rows][cols] matrix (leading dimension ld elements) of bf16
+// (box = box_rows x 64 columns) or FP32 (box = box_rows x 32 columns): 128-byte
+// box rows, 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+              bool f32 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (f32 ? 4 : 2)};
+  const cuuint32_t box[2] = {f32 ? 32u : 64u, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// ------------------------------------------------------------ router split
-
-// BF16x3 operand split.  For each FP32 value x: hi = RNE(x), lo = RNE(x - hi)
-// (x - hi is exact in FP32).  Writes three bf16 segments of an R x C source,
-// either side by side (dst is R x 3C) or stacked (dst is 3R x C); bit i of
-// lo_mask selects lo for segment i.  The A operand uses (hi, hi, lo) and the B
-// operand (hi, lo, hi), so the contraction over the tripled axis is
-// sum hi*hi + hi*lo + lo*hi (FlashInfer page "perf(cake_dense_projection_gemm):
-// cache the router entry points' calls by their own tensors": FP32 router GEMM
-// through BF16x3 emulation).
-__global__ void __launch_bounds__(256) split_bf16x3_kernel(const float* __restrict__ src, int64_t R, int64_t C,
-                                                           int64_t lds, uint16_t* __restrict__ dst,
-                                                           int stacked, int lo_mask) {
-  const int64_t quads = C / 4;
-  const int64_t total = R * quads;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t r = i / quads;
-    const int64_t c = (i - r * quads) * 4;
-    const float4 x = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
-    const uint32_t h01 = pack_bf16x2(x.x, x.y);
-    const uint32_t h23 = pack_bf16x2(x.z, x.w);
-    const float hx = __uint_as_float(h01 << 16), hy = __uint_as_float(h01 & 0xFFFF0000u);
-    const float hz = __uint_as_float(h23 << 16), hw = __uint_as_float(h23 & 0xFFFF0000u);
-    const uint2 hi = make_uint2(h01, h23);
-    const uint2 lo = make_uint2(pack_bf16x2(x.x - hx, x.y - hy), pack_bf16x2(x.z - hz, x.w - hw));
-#pragma unroll
-    for (int seg = 0; seg < 3; ++seg) {
-      const uint2 v = ((lo_mask >> seg) & 1) ? lo : hi;
-      uint16_t* d = stacked ? dst + (seg * R + r) * C + c : dst + r * (3 * C) + seg * C + c;
-      *reinterpret_cast<uint2*>(d) = v;
-    }
-  }
-}
-
-cudaError_t launch_split(const float* src, int64_t R, int64_t C, int64_t lds, uint16_t* dst, bool stacked,
-                         int lo_mask, int sm, cudaStream_t stream) {
-  const int64_t total = R * (C / 4);
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sm) * 8;
-  if (blocks > cap) blocks = cap;
-  split_bf16x3_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, R, C, lds, dst, stacked ? 1 : 0,
-                                                                         lo_mask);
-  return cudaGetLastError();
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------ argument checks
@@ -195,8 +150,8 @@ dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
   if (T < 0 || N < 1 || K < 1) return DP_ERR_INVALID_ARG;
   if (N % 8 != 0 || K % 8 != 0) return DP_ERR_UNSUPPORTED;
   const int64_t lim = 0x7FFFFFFF;
-  const int64_t mult = op >= kOpRouterFwd ? 3 : 1;  // the router triples the contraction axis
-  if (T * mult > lim || N * mult > lim || K * mult > lim) return DP_ERR_UNSUPPORTED;
+  (void)op;
+  if (T > lim || N > lim || K > lim) return DP_ERR_UNSUPPORTED;
   return DP_OK;
 }
 
@@ -210,9 +165,15 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
     return DP_ERR_UNSUPPORTED;
   GemmLaunch l;
   std::memset(&l, 0, sizeof(l));
-  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, 64) : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM);
-  const bool ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, 64)
-                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn));
+  // Boxes: K-major operands one box of bk contraction columns x tile rows; MN-major
+  // operands boxes of 64 (bf16) or 32 (FP32) tile columns x bk contraction rows.
+  const bool f32 = p.op >= kOpRouterFwd;  // FP32 operands, split into bf16 hi/lo in the kernel
+  const uint32_t kb_rows = static_cast<uint32_t>(p.bk);
+  const uint32_t b_rows = static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn);
+  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, f32)
+                           : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, f32);
+  const bool ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, f32)
+                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows, f32);
   if (!ok_a || !ok_b) return DP_ERR_LAUNCH;
   GemmArgs& a = l.args;
   a.gm = p.gm;
@@ -235,6 +196,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.fault = dev.fault;
   l.grid = p.grid;
   l.pair = p.pair;
+  l.x3 = f32;
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);
@@ -299,38 +261,9 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
     return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
   }
 
-  // Router: split both FP32 operands into (hi, lo) bf16 segments along the
-  // contraction axis, then one BF16 GEMM over the tripled contraction.
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  uint16_t* a3 = reinterpret_cast<uint16_t*>(w + p.off_router_a);
-  uint16_t* b3 = reinterpret_cast<uint16_t*>(w + p.off_router_b);
-  const float* af = static_cast<const float*>(a);
-  const float* bf = static_cast<const float*>(b);
-  constexpr int kHiHiLo = 0b100, kHiLoHi = 0b010;
-  cudaError_t e = cudaSuccess;
-  int64_t ld3a = 0, ld3b = 0;
-  switch (op) {
-    case kOpRouterFwd:  // A' = X [T][3K], B' = W [N][3K]
-      e = launch_split(af, T, K, lda, a3, false, kHiHiLo, dev->sm_count, stream);
-      if (e == cudaSuccess) e = launch_split(bf, N, K, ldb, b3, false, kHiLoHi, dev->sm_count, stream);
-      ld3a = 3 * K;
-      ld3b = 3 * K;
-      break;
-    case kOpRouterDgrad:  // A' = dY [T][3N], B' = W stacked [3N][K]
-      e = launch_split(af, T, N, lda, a3, false, kHiHiLo, dev->sm_count, stream);
-      if (e == cudaSuccess) e = launch_split(bf, N, K, ldb, b3, true, kHiLoHi, dev->sm_count, stream);
-      ld3a = 3 * N;
-      ld3b = K;
-      break;
-    default:  // A' = dY stacked [3T][N], B' = X stacked [3T][K]
-      e = launch_split(af, T, N, lda, a3, true, kHiHiLo, dev->sm_count, stream);
-      if (e == cudaSuccess) e = launch_split(bf, T, K, ldb, b3, true, kHiLoHi, dev->sm_count, stream);
-      ld3a = N;
-      ld3b = K;
-      break;
-  }
-  if (e != cudaSuccess) return DP_ERR_LAUNCH;
-  return launch_view(p, *dev, a3, ld3a, b3, ld3b, out, ldo, ws, stream);
+  // Router: the FP32 operands go to the fused BF16x3 mode, which splits each
+  // 32-wide block into bf16 hi/lo in shared memory.
+  return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
 }
 
 }  // namespace

@@ -59,21 +59,33 @@ struct GemmArgs {
   uint32_t* fault;     // device status word
 };
 
-template <int BN, bool PAIR = false>
+// X3: the FP32 router's fused BF16x3 mode.  A stage then holds the bf16 hi and lo
+// halves of a 32-wide contraction block of each operand ([A_hi | A_lo | B_hi | B_lo]),
+// written by converter warps from an FP32 staging tile that TMA loads into a
+// second ring of the same size.
+template <int BN, bool PAIR = false, bool X3 = false>
 struct TileCfg {
+  static_assert(!(PAIR && X3), "the fused BF16x3 mode uses single-CTA tiles");
   static constexpr int BM = kBlockM;             // accumulator rows per CTA
   static constexpr int TM = PAIR ? 2 * BM : BM;  // output tile rows (a CTA pair splits them)
   static constexpr int BNH = PAIR ? BN / 2 : BN; // B rows each CTA loads
-  static constexpr int BK = kBlockK;
-  static constexpr int STAGES = stages_for(BN, PAIR);
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BNH * BK * 2;
+  static constexpr int BK = X3 ? kRouterBlockK : kBlockK;
+  static constexpr int STAGES = X3 ? stages_x3(BN) : stages_for(BN, PAIR);
+  static constexpr int A_HALF = BM * BK * 2;     // one bf16 copy of the A tile
+  static constexpr int B_HALF = BNH * BK * 2;
+  static constexpr int A_BYTES = X3 ? 2 * A_HALF : A_HALF;
+  static constexpr int B_BYTES = X3 ? 2 * B_HALF : B_HALF;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // FP32 staging of A (X3)
+  static constexpr int SB_BYTES = X3 ? BNH * BK * 4 : 0;
+  static constexpr int SSTAGE_BYTES = SA_BYTES + SB_BYTES;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full x2, tmem_empty x2, drain
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 64;
+  // full, empty, tmem_full x2, tmem_empty x2, drain (+ staging full / empty for X3)
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + (X3 ? 2 * STAGES : 0);
+  static constexpr int SMEM_BYTES = 1024 + STAGES * (STAGE_BYTES + SSTAGE_BYTES) + NUM_BARS * 8 + 64;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(STAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "swizzle alignment");
 };
 
 // Work unit u -> output tile, contraction range and, for split units, the split
@@ -169,11 +181,11 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmArgs args) {
-  using C = TileCfg<BN, PAIR>;
+  using C = TileCfg<BN, PAIR, X3>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(C::TM, BN, A_MN, B_MN);
   // With PAIR, a cluster of two CTAs computes one TM x BN tile: rank r loads A rows
@@ -188,8 +200,10 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte alignment
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bar0 = base + STAGES * C::STAGE_BYTES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + STAGES * C::STAGE_BYTES + C::NUM_BARS * 8);
+  const uint32_t sbase = base + STAGES * C::STAGE_BYTES;  // FP32 staging ring (X3)
+  const uint32_t bar0 = sbase + STAGES * C::SSTAGE_BYTES;
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(base_ptr + STAGES * (C::STAGE_BYTES + C::SSTAGE_BYTES) + C::NUM_BARS * 8);
   volatile uint32_t* flag_wait = tmem_slot + 2;  // [2], double-buffered by unit parity
   volatile uint32_t* flag_last = tmem_slot + 4;  // [2]
 
@@ -198,14 +212,20 @@ __global__ void __launch_bounds__(256, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };            // X3 staging landed
+  auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + STAGES + s); };  // X3 staging read
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(threadIdx.x) & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), X3 ? 2 : 1);  // X3: one arrival per converter warp
       mbar_init(empty_bar(s), 1);
+      if (X3) {
+        mbar_init(sfull_bar(s), 1);
+        mbar_init(sempty_bar(s), 2);
+      }
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -245,10 +265,36 @@ __global__ void __launch_bounds__(256, 1)
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
+          if (!mbar_wait<PAIR>(X3 ? sempty_bar(stage) : empty_bar(stage), phase ^ 1u)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
             break;
+          }
+          if (X3) {
+            // FP32 staging tiles; the converter warps turn them into the bf16 hi/lo stage
+            const uint32_t xa = sbase + stage * C::SSTAGE_BYTES;
+            const uint32_t xb = xa + C::SA_BYTES;
+            const uint32_t xf = sfull_bar(stage);
+            mbar_expect_tx(xf, C::SSTAGE_BYTES);
+            if (A_MN) {
+#pragma unroll
+              for (int j = 0; j < C::BM / 32; ++j) tma_load_2d(xa + 4096 * j, &tmA, xf, a_row0 + 32 * j, kb * C::BK);
+            } else {
+              tma_load_2d(xa, &tmA, xf, kb * C::BK, a_row0);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int j = 0; j < C::BNH / 32; ++j) tma_load_2d(xb + 4096 * j, &tmB, xf, b_row0 + 32 * j, kb * C::BK);
+            } else {
+              tma_load_2d(xb, &tmB, xf, kb * C::BK, b_row0);
+            }
+            issued |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
@@ -287,8 +333,9 @@ __global__ void __launch_bounds__(256, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u) {
           const uint32_t par = (issued_phase >> s) & 1u;
-          if (!(PAIR ? mbar_wait<true>(empty_bar(s), par) : mbar_wait(full_bar(s), par)))
-            atomicOr(args.fault, kFaultDrainWait);
+          const bool landed = PAIR ? mbar_wait<true>(empty_bar(s), par)
+                                   : mbar_wait(X3 ? sfull_bar(s) : full_bar(s), par);
+          if (!landed) atomicOr(args.fault, kFaultDrainWait);
         }
     }
   } else if (warp == 1) {
@@ -320,6 +367,24 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
+            if (X3) {
+              // bf16 hi/lo tiles, 32 contraction elements: K-major rows are 64 bytes
+              // (64-byte swizzle, 8-row groups 512 B apart, step 32 B per 16 elements);
+              // MN-major tiles keep 128-byte rows (64-element groups 4 KB apart).
+              auto d_a = [&](uint32_t t) {
+                return A_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
+              };
+              auto d_b = [&](uint32_t t) {
+                return B_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
+              };
+              const uint64_t a_hi = d_a(sa), a_lo = d_a(sa + C::A_HALF);
+              const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
+              // x*w ~ lo_x*hi_w + hi_x*lo_w + hi_x*hi_w (lo*lo dropped), small terms first
+              mma_bf16(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+              mma_bf16(d_tmem, a_hi, b_lo, IDESC, 1u);
+              mma_bf16(d_tmem, a_hi, b_hi, IDESC, 1u);
+              continue;
+            }
             // K-major: step 16 elements (32 bytes) along the swizzled row;
             // MN-major: step 16 contraction rows (16 x 128 bytes).
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
@@ -352,6 +417,89 @@ __global__ void __launch_bounds__(256, 1)
       else
         mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) atomicOr(args.fault, kFaultDrainWait);
+    }
+  } else if (X3 && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ converter (X3)
+    // Turns each FP32 staging stage into the bf16 hi/lo stage the MMAs read:
+    // hi = RNE(x), lo = RNE(x - hi), written in the tensor core's swizzled layout.
+    const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..63
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    // 16-byte chunk c of bf16 row r (8 elements) <- FP32 chunks 2c, 2c+1 of FP32 row r.
+    // K-major: FP32 rows of 128 B (128-byte swizzle), bf16 rows of 64 B (64-byte swizzle).
+    // MN-major: FP32 boxes of 32 elements x 32 contraction rows (4 KB each, 128-byte
+    // swizzle); bf16 groups of 64 elements x 32 rows (4 KB each, 128-byte swizzle).
+    // Each thread handles kBatch tasks at a time, all loads first, so the shared-
+    // memory latency of one task overlaps the others.
+    constexpr int kBatch = 4;
+    auto convert = [&](bool mn, uint32_t src, uint32_t hi, uint32_t lo, int extent) {
+      const int per_row = mn ? extent / 8 : 4;  // 16-byte bf16 chunks per row
+      const int total = mn ? 32 * per_row : extent * 4;
+      for (int t0 = tid; t0 < total; t0 += 64 * kBatch) {
+        float4 x0[kBatch], x1[kBatch];
+        uint32_t dst[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int t = t0 + 64 * b;
+          if (t < total) {
+            uint32_t a0, a1;
+            if (mn) {
+              const int k = t / per_row, q = t - (t / per_row) * per_row;
+              const int g = q >> 3, c = q & 7;
+              const uint32_t row = src + (2 * g + (c >> 2)) * 4096 + k * 128;
+              const int j0 = 2 * (c & 3);
+              a0 = row + ((j0 ^ (k & 7)) << 4);
+              a1 = row + (((j0 + 1) ^ (k & 7)) << 4);
+              dst[b] = g * 4096 + k * 128 + ((c ^ (k & 7)) << 4);
+            } else {
+              const int r = t >> 2, c = t & 3;
+              const uint32_t row = src + r * 128;
+              a0 = row + (((2 * c) ^ (r & 7)) << 4);
+              a1 = row + (((2 * c + 1) ^ (r & 7)) << 4);
+              dst[b] = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+            }
+            x0[b] = ld_shared_f4(a0);
+            x1[b] = ld_shared_f4(a1);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (t0 + 64 * b < total) {
+            uint4 h, l;
+            split8_bf16x3(x0[b], x1[b], h, l);
+            st_shared_u4(hi + dst[b], h);
+            st_shared_u4(lo + dst[b], l);
+          }
+        }
+      }
+    };
+    for (int u = unit0; ok && u < args.units; u += unit_step) {
+      const Unit w = decode_unit(args, u);
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        // every lane waits itself; the warp leaves together if any wait gives up
+        const bool mine = mbar_wait(sfull_bar(stage), phase) && mbar_wait(empty_bar(stage), phase ^ 1u);
+        if (!__all_sync(0xffffffffu, mine)) {
+          if (lane == 0) atomicOr(args.fault, kFaultProducerWait);
+          ok = false;
+          break;
+        }
+        const uint32_t xa = sbase + stage * C::SSTAGE_BYTES;
+        const uint32_t sa = base + stage * C::STAGE_BYTES;
+        const uint32_t sb = sa + C::A_BYTES;
+        convert(A_MN, xa, sa, sa + C::A_HALF, C::BM);
+        convert(B_MN, xa + C::SA_BYTES, sb, sb + C::B_HALF, C::BNH);
+        fence_proxy_async_shared();  // the tensor core reads what this thread wrote
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(sempty_bar(stage));  // staging tile may be reloaded
+          mbar_arrive(full_bar(stage));    // bf16 stage ready for the MMAs
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
@@ -517,6 +665,7 @@ struct GemmLaunch {
   GemmArgs args;
   int grid;   // CTAs (twice the number of pairs for a paired plan)
   bool pair;  // clusters of two CTAs share each tile
+  bool x3;    // FP32 operands through the fused BF16x3 mode (router)
 };
 
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
@@ -527,12 +676,12 @@ cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();
 cudaError_t set_attributes_mm();
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
 cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = TileCfg<BN, PAIR>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = TileCfg<BN, PAIR, X3>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -541,13 +690,13 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;  // single-CTA tiles launch without a cluster
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR>, l.tmA, l.tmB, l.args);
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.args);
 }
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
 cudaError_t set_attr_t() {
-  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TileCfg<BN, PAIR>::SMEM_BYTES);
+  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, PAIR, X3>::SMEM_BYTES);
 }
 
 }  // namespace dp

@@ -1,11 +1,24 @@
-// Instantiations of the BF16 GEMM for the forward: K-major A (X or dY), K-major B (W).
+// Instantiations of the GEMM for the forward: K-major A (X or dY), K-major B (W).
 // One translation unit per operand-major combination so the builds run in parallel.
-// Single-CTA tiles are 128 x {64, 128, 256}; CTA-pair tiles are 256 x {128, 256}.
+// BF16 operands: single-CTA tiles 128 x {64, 128, 256}, CTA-pair tiles 256 x {128, 256}.
+// FP32 router operands (fused BF16x3 split): single-CTA tiles 128 x {64, 128, 256}.
 #include "gemm_kernel.cuh"
 
 namespace dp {
 
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream) {
+  if (l.x3) {
+    switch (bn) {
+      case 64:
+        return launch_gemm_t<64, false, false, false, true>(l, stream);
+      case 128:
+        return launch_gemm_t<128, false, false, false, true>(l, stream);
+      case 256:
+        return launch_gemm_t<256, false, false, false, true>(l, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   if (l.pair) {
     switch (bn) {
       case 128:
@@ -34,6 +47,9 @@ cudaError_t set_attributes_kk() {
   if (e == cudaSuccess) e = set_attr_t<256, false, false, false>();
   if (e == cudaSuccess) e = set_attr_t<128, false, false, true>();
   if (e == cudaSuccess) e = set_attr_t<256, false, false, true>();
+  if (e == cudaSuccess) e = set_attr_t<64, false, false, false, true>();
+  if (e == cudaSuccess) e = set_attr_t<128, false, false, false, true>();
+  if (e == cudaSuccess) e = set_attr_t<256, false, false, false, true>();
   return e;
 }
 

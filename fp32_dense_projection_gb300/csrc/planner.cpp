@@ -27,6 +27,7 @@ constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceBytesPerNs = 50.0;    // last-arriver read of the split partials (one SM)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
+constexpr double kX3Rate = 0.5;               // fused BF16x3: split work and shared-memory traffic per MMA
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -35,7 +36,9 @@ size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 struct View {
   int64_t gm, gn, gk;
   bool a_mn, b_mn;
-  int a_elem, b_elem;  // bytes per element as streamed by the GEMM (bf16 = 2)
+  int a_elem, b_elem;  // bytes per element as streamed by the GEMM (bf16 = 2, fp32 = 4)
+  int terms = 1;       // MMAs per contraction element (3 for the router's BF16x3)
+  int bk = kBlockK;    // contraction block (32 for the router's fused split)
 };
 
 bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
@@ -49,15 +52,16 @@ bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
     case kOpWgrad:  // dW[N,K] = dY[T,N]^T X[T,K] : A = dY (MN-major), B = X (MN-major)
       *v = {N, K, T, true, true, 2, 2};
       return true;
-    // Router: the same views with the contraction tripled (hi|hi|lo against hi|lo|hi).
+    // Router: the same views on FP32 operands, each 32-wide block split into bf16
+    // hi/lo in shared memory and contracted with three MMAs.
     case kOpRouterFwd:
-      *v = {T, N, 3 * K, false, false, 2, 2};
+      *v = {T, N, K, false, false, 4, 4, 3, kRouterBlockK};
       return true;
     case kOpRouterDgrad:
-      *v = {T, K, 3 * N, false, true, 2, 2};
+      *v = {T, K, N, false, true, 4, 4, 3, kRouterBlockK};
       return true;
     case kOpRouterWgrad:
-      *v = {N, K, 3 * T, true, true, 2, 2};
+      *v = {N, K, T, true, true, 4, 4, 3, kRouterBlockK};
       return true;
     default:
       return false;
@@ -79,9 +83,9 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
                int out_bytes) {
   const double a_rows = static_cast<double>(std::min<int64_t>(kBlockM, v.gm));
   const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn)) / (t.pair ? 2.0 : 1.0);
-  const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
-  const double flop_per_kb = 2.0 * kBlockM * t.bn * kBlockK;  // per SM
-  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0);
+  const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
+  const double flop_per_kb = 2.0 * kBlockM * t.bn * v.bk * v.terms;  // per SM, tensor-pipe work
+  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0) / (v.terms > 1 ? kX3Rate : 1.0);
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
   const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
@@ -97,13 +101,13 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
 double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes) {
   const int64_t slots = t.pair ? sm / 2 : sm;
   const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
-  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, kBlockK));
+  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, v.bk));
   const int64_t split_units = (tiles - full) * splits;
   const int64_t units = full + split_units;
   const int64_t active_sms = std::min<int64_t>(units, slots) * (t.pair ? 2 : 1);
   const double a_rows = static_cast<double>(std::min<int64_t>(t.rows(), v.gm));
   const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn));
-  const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * kBlockK;
+  const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
   const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
   const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
   double time = 0.0;
@@ -143,6 +147,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
     if (o.pair >= 0 && pair != o.pair) continue;
     if (pair && !kAutoPair && o.pair != 1) continue;
     if (pair && (sm < 2 || v.gm <= kBlockM)) continue;  // a pair needs two row blocks of work
+    if (pair && v.terms > 1) continue;                  // the fused BF16x3 mode is single-CTA
     const int64_t slots = pair ? sm / 2 : sm;
     for (int bn : {256, 128, 64}) {
       if (pair && bn < 128) continue;  // each CTA of a pair holds bn / 2 >= 64 columns of B
@@ -153,7 +158,9 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // counters / partial slots: one per CTA tile
       // bounded accumulation length, unless the tiles are too many to split at all
       // (then whole K per tile: a longer running sum, the only case without the bound)
-      const int64_t min_s = cta_tiles > kMaxSplitTiles ? 1 : ceil_div(nkb, kMaxAccumBlocks);
+      // (kMaxAccumBlocks counts 64-element blocks of one MMA each; BF16x3 accumulates three)
+      const int64_t max_blocks = kMaxAccumBlocks * kBlockK / (v.bk * v.terms);
+      const int64_t min_s = cta_tiles > kMaxSplitTiles ? 1 : ceil_div(nkb, max_blocks);
       const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(nkb, 64));
       // every tile split the same way (s = 1: whole K per tile)
       for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0; ++s) {
@@ -189,7 +196,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.out_f32 = (op >= kOpRouterFwd) ? 1 : (out_f32 ? 1 : 0);
   plan.a_mn = v.a_mn;
   plan.b_mn = v.b_mn;
-  plan.nkb = ceil_div(v.gk, kBlockK);
+  plan.nkb = ceil_div(v.gk, v.bk);
+  plan.bk = v.bk;
   const int out_bytes = plan.out_f32 ? 4 : 2;
 
   Choice c;
@@ -217,7 +225,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.bm = static_cast<int>(c.tiling.rows());
   plan.bn = c.tiling.bn;
   plan.splits = static_cast<int>(c.splits);
-  plan.stages = stages_for(plan.bn, plan.pair);
+  plan.stages = v.terms > 1 ? stages_x3(plan.bn) : stages_for(plan.bn, plan.pair);
   plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
   const int64_t tiles = plan.tiles_m * plan.tiles_n;
@@ -231,42 +239,18 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   const int64_t slots = plan.pair ? sm / 2 : sm;
   plan.grid = static_cast<int>(std::min<int64_t>(plan.units, slots) * (plan.pair ? 2 : 1));
 
-  // workspace layout: [counters | split partials | router A' | router B']
+  // workspace layout: [counters | split partials]
   size_t off = kCounterBytes;
-  const bool router_copies = op >= kOpRouterFwd && v.gm > 0;
-  if (plan.splits > 1 || router_copies) {
+  if (plan.splits > 1) {
     plan.off_counters = 0;
     plan.bytes_counters = kCounterBytes;
-  }
-  if (plan.splits > 1) {
     // one FP32 partial per split of every split tile, per CTA of the tile
     plan.off_partials = off;
     plan.bytes_partials = static_cast<size_t>(tiles - plan.full_units) * (plan.pair ? 2 : 1) * plan.splits *
                           kBlockM * plan.bn * sizeof(float);
     off += plan.bytes_partials;
   }
-  if (router_copies) {
-    // hi/lo bf16 copies of both operands, concatenated along the contraction
-    int64_t a_elems = 0, b_elems = 0;
-    if (op == kOpRouterFwd) {
-      a_elems = T * 3 * K;
-      b_elems = N * 3 * K;
-    } else if (op == kOpRouterDgrad) {
-      a_elems = T * 3 * N;
-      b_elems = 3 * N * K;
-    } else {
-      a_elems = 3 * T * N;
-      b_elems = 3 * T * K;
-    }
-    off = round_up(off, 1024);
-    plan.off_router_a = off;
-    plan.bytes_router_a = static_cast<size_t>(a_elems) * 2;
-    off = round_up(off + plan.bytes_router_a, 1024);
-    plan.off_router_b = off;
-    plan.bytes_router_b = static_cast<size_t>(b_elems) * 2;
-    off += plan.bytes_router_b;
-  }
-  plan.ws_bytes = (plan.splits > 1 || router_copies) ? round_up(off, 256) : 0;
+  plan.ws_bytes = plan.splits > 1 ? round_up(off, 256) : 0;
   *p = plan;
   return true;
 }

@@ -56,11 +56,9 @@ struct Plan {
   // `splits` ways (all tiles when full_units = 0, the last partial wave otherwise)
   int64_t full_units = 0;
   // workspace layout (byte offsets from the workspace base): counters first, in
-  // a fixed region of kCounterBytes, then split partials, then router operands
+  // a fixed region of kCounterBytes, then split partials
   size_t off_counters = 0, bytes_counters = 0;
   size_t off_partials = 0, bytes_partials = 0;
-  size_t off_router_a = 0, bytes_router_a = 0;
-  size_t off_router_b = 0, bytes_router_b = 0;
   size_t ws_bytes = 0;
 };
 
@@ -73,6 +71,15 @@ constexpr int stages_for_rows(int b_rows) {
              : 8;
 }
 constexpr int stages_for(int bn, bool pair = false) { return stages_for_rows(pair ? bn / 2 : bn); }
+
+// The FP32 router's fused BF16x3 GEMM streams 32-wide contraction blocks: per
+// stage an FP32 staging tile ((128 + bn) rows x 128 bytes, loaded by TMA) and its
+// bf16 hi/lo copy for the tensor core (the same bytes), so stages = 192 KB / twice that.
+constexpr int kRouterBlockK = 32;
+constexpr int stages_x3(int bn) {
+  return (192 * 1024) / (2 * (kBlockM + bn) * kRouterBlockK * 4) < 8 ? (192 * 1024) / (2 * (kBlockM + bn) * kRouterBlockK * 4)
+                                                                     : 8;
+}
 
 // Overrides of the planner's choices, for tests and tuning (all unset in normal
 // use): > 0 forces the tile width / uniform split count / last-wave split count;

@@ -210,6 +210,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          (static_cast<uint64_t>(2) << 61);
 }
 
+// Descriptor with an explicit layout type (bits [61,64)): 2 = 128-byte swizzle,
+// 4 = 64-byte swizzle.  For 64-byte-swizzled K-major tiles (32 bf16 per row) the
+// 8-row group stride is 512 bytes.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16) |
+         (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(layout & 7u) << 61);
+}
+
 // Instruction descriptor, kind::f16 with BF16 A/B and FP32 D.
 //   [4,6) D format = 1 (F32); [7,10) A format = 1 (BF16); [10,13) B format = 1 (BF16);
 //   bit 15 A major (1 = MN); bit 16 B major; [17,23) N>>3; [24,29) M>>4.
@@ -302,6 +312,25 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ------------------------------------------------------------ shared memory
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tensor core) before signalling that the data is ready.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // --------------------------------------------------------------- conversions
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -309,6 +338,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   // cvt.rn.bf16x2.f32 d, a, b: a goes to the upper half, b to the lower half.
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// BF16x3 split of eight FP32 values (two float4 in element order): hi = RNE(x),
+// lo = RNE(x - hi), where x - hi is exact in FP32; each packed into one 16-byte
+// chunk of eight bf16 in the same element order.
+__device__ __forceinline__ void split8_bf16x3(const float4& a, const float4& b, uint4& hi, uint4& lo) {
+  const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+    const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xFFFF0000u);
+    l[i] = pack_bf16x2(x[2 * i] - h0, x[2 * i + 1] - h1);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 }  // namespace dp

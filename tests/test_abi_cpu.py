@@ -57,7 +57,9 @@ SM = 152
 def test_plan_is_valid(op, T, N, K):
     p = dp.plan(op, T, N, K, out_f32=False, sm_count=SM)
     pair = bool(p["cta_pair"])
-    assert p["block_m"] == (256 if pair else 128) and p["block_k"] == 64
+    assert p["block_m"] == (256 if pair else 128)
+    assert p["block_k"] == (32 if op.startswith("router") else 64)  # router: fused split of 32-wide blocks
+    assert not (pair and op.startswith("router"))
     assert p["block_n"] in ((128, 256) if pair else (64, 128, 256))
     slots = SM // 2 if pair else SM
     ctas_per_tile = 2 if pair else 1
@@ -70,8 +72,9 @@ def test_plan_is_valid(op, T, N, K):
     assert p["full_units"] in (0, tiles) or (p["full_units"] % slots == 0 and tiles - p["full_units"] < slots)
     assert 1 <= p["splits"] <= max(1, p["k_blocks"])
     assert p["tiles_m"] * p["block_m"] >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
-    assert p["k_blocks"] * 64 >= p["gemm_k"] > (p["k_blocks"] - 1) * 64
-    mult = 3 if op.startswith("router") else 1
+    bk = p["block_k"]
+    assert p["k_blocks"] * bk >= p["gemm_k"] > (p["k_blocks"] - 1) * bk
+    mult = 1
     if op.endswith("wgrad"):
         if p["swap_ab"]:
             assert op == "wgrad" and (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (K, N, T)
@@ -203,9 +206,11 @@ def test_workspace_keeps_a_fixed_counter_region():
 @pytest.mark.parametrize("op", list(dp.OP_NAMES))
 @pytest.mark.parametrize("T", [1025, 16173, 16384, 65537, 200000])
 def test_accumulation_length_is_bounded(op, T):
-    # no TMEM accumulator sums more than 256 contraction blocks (16384 tokens)
+    # no TMEM accumulator takes more than 16384 MMA accumulations per element: 16384
+    # contraction elements, or 16384 / 3 for the router's three BF16x3 terms
+    terms = 3 if op.startswith("router") else 1
     for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
         p = dp.plan(op, T, N, K, sm_count=SM)
-        per_split = -(-p["k_blocks"] // p["splits"])
+        per_split = -(-p["k_blocks"] // p["splits"]) * p["block_k"]
         if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else no counters: whole K
-            assert per_split <= 256, (op, T, N, K, p)
+            assert per_split * terms <= 16384 + p["block_k"] * terms, (op, T, N, K, p)

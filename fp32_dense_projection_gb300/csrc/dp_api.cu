@@ -98,16 +98,16 @@ EncodeTiledFn encode_fn() {
 // (box = box_rows x 64 columns) or FP32 (box = box_rows x 32 columns): 128-byte
 // box rows, 128-byte swizzle, zero fill outside the matrix.
 bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
-              bool f32 = false) {
+              bool f32 = false, uint32_t box_cols = 0, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (f32 ? 4 : 2)};
-  const cuuint32_t box[2] = {f32 ? 32u : 64u, box_rows};
+  const cuuint32_t box[2] = {box_cols ? box_cols : (f32 ? 32u : 64u), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------ argument checks
@@ -159,21 +159,30 @@ dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
 
 // A: operand (m, k) -- K-major: [gm][gk] matrix; MN-major: [gk][gm] matrix.
 // B: operand (n, k) -- K-major: [gn][gk] matrix; MN-major: [gk][gn] matrix.
+// Router BF16x3 plans (x3): A is FP32, B and B_lo are B's bf16 hi and lo planes.
 dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
-                      int64_t ldb, void* out, int64_t ldo, void* ws, cudaStream_t stream) {
+                      int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, cudaStream_t stream) {
   if (p.units > 0x7FFFFFFF || p.tiles_m > 0x7FFFFFFF || p.tiles_n > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF)
     return DP_ERR_UNSUPPORTED;
   GemmLaunch l;
   std::memset(&l, 0, sizeof(l));
+  const bool x3 = p.op == kOpRouterFwd || p.op == kOpRouterWgrad;
   // Boxes: K-major operands one box of bk contraction columns x tile rows; MN-major
   // operands boxes of 64 (bf16) or 32 (FP32) tile columns x bk contraction rows.
-  const bool f32 = p.op >= kOpRouterFwd;  // FP32 operands, split into bf16 hi/lo in the kernel
   const uint32_t kb_rows = static_cast<uint32_t>(p.bk);
   const uint32_t b_rows = static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn);
-  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, f32)
-                           : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, f32);
-  const bool ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, f32)
-                           : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows, f32);
+  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, x3)
+                           : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, x3);
+  bool ok_b;
+  if (!x3) {
+    ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows) : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows);
+    l.tmB2 = l.tmB;
+  } else if (p.b_mn) {  // 64-column groups of 32 rows, 128-byte swizzle
+    ok_b = make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows) && make_map(&l.tmB2, B_lo, p.gk, p.gn, ldb, kb_rows);
+  } else {  // rows of 32 contraction elements (64 bytes), 64-byte swizzle
+    ok_b = make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows, false, kb_rows, CU_TENSOR_MAP_SWIZZLE_64B) &&
+           make_map(&l.tmB2, B_lo, p.gn, p.gk, ldb, b_rows, false, kb_rows, CU_TENSOR_MAP_SWIZZLE_64B);
+  }
   if (!ok_a || !ok_b) return DP_ERR_LAUNCH;
   GemmArgs& a = l.args;
   a.gm = p.gm;
@@ -196,7 +205,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.fault = dev.fault;
   l.grid = p.grid;
   l.pair = p.pair;
-  l.x3 = f32;
+  l.x3 = x3;
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);
@@ -257,13 +266,33 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
   if (p.ws_bytes > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
 
   if (!router) {
-    if (p.swap) return launch_view(p, *dev, b, ldb, a, lda, out, ldo, ws, stream);  // A = X, B = dY
-    return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
+    if (p.swap) return launch_view(p, *dev, b, ldb, a, lda, nullptr, out, ldo, ws, stream);  // A = X, B = dY
+    return launch_view(p, *dev, a, lda, b, ldb, nullptr, out, ldo, ws, stream);
   }
 
-  // Router: the FP32 operands go to the fused BF16x3 mode, which splits each
-  // 32-wide block into bf16 hi/lo in shared memory.
-  return launch_view(p, *dev, a, lda, b, ldb, out, ldo, ws, stream);
+  // Router (BF16x3).  The operand that every row tile reuses is split into bf16
+  // hi/lo once here; the streamed FP32 operand is split inside the GEMM.
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* sa = reinterpret_cast<uint16_t*>(w + p.off_split_a);
+  uint16_t* sb = reinterpret_cast<uint16_t*>(w + p.off_split_b);
+  SplitJob jobs[2];
+  int njobs = 1;
+  std::memset(jobs, 0, sizeof(jobs));
+  if (op == kOpRouterFwd) {  // W [N][K] -> hi, lo planes
+    jobs[0] = {static_cast<const float*>(b), sb, N, K, ldb, p.ld_split_b, N * p.ld_split_b, 2, 0x2u};
+  } else if (op == kOpRouterWgrad) {  // dY [T][N] -> hi, lo planes
+    jobs[0] = {static_cast<const float*>(a), sb, T, N, lda, p.ld_split_b, T * p.ld_split_b, 2, 0x2u};
+  } else {  // dY' = [lo | hi | hi] (T x 3N), W' = [hi; lo; hi] (3N x K)
+    jobs[0] = {static_cast<const float*>(a), sa, T, N, lda, p.ld_split_a, N, 3, 0x1u};
+    jobs[1] = {static_cast<const float*>(b), sb, N, K, ldb, p.ld_split_b, N * p.ld_split_b, 3, 0x2u};
+    njobs = 2;
+  }
+  if (launch_split_x3(jobs, njobs, dev->sm_count, stream) != cudaSuccess) return DP_ERR_LAUNCH;
+  if (op == kOpRouterFwd)  // A = X (FP32), B = W planes
+    return launch_view(p, *dev, a, lda, sb, p.ld_split_b, sb + N * p.ld_split_b, out, ldo, ws, stream);
+  if (op == kOpRouterWgrad)  // dW^T = X^T dY: A = X (FP32), B = dY planes; stored transposed
+    return launch_view(p, *dev, b, ldb, sb, p.ld_split_b, sb + T * p.ld_split_b, out, ldo, ws, stream);
+  return launch_view(p, *dev, sa, p.ld_split_a, sb, p.ld_split_b, nullptr, out, ldo, ws, stream);
 }
 
 }  // namespace

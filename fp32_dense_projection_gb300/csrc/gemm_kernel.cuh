@@ -59,33 +59,36 @@ struct GemmArgs {
   uint32_t* fault;     // device status word
 };
 
-// X3: the FP32 router's fused BF16x3 mode.  A stage then holds the bf16 hi and lo
-// halves of a 32-wide contraction block of each operand ([A_hi | A_lo | B_hi | B_lo]),
-// written by converter warps from an FP32 staging tile that TMA loads into a
-// second ring of the same size.
+// X3: the FP32 router's BF16x3 mode.  A stage of the MMA ring then holds the bf16
+// hi and lo halves of a 32-wide contraction block of each operand
+// ([A_hi | A_lo | B_hi | B_lo]).  A's halves are written by converter warps from an
+// FP32 staging tile that TMA loads into a separate, one-stage-deeper ring; B's
+// halves are loaded by TMA from two bf16 planes split before the launch.
 template <int BN, bool PAIR = false, bool X3 = false>
 struct TileCfg {
-  static_assert(!(PAIR && X3), "the fused BF16x3 mode uses single-CTA tiles");
+  static_assert(!(PAIR && X3), "the BF16x3 mode uses single-CTA tiles");
   static constexpr int BM = kBlockM;             // accumulator rows per CTA
   static constexpr int TM = PAIR ? 2 * BM : BM;  // output tile rows (a CTA pair splits them)
   static constexpr int BNH = PAIR ? BN / 2 : BN; // B rows each CTA loads
   static constexpr int BK = X3 ? kRouterBlockK : kBlockK;
   static constexpr int STAGES = X3 ? stages_x3(BN) : stages_for(BN, PAIR);
+  static constexpr int SSTAGES = X3 ? staging_stages_x3(BN) : 0;  // FP32 staging ring (X3)
   static constexpr int A_HALF = BM * BK * 2;     // one bf16 copy of the A tile
   static constexpr int B_HALF = BNH * BK * 2;
   static constexpr int A_BYTES = X3 ? 2 * A_HALF : A_HALF;
   static constexpr int B_BYTES = X3 ? 2 * B_HALF : B_HALF;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // FP32 staging of A (X3)
-  static constexpr int SB_BYTES = X3 ? BNH * BK * 4 : 0;
-  static constexpr int SSTAGE_BYTES = SA_BYTES + SB_BYTES;
+  static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // one FP32 staging tile of A (X3)
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int EPI_BYTES = 4 * 4096;  // a 32 x 32 FP32 output block per epilogue warp
   // full, empty, tmem_full x2, tmem_empty x2, drain (+ staging full / empty for X3)
-  static constexpr int NUM_BARS = 2 * STAGES + 5 + (X3 ? 2 * STAGES : 0);
-  static constexpr int SMEM_BYTES = 1024 + STAGES * (STAGE_BYTES + SSTAGE_BYTES) + NUM_BARS * 8 + 64;
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SSTAGES;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + SSTAGES * SA_BYTES + EPI_BYTES + NUM_BARS * 8 + 64;
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(STAGE_BYTES % 1024 == 0 && SSTAGE_BYTES % 1024 == 0, "swizzle alignment");
+  static_assert(STAGE_BYTES % 1024 == 0 && SA_BYTES % 1024 == 0, "swizzle alignment");
+  static_assert(!X3 || (STAGE_BYTES == x3_stage_bytes(BN) && SA_BYTES == kX3StagingBytes), "planner sizes");
 };
 
 // Work unit u -> output tile, contraction range and, for split units, the split
@@ -181,12 +184,170 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_
   }
 }
 
+// Store a 32 x 32 block of the output, called by a whole warp: lane i holds the
+// 32 values of row m0 + i, columns [col0, col0 + 32).  stage_block32 puts the block
+// in the warp's 4 KB of shared memory (16-byte chunks XOR-swizzled by row, so
+// neither the row-wise writes nor the column-wise reads conflict on banks);
+// flush_block32 reads it back by columns and writes 16-byte stores of which each
+// instruction covers whole 128-byte (FP32) or 64-byte (BF16) row segments, instead
+// of one 16-byte piece of 32 different rows.  (The transposed store of the swapped
+// weight gradient is already coalesced and goes straight out.)
+__device__ __forceinline__ void stage_block32(const GemmArgs& a, uint32_t buf, int lane, const float (&v)[32]) {
+  __syncwarp();  // the previous block's reads of buf are done
+  if (a.out_f32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_u4(buf + lane * 128 + ((j ^ (lane & 7)) << 4),
+                   make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                              __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_u4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4),
+                   make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7])));
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void flush_block32(const GemmArgs& a, uint32_t buf, int lane, int64_t m0, int64_t col0) {
+  const int64_t rows_left = a.gm - m0;
+  if (a.out_f32) {
+    const int ch = lane & 7, r0 = lane >> 3;
+    const bool col_ok = col0 + 4 * ch < a.gn;
+    float* p = static_cast<float*>(a.out) + (m0 + r0) * a.ldo + col0 + 4 * ch;
+    const int64_t step = 4 * a.ldo;
+#pragma unroll
+    for (int i = 0; i < 8; ++i, p += step) {
+      const int r = 4 * i + r0;
+      const uint4 x = ld_shared_u4(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+      if (col_ok && r < rows_left) *reinterpret_cast<uint4*>(p) = x;
+    }
+  } else {
+    const int ch = lane & 3, r0 = lane >> 2;
+    const bool col_ok = col0 + 8 * ch < a.gn;
+    uint16_t* p = static_cast<uint16_t*>(a.out) + (m0 + r0) * a.ldo + col0 + 8 * ch;
+    const int64_t step = 8 * a.ldo;
+#pragma unroll
+    for (int i = 0; i < 4; ++i, p += step) {
+      const int r = 8 * i + r0;
+      const uint4 x = ld_shared_u4(buf + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+      if (col_ok && r < rows_left) *reinterpret_cast<uint4*>(p) = x;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_block32(const GemmArgs& a, uint32_t buf, int lane, int64_t m0, int64_t col0,
+                                              const float (&v)[32]) {
+  if (a.out_trans) {
+    store_row32(a, m0 + lane, col0, v);
+    return;
+  }
+  stage_block32(a, buf, lane, v);
+  flush_block32(a, buf, lane, m0, col0);
+}
+
+// Ordered reduction of one split tile's partials by its last-arriving CTA, for the
+// 32 rows [m0, m0 + 32) of one epilogue warp (rows wrow.. of the CTA's partial
+// tiles).  (Chunk, split) pairs qq = c * splits + sp are walked in order, two at a
+// time, with the next two pairs' loads issued before the current ones are added:
+// partials of one 32-column chunk are summed in ascending split order, in FP32,
+// rounded once, and four chunk-splits of loads are in flight per thread.
+// Lane layout: for the row-major output value i of a lane is row 4i + lane/8,
+// float4 column chunk lane%8 of the 32-column chunk, so each store instruction
+// writes four whole 128-byte row segments; for the transposed store it is row
+// `lane`, chunk i, so consecutive lanes write consecutive elements of each output
+// row.  Both are linear in i: row = r0 + i * dr, chunk = c0 + i * dc.
+template <int BN>
+__device__ __forceinline__ void reduce_split_tile(const GemmArgs& args, const float4* p0, int lane, int wrow,
+                                                  int64_t m0, int64_t n0) {
+  constexpr int BM = kBlockM;
+  const bool tr = args.out_trans != 0;
+  const int r0 = tr ? lane : (lane >> 3), dr = tr ? 0 : 4;
+  const int c0 = tr ? 0 : (lane & 7), dc = tr ? 1 : 0;
+  const int64_t rows_left = args.gm - m0;
+  const int S = args.splits;
+  int nch = BN / 32;
+  while (nch > 0 && n0 + (nch - 1) * 32 >= args.gn) --nch;
+  const int total = nch * S;
+  const size_t pstride = static_cast<size_t>(BM) * BN / 4;
+  const float4* lane_base = p0 + wrow + c0 * BM + r0;
+  const int istep = dc * BM + dr;  // float4 distance between a lane's values i and i + 1
+  float4 cur0[8], cur1[8], nxt0[8], nxt1[8];
+  // (padding rows of a thin tile hold no partials: their sums are never stored)
+  auto load = [&](float4(&dst)[8], int qq) {
+    if (qq < total) {
+      const int c = qq / S, sp = qq - (qq / S) * S;
+      const float4* src = lane_base + sp * pstride + static_cast<size_t>(c * 8) * BM;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i * istep);
+    }
+  };
+  float4 acc[8];
+  auto consume = [&](const float4(&x)[8], int qq) {
+    if (qq < total) {
+      const int c = qq / S, sp = qq - (qq / S) * S;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (sp == 0) {
+          acc[i] = x[i];
+        } else {
+          acc[i].x += x[i].x;
+          acc[i].y += x[i].y;
+          acc[i].z += x[i].z;
+          acc[i].w += x[i].w;
+        }
+      }
+      if (sp == S - 1) {
+        const int64_t col = n0 + c * 32;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = r0 + i * dr;
+          const int64_t cc = col + 4 * (c0 + i * dc);
+          if (r >= rows_left || cc >= args.gn) continue;
+          if (tr) {
+            const float e[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int64_t o = (cc + t) * args.ldo + m0 + r;
+              if (args.out_f32)
+                static_cast<float*>(args.out)[o] = e[t];
+              else
+                static_cast<uint16_t*>(args.out)[o] = static_cast<uint16_t>(pack_bf16x2(e[t], 0.0f) & 0xFFFFu);
+            }
+          } else if (args.out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(args.out) + (m0 + r) * args.ldo + cc) = acc[i];
+          } else {
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(args.out) + (m0 + r) * args.ldo + cc) =
+                make_uint2(pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
+          }
+        }
+      }
+    }
+  };
+  load(cur0, 0);
+  load(cur1, 1);
+#pragma unroll 1
+  for (int qq = 0; qq < total; qq += 2) {
+    load(nxt0, qq + 2);
+    load(nxt1, qq + 3);
+    consume(cur0, qq);
+    consume(cur1, qq + 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cur0[i] = nxt0[i];
+      cur1[i] = nxt1[i];
+    }
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
   using C = TileCfg<BN, PAIR, X3>;
   constexpr int STAGES = C::STAGES;
+  constexpr int SSTAGES = C::SSTAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(C::TM, BN, A_MN, B_MN);
   // With PAIR, a cluster of two CTAs computes one TM x BN tile: rank r loads A rows
   // [r*128, r*128+128) and B rows [r*BN/2, (r+1)*BN/2) of the tile into the same
@@ -201,9 +362,10 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1024-byte alignment
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sbase = base + STAGES * C::STAGE_BYTES;  // FP32 staging ring (X3)
-  const uint32_t bar0 = sbase + STAGES * C::SSTAGE_BYTES;
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(base_ptr + STAGES * (C::STAGE_BYTES + C::SSTAGE_BYTES) + C::NUM_BARS * 8);
+  const uint32_t ebase = sbase + SSTAGES * C::SA_BYTES;   // epilogue output blocks
+  const uint32_t bar0 = ebase + C::EPI_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + STAGES * C::STAGE_BYTES + SSTAGES * C::SA_BYTES +
+                                                    C::EPI_BYTES + C::NUM_BARS * 8);
   volatile uint32_t* flag_wait = tmem_slot + 2;  // [2], double-buffered by unit parity
   volatile uint32_t* flag_last = tmem_slot + 4;  // [2]
 
@@ -212,20 +374,20 @@ __global__ void __launch_bounds__(256, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };            // X3 staging landed
-  auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + STAGES + s); };  // X3 staging read
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };             // X3 staging landed
+  auto sempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + SSTAGES + s); };  // X3 staging read
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(threadIdx.x) & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), X3 ? 2 : 1);  // X3: one arrival per converter warp
+      mbar_init(full_bar(s), X3 ? 3 : 1);  // X3: the B loads' arrival and one per converter warp
       mbar_init(empty_bar(s), 1);
-      if (X3) {
-        mbar_init(sfull_bar(s), 1);
-        mbar_init(sempty_bar(s), 2);
-      }
+    }
+    for (int s = 0; s < SSTAGES; ++s) {
+      mbar_init(sfull_bar(s), 1);
+      mbar_init(sempty_bar(s), 2);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -256,37 +418,59 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_phase = 0;  // per-stage bit masks, for the final drain
+      if (X3) tma_prefetch_map(&tmB2);
+      int stage = 0, sstage = 0;
+      uint32_t phase = 0, sphase = 0;
+      // per-stage bit masks of issued loads and their phases, for the final drain
+      uint32_t issued = 0, issued_phase = 0, sissued = 0, sissued_phase = 0;
       bool ok = true;
       for (int u = unit0; ok && u < args.units; u += unit_step) {
         const Unit w = decode_unit(args, u);
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait<PAIR>(X3 ? sempty_bar(stage) : empty_bar(stage), phase ^ 1u)) {
-            atomicOr(args.fault, kFaultProducerWait);
-            ok = false;
-            break;
-          }
           if (X3) {
-            // FP32 staging tiles; the converter warps turn them into the bf16 hi/lo stage
-            const uint32_t xa = sbase + stage * C::SSTAGE_BYTES;
-            const uint32_t xb = xa + C::SA_BYTES;
-            const uint32_t xf = sfull_bar(stage);
-            mbar_expect_tx(xf, C::SSTAGE_BYTES);
+            // FP32 staging tile of A; the converter warps split it into the bf16 stage
+            if (!mbar_wait(sempty_bar(sstage), sphase ^ 1u)) {
+              atomicOr(args.fault, kFaultProducerWait);
+              ok = false;
+              break;
+            }
+            const uint32_t xa = sbase + sstage * C::SA_BYTES;
+            const uint32_t xf = sfull_bar(sstage);
+            mbar_expect_tx(xf, C::SA_BYTES);
             if (A_MN) {
 #pragma unroll
               for (int j = 0; j < C::BM / 32; ++j) tma_load_2d(xa + 4096 * j, &tmA, xf, a_row0 + 32 * j, kb * C::BK);
             } else {
               tma_load_2d(xa, &tmA, xf, kb * C::BK, a_row0);
             }
+            sissued |= 1u << sstage;
+            sissued_phase = (sissued_phase & ~(1u << sstage)) | (sphase << sstage);
+            if (++sstage == SSTAGES) {
+              sstage = 0;
+              sphase ^= 1u;
+            }
+            // B's bf16 hi and lo tiles straight into the MMA stage
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
+              atomicOr(args.fault, kFaultProducerWait);
+              ok = false;
+              break;
+            }
+            const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
+            const uint32_t fb = full_bar(stage);
+            mbar_expect_tx(fb, C::B_BYTES);
             if (B_MN) {
+              // 64-column groups of 32 contraction rows (4 KB, 128-byte swizzle)
 #pragma unroll
-              for (int j = 0; j < C::BNH / 32; ++j) tma_load_2d(xb + 4096 * j, &tmB, xf, b_row0 + 32 * j, kb * C::BK);
+              for (int j = 0; j < C::BNH / 64; ++j) {
+                tma_load_2d(sb + 4096 * j, &tmB, fb, b_row0 + 64 * j, kb * C::BK);
+                tma_load_2d(sb + C::B_HALF + 4096 * j, &tmB2, fb, b_row0 + 64 * j, kb * C::BK);
+              }
             } else {
-              tma_load_2d(xb, &tmB, xf, kb * C::BK, b_row0);
+              // rows of 32 contraction elements (64 bytes, 64-byte swizzle)
+              tma_load_2d(sb, &tmB, fb, kb * C::BK, b_row0);
+              tma_load_2d(sb + C::B_HALF, &tmB2, fb, kb * C::BK, b_row0);
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -295,6 +479,11 @@ __global__ void __launch_bounds__(256, 1)
               phase ^= 1u;
             }
             continue;
+          }
+          if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
+            atomicOr(args.fault, kFaultProducerWait);
+            ok = false;
+            break;
           }
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
@@ -330,12 +519,16 @@ __global__ void __launch_bounds__(256, 1)
       // Every load this thread issued has landed before the CTA may exit: on the
       // stage's full barrier, or for a pair (whose loads complete on the leader's
       // barrier) on the empty barrier the leader's MMAs release after reading it.
+      // (X3: the staging tiles on their own full barriers.)
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u) {
           const uint32_t par = (issued_phase >> s) & 1u;
-          const bool landed = PAIR ? mbar_wait<true>(empty_bar(s), par)
-                                   : mbar_wait(X3 ? sfull_bar(s) : full_bar(s), par);
+          const bool landed = PAIR ? mbar_wait<true>(empty_bar(s), par) : mbar_wait(full_bar(s), par);
           if (!landed) atomicOr(args.fault, kFaultDrainWait);
+        }
+      for (int s = 0; s < SSTAGES; ++s)
+        if ((sissued >> s) & 1u) {
+          if (!mbar_wait(sfull_bar(s), (sissued_phase >> s) & 1u)) atomicOr(args.fault, kFaultDrainWait);
         }
     }
   } else if (warp == 1) {
@@ -420,11 +613,11 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (X3 && (warp == 2 || warp == 3)) {
     // ------------------------------------------------------------ converter (X3)
-    // Turns each FP32 staging stage into the bf16 hi/lo stage the MMAs read:
+    // Turns each FP32 staging tile of A into the bf16 hi/lo A tiles of an MMA stage:
     // hi = RNE(x), lo = RNE(x - hi), written in the tensor core's swizzled layout.
     const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..63
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, sstage = 0;
+    uint32_t phase = 0, sphase = 0;
     bool ok = true;
     // 16-byte chunk c of bf16 row r (8 elements) <- FP32 chunks 2c, 2c+1 of FP32 row r.
     // K-major: FP32 rows of 128 B (128-byte swizzle), bf16 rows of 64 B (64-byte swizzle).
@@ -478,22 +671,23 @@ __global__ void __launch_bounds__(256, 1)
       const Unit w = decode_unit(args, u);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         // every lane waits itself; the warp leaves together if any wait gives up
-        const bool mine = mbar_wait(sfull_bar(stage), phase) && mbar_wait(empty_bar(stage), phase ^ 1u);
+        const bool mine = mbar_wait(sfull_bar(sstage), sphase) && mbar_wait(empty_bar(stage), phase ^ 1u);
         if (!__all_sync(0xffffffffu, mine)) {
           if (lane == 0) atomicOr(args.fault, kFaultProducerWait);
           ok = false;
           break;
         }
-        const uint32_t xa = sbase + stage * C::SSTAGE_BYTES;
         const uint32_t sa = base + stage * C::STAGE_BYTES;
-        const uint32_t sb = sa + C::A_BYTES;
-        convert(A_MN, xa, sa, sa + C::A_HALF, C::BM);
-        convert(B_MN, xa + C::SA_BYTES, sb, sb + C::B_HALF, C::BNH);
+        convert(A_MN, sbase + sstage * C::SA_BYTES, sa, sa + C::A_HALF, C::BM);
         fence_proxy_async_shared();  // the tensor core reads what this thread wrote
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(sempty_bar(stage));  // staging tile may be reloaded
-          mbar_arrive(full_bar(stage));    // bf16 stage ready for the MMAs
+          mbar_arrive(sempty_bar(sstage));  // staging tile may be reloaded
+          mbar_arrive(full_bar(stage));     // A half of the bf16 stage ready for the MMAs
+        }
+        if (++sstage == SSTAGES) {
+          sstage = 0;
+          sphase ^= 1u;
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -506,6 +700,7 @@ __global__ void __launch_bounds__(256, 1)
     const int q = warp & 3;          // TMEM sub-partition this warp may read
     const int row = q * 32 + lane;   // accumulator row == TMEM lane
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t ebuf = ebase + q * 4096;  // this warp's output block
     const bool leader = threadIdx.x == 128;
     int local = 0;
     // the epilogue warps (of both CTAs of a pair) release the accumulator on the
@@ -537,6 +732,7 @@ __global__ void __launch_bounds__(256, 1)
       if (flag_wait[local & 1] == 0u) break;
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(tm) * C::TM + static_cast<int64_t>(rank) * C::BM + row;
+      const int64_t m0 = m - lane;  // row of lane 0
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
       if (!w.split) {
@@ -549,7 +745,7 @@ __global__ void __launch_bounds__(256, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_row32(args, m, n0 + c * 32, v);
+          store_block32(args, ebuf, lane, m0, n0 + c * 32, v);
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
@@ -580,63 +776,8 @@ __global__ void __launch_bounds__(256, 1)
           // Last split to arrive: sum all partials in ascending split order, round once.
           __threadfence();
           const float4* p0 = args.partials + static_cast<size_t>(slot) * args.splits * (C::BM * BN / 4);
-          if (m < args.gm) {
-            // Walk (chunk, split) pairs q = c * splits + sp in order, two at a time,
-            // with the next two pairs' loads issued before the current ones are
-            // added: partials of one 32-column chunk are summed in ascending split
-            // order, and four chunk-splits of loads are in flight per thread.
-            const int S = args.splits;
-            int nch = BN / 32;
-            while (nch > 0 && n0 + (nch - 1) * 32 >= args.gn) --nch;
-            const int total = nch * S;
-            const size_t pstride = static_cast<size_t>(C::BM) * BN / 4;
-            float4 cur0[8], cur1[8], nxt0[8], nxt1[8];
-            auto load = [&](float4(&dst)[8], int q) {
-              if (q < total) {
-                const int c = q / S, sp = q - (q / S) * S;
-                const float4* src = p0 + sp * pstride + static_cast<size_t>(c * 8) * C::BM + row;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = __ldcg(src + j * C::BM);
-              }
-            };
-            float v[32];
-            auto consume = [&](const float4(&x)[8], int q) {
-              if (q < total) {
-                const int c = q / S, sp = q - (q / S) * S;
-                if (sp == 0) {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    v[4 * j] = x[j].x;
-                    v[4 * j + 1] = x[j].y;
-                    v[4 * j + 2] = x[j].z;
-                    v[4 * j + 3] = x[j].w;
-                  }
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    v[4 * j] += x[j].x;
-                    v[4 * j + 1] += x[j].y;
-                    v[4 * j + 2] += x[j].z;
-                    v[4 * j + 3] += x[j].w;
-                  }
-                }
-                if (sp == S - 1) store_row32(args, m, n0 + c * 32, v);
-              }
-            };
-            load(cur0, 0);
-            load(cur1, 1);
-#pragma unroll 1
-            for (int q = 0; q < total; q += 2) {
-              load(nxt0, q + 2);
-              load(nxt1, q + 3);
-              consume(cur0, q);
-              consume(cur1, q + 1);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                cur0[j] = nxt0[j];
-                cur1[j] = nxt1[j];
-              }
-            }
+          if (m0 < args.gm) {
+            reduce_split_tile<BN>(args, p0, lane, row - lane, m0, n0);
           }
           if (leader) atomicExch(&args.counters[slot], 0u);  // ready for the next launch
         }
@@ -662,15 +803,25 @@ __global__ void __launch_bounds__(256, 1)
 // Host-side launch of one instantiation (defined in the per-view .cu files).
 struct GemmLaunch {
   CUtensorMap tmA, tmB;
+  CUtensorMap tmB2;  // X3: B's bf16 lo plane (tmB is the hi plane); otherwise unused
   GemmArgs args;
   int grid;   // CTAs (twice the number of pairs for a paired plan)
   bool pair;  // clusters of two CTAs share each tile
-  bool x3;    // FP32 operands through the fused BF16x3 mode (router)
+  bool x3;    // router BF16x3 mode: FP32 A split in the kernel, B from pre-split planes
 };
 
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
 cudaError_t launch_gemm_km(int bn, const GemmLaunch& l, cudaStream_t stream);  // input gradient
 cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream);  // weight gradient
+// Router operand split: the bf16 hi/lo copies the BF16x3 GEMMs read (split_x3.cu).
+struct SplitJob {
+  const float* x;       // FP32 [rows][cols], leading dimension ldx (multiple of 4)
+  uint16_t* out;        // segment s of row r starts at out + s * seg_stride + r * ldo
+  int64_t rows, cols, ldx, ldo, seg_stride;
+  int32_t nseg;         // 2 or 3 segments
+  uint32_t lo_mask;     // bit s set: segment s holds lo = RNE(x - hi), else hi = RNE(x)
+};
+cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream);
 // Dynamic shared memory limits of each instantiation, on the current device.
 cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();
@@ -690,7 +841,7 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;  // single-CTA tiles launch without a cluster
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.args);
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.tmB2, l.args);
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>

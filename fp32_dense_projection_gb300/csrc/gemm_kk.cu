@@ -1,7 +1,8 @@
 // Instantiations of the GEMM for the forward: K-major A (X or dY), K-major B (W).
 // One translation unit per operand-major combination so the builds run in parallel.
 // BF16 operands: single-CTA tiles 128 x {64, 128, 256}, CTA-pair tiles 256 x {128, 256}.
-// FP32 router operands (fused BF16x3 split): single-CTA tiles 128 x {64, 128, 256}.
+// Router BF16x3 forward (FP32 X split in the kernel, W from pre-split planes):
+// single-CTA tiles 128 x {64, 128, 256}.
 #include "gemm_kernel.cuh"
 
 namespace dp {

@@ -1,7 +1,8 @@
 // Instantiations of the GEMM for the weight gradient: MN-major A (dY or X), MN-major B (X or dY).
 // One translation unit per operand-major combination so the builds run in parallel.
 // BF16 operands: single-CTA tiles 128 x {64, 128, 256}, CTA-pair tiles 256 x {128, 256}.
-// FP32 router operands (fused BF16x3 split): single-CTA tiles 128 x {64, 128, 256}.
+// Router BF16x3 (swapped weight gradient: FP32 X split in the kernel, dY from pre-split
+// planes): single-CTA tiles 128 x {64, 128, 256}.
 #include "gemm_kernel.cuh"
 
 namespace dp {

@@ -27,7 +27,7 @@ constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceBytesPerNs = 50.0;    // last-arriver read of the split partials (one SM)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
-constexpr double kX3Rate = 0.5;               // fused BF16x3: split work and shared-memory traffic per MMA
+constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -52,16 +52,21 @@ bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
     case kOpWgrad:  // dW[N,K] = dY[T,N]^T X[T,K] : A = dY (MN-major), B = X (MN-major)
       *v = {N, K, T, true, true, 2, 2};
       return true;
-    // Router: the same views on FP32 operands, each 32-wide block split into bf16
-    // hi/lo in shared memory and contracted with three MMAs.
+    // Router forward: A = X (FP32, split into bf16 hi/lo in the kernel), B = W's
+    // bf16 hi and lo planes (split once per call); three MMAs per 32-wide block.
     case kOpRouterFwd:
       *v = {T, N, K, false, false, 4, 4, 3, kRouterBlockK};
       return true;
+    // Router input gradient: the plain BF16 view over the concatenated operands
+    // dY' = [lo | hi | hi] (T x 3N) and W' = [hi; lo; hi] (3N x K).
     case kOpRouterDgrad:
-      *v = {T, K, N, false, true, 4, 4, 3, kRouterBlockK};
+      *v = {T, K, 3 * N, false, true, 2, 2};
       return true;
+    // Router weight gradient, always swapped: dW^T[K,N] = X^T dY with A = X (FP32,
+    // MN-major, split in the kernel) and B = dY's bf16 hi/lo planes (MN-major),
+    // stored transposed; X streams through the SMs once when N fits one tile.
     case kOpRouterWgrad:
-      *v = {N, K, T, true, true, 4, 4, 3, kRouterBlockK};
+      *v = {K, N, T, true, true, 4, 4, 3, kRouterBlockK};
       return true;
     default:
       return false;
@@ -85,13 +90,15 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn)) / (t.pair ? 2.0 : 1.0);
   const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
   const double flop_per_kb = 2.0 * kBlockM * t.bn * v.bk * v.terms;  // per SM, tensor-pipe work
-  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0) / (v.terms > 1 ? kX3Rate : 1.0);
+  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0);
+  // BF16x3: the converter warps split every A element of the block
+  const double t_split = v.terms > 1 ? kb * kBlockM * v.bk / kX3SplitPerNs : 0.0;
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
   const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
   const double t_load = kb * bytes_per_kb / bw;
   const double out_tile = a_rows * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * (split ? 4.0 : out_bytes);
-  return std::max(t_mma, t_load) + out_tile / dram;
+  return std::max(std::max(t_mma, t_load), t_split) + out_tile / dram;
 }
 
 // Modelled time of a plan: `full` whole-K units followed by (tiles - full) tiles
@@ -147,7 +154,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
     if (o.pair >= 0 && pair != o.pair) continue;
     if (pair && !kAutoPair && o.pair != 1) continue;
     if (pair && (sm < 2 || v.gm <= kBlockM)) continue;  // a pair needs two row blocks of work
-    if (pair && v.terms > 1) continue;                  // the fused BF16x3 mode is single-CTA
+    if (pair && v.terms > 1) continue;                  // the BF16x3 mode is single-CTA
     const int64_t slots = pair ? sm / 2 : sm;
     for (int bn : {256, 128, 64}) {
       if (pair && bn < 128) continue;  // each CTA of a pair holds bn / 2 >= 64 columns of B
@@ -194,6 +201,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.N = N;
   plan.K = K;
   plan.out_f32 = (op >= kOpRouterFwd) ? 1 : (out_f32 ? 1 : 0);
+  plan.swap = op == kOpRouterWgrad;  // the router's weight gradient is always computed transposed
   plan.a_mn = v.a_mn;
   plan.b_mn = v.b_mn;
   plan.nkb = ceil_div(v.gk, v.bk);
@@ -204,7 +212,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   c.have = true;  // empty problems: any tiling, no work units
   if (v.gm > 0 && plan.nkb > 0) {
     c.have = false;
-    if (o.swap != 1) search(v, plan.nkb, sm, out_bytes, o, &c);
+    // (the orientation override applies to the BF16 weight gradient only)
+    if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, o, &c);
     if (op == kOpWgrad && o.swap != 0) {
       // thin outputs: let K fill the 128-row tile side and N be the MMA's N
       const View sv = {K, N, T, true, true, 2, 2};
@@ -239,7 +248,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   const int64_t slots = plan.pair ? sm / 2 : sm;
   plan.grid = static_cast<int>(std::min<int64_t>(plan.units, slots) * (plan.pair ? 2 : 1));
 
-  // workspace layout: [counters | split partials]
+  // workspace layout: [counters | split partials | router's pre-split operands]
   size_t off = kCounterBytes;
   if (plan.splits > 1) {
     plan.off_counters = 0;
@@ -250,7 +259,29 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
                           kBlockM * plan.bn * sizeof(float);
     off += plan.bytes_partials;
   }
-  plan.ws_bytes = plan.splits > 1 ? round_up(off, 256) : 0;
+  const bool router = op >= kOpRouterFwd;
+  if (router && T > 0) {
+    auto region = [&](size_t bytes, size_t* at) {
+      off = round_up(off, 256);
+      *at = off;
+      off += bytes;
+      return bytes;
+    };
+    const size_t e = sizeof(uint16_t);
+    if (op == kOpRouterFwd) {  // W: hi and lo planes [N][K]
+      plan.ld_split_b = static_cast<int64_t>(round_up(K, 8));
+      plan.bytes_split_b = region(2 * static_cast<size_t>(N) * plan.ld_split_b * e, &plan.off_split_b);
+    } else if (op == kOpRouterWgrad) {  // dY: hi and lo planes [T][N]
+      plan.ld_split_b = static_cast<int64_t>(round_up(N, 8));
+      plan.bytes_split_b = region(2 * static_cast<size_t>(T) * plan.ld_split_b * e, &plan.off_split_b);
+    } else {  // dY' [T][3N] and W' [3N][K]
+      plan.ld_split_a = static_cast<int64_t>(round_up(3 * N, 8));
+      plan.bytes_split_a = region(static_cast<size_t>(T) * plan.ld_split_a * e, &plan.off_split_a);
+      plan.ld_split_b = static_cast<int64_t>(round_up(K, 8));
+      plan.bytes_split_b = region(3 * static_cast<size_t>(N) * plan.ld_split_b * e, &plan.off_split_b);
+    }
+  }
+  plan.ws_bytes = (plan.splits > 1 || (router && T > 0)) ? round_up(off, 256) : 0;
   *p = plan;
   return true;
 }

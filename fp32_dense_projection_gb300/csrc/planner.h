@@ -59,6 +59,11 @@ struct Plan {
   // a fixed region of kCounterBytes, then split partials
   size_t off_counters = 0, bytes_counters = 0;
   size_t off_partials = 0, bytes_partials = 0;
+  // router: bf16 hi/lo copies of the FP32 operands the kernel reads pre-split
+  // (forward: W; weight gradient: dY; input gradient: both, in concatenated form)
+  size_t off_split_a = 0, bytes_split_a = 0;
+  size_t off_split_b = 0, bytes_split_b = 0;
+  int64_t ld_split_a = 0, ld_split_b = 0;  // their leading dimensions (elements)
   size_t ws_bytes = 0;
 };
 
@@ -72,14 +77,21 @@ constexpr int stages_for_rows(int b_rows) {
 }
 constexpr int stages_for(int bn, bool pair = false) { return stages_for_rows(pair ? bn / 2 : bn); }
 
-// The FP32 router's fused BF16x3 GEMM streams 32-wide contraction blocks: per
-// stage an FP32 staging tile ((128 + bn) rows x 128 bytes, loaded by TMA) and its
-// bf16 hi/lo copy for the tensor core (the same bytes), so stages = 192 KB / twice that.
+// The FP32 router's BF16x3 GEMM (forward and weight gradient) streams 32-wide
+// contraction blocks.  The streamed FP32 operand A is loaded by TMA into a staging
+// ring (128 x 32 FP32 = 16 KB per stage) and split into bf16 hi/lo by converter
+// warps; the reused operand B arrives already split, as two bf16 planes.  A stage
+// of the MMA ring holds [A_hi | A_lo | B_hi | B_lo] ((128 + bn) x 32 x 2 x 2 bytes).
+// The staging ring is one stage deeper than the MMA ring; both fit in 208 KB.
 constexpr int kRouterBlockK = 32;
+constexpr int kX3StagingBytes = kBlockM * kRouterBlockK * 4;
+constexpr int x3_stage_bytes(int bn) { return (kBlockM + bn) * kRouterBlockK * 4; }
 constexpr int stages_x3(int bn) {
-  return (192 * 1024) / (2 * (kBlockM + bn) * kRouterBlockK * 4) < 8 ? (192 * 1024) / (2 * (kBlockM + bn) * kRouterBlockK * 4)
-                                                                     : 8;
+  return (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn) + kX3StagingBytes) < 6
+             ? (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn) + kX3StagingBytes)
+             : 6;
 }
+constexpr int staging_stages_x3(int bn) { return stages_x3(bn) + 1; }
 
 // Overrides of the planner's choices, for tests and tuning (all unset in normal
 // use): > 0 forces the tile width / uniform split count / last-wave split count;

@@ -325,6 +325,13 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core) before signalling that the data is ready.
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -57,9 +57,10 @@ SM = 152
 def test_plan_is_valid(op, T, N, K):
     p = dp.plan(op, T, N, K, out_f32=False, sm_count=SM)
     pair = bool(p["cta_pair"])
+    x3 = op in ("router_fwd", "router_wgrad")  # FP32 A split in the kernel, 32-wide blocks
     assert p["block_m"] == (256 if pair else 128)
-    assert p["block_k"] == (32 if op.startswith("router") else 64)  # router: fused split of 32-wide blocks
-    assert not (pair and op.startswith("router"))
+    assert p["block_k"] == (32 if x3 else 64)
+    assert not (pair and x3)
     assert p["block_n"] in ((128, 256) if pair else (64, 128, 256))
     slots = SM // 2 if pair else SM
     ctas_per_tile = 2 if pair else 1
@@ -74,19 +75,25 @@ def test_plan_is_valid(op, T, N, K):
     assert p["tiles_m"] * p["block_m"] >= p["gemm_m"] and p["tiles_n"] * p["block_n"] >= p["gemm_n"]
     bk = p["block_k"]
     assert p["k_blocks"] * bk >= p["gemm_k"] > (p["k_blocks"] - 1) * bk
-    mult = 1
-    if op.endswith("wgrad"):
+    if op == "router_wgrad":  # always transposed: dW^T = X^T dY
+        assert p["swap_ab"] == 1 and (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (K, N, T)
+        assert p["a_mn_major"] == 1 and p["b_mn_major"] == 1
+    elif op.endswith("wgrad"):
         if p["swap_ab"]:
-            assert op == "wgrad" and (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (K, N, T)
+            assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (K, N, T)
         else:
-            assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (N, K, mult * T)
+            assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (N, K, T)
         assert p["a_mn_major"] == 1 and p["b_mn_major"] == 1
     elif op.endswith("dgrad"):
-        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, K, mult * N)
+        # the router contracts the concatenated [lo | hi | hi] x [hi; lo; hi] operands
+        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, K, (3 if op == "router_dgrad" else 1) * N)
         assert p["a_mn_major"] == 0 and p["b_mn_major"] == 1
     else:
-        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, N, mult * K)
+        assert (p["gemm_m"], p["gemm_n"], p["gemm_k"]) == (T, N, K)
         assert p["a_mn_major"] == 0 and p["b_mn_major"] == 0
+    assert not p["swap_ab"] or op.endswith("wgrad")
+    if op.startswith("router"):  # the pre-split bf16 operands live in the workspace
+        assert p["workspace_bytes"] > 0
     # pure function: same answer twice, and the workspace query agrees
     assert dp.plan(op, T, N, K, sm_count=SM) == p
     assert dp.workspace_size(op, T, N, K, sm_count=SM) == p["workspace_bytes"]
@@ -207,8 +214,9 @@ def test_workspace_keeps_a_fixed_counter_region():
 @pytest.mark.parametrize("T", [1025, 16173, 16384, 65537, 200000])
 def test_accumulation_length_is_bounded(op, T):
     # no TMEM accumulator takes more than 16384 MMA accumulations per element: 16384
-    # contraction elements, or 16384 / 3 for the router's three BF16x3 terms
-    terms = 3 if op.startswith("router") else 1
+    # contraction elements, or 16384 / 3 for the three BF16x3 terms of the router's
+    # forward and weight gradient (its input gradient contracts over 3N elements)
+    terms = 3 if op in ("router_fwd", "router_wgrad") else 1
     for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
         p = dp.plan(op, T, N, K, sm_count=SM)
         per_split = -(-p["k_blocks"] // p["splits"]) * p["block_k"]

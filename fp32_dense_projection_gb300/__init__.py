@@ -122,10 +122,10 @@ def device_error(clear: bool = True) -> int:
 # ------------------------------------------------------------------ workspace
 
 class Workspace:
-    """A caller-owned, zero-initialised device workspace that grows on demand.
+    """A caller-owned device workspace that grows on demand.
 
-    The library needs the workspace zeroed before its first use only (its split
-    counters reset themselves); a grown buffer is a fresh zeroed tensor.
+    The library uses it as scratch (split partials, the router's bf16 operand
+    copies) and needs no initial value in it.
     """
 
     def __init__(self, device=None):
@@ -136,7 +136,7 @@ class Workspace:
         if nbytes == 0:
             return None
         if self.buf is None or self.buf.numel() < nbytes:
-            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         return self.buf
 
 

@@ -201,7 +201,6 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.out_trans = p.swap ? 1 : 0;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
-  a.counters = p.splits > 1 ? reinterpret_cast<uint32_t*>(w + p.off_counters) : nullptr;
   a.fault = dev.fault;
   l.grid = p.grid;
   l.pair = p.pair;
@@ -213,6 +212,9 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
     e = launch_gemm_km(p.bn, l, stream);
   else if (p.a_mn && p.b_mn)
     e = launch_gemm_mm(p.bn, l, stream);
+  // split tiles: the ordered sum of their partials, queued behind the GEMM
+  const int64_t split_tiles = p.tiles_m * p.tiles_n - p.full_units;
+  if (e == cudaSuccess && p.splits > 1 && split_tiles > 0) e = launch_split_reduce(l, p.bn, p.pair, split_tiles, stream);
   return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
 }
 

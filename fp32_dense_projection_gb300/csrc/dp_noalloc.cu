@@ -5,24 +5,22 @@
 // serving or real-time runtime that reserves all device memory at start-up, or a
 // plugin whose host forbids cudaMalloc on its hot path because it can
 // synchronise the device.  For them this entry point runs the same weight-gradient
-// kernel as dp_gemm_wgrad_ex, with its split partials and counters placed in a
-// scratch array that is part of the library image itself.
+// kernels as dp_gemm_wgrad_ex, with its split partials placed in a scratch array
+// that is part of the library image itself.
 //
 // The scratch array is a file-scope __device__ array of kScratchBytes.  Every GPU
 // that loads this part of the library holds it until the process exits.  In host
 // code its name is only a stand-in for the device symbol, so its device address
 // is looked up once per device, with that device current, via
 // cudaGetSymbolAddress; the first call on each device does this set-up and should
-// therefore come before any stream capture.  Every call shares the one array and
-// finds the previous call's contents there: the call clears the split counters
-// (which must start at zero) on its stream before the kernel runs, and calls that
-// overlap on the GPU (two streams, two threads) race on the array.
+// therefore come before any stream capture.  Every call shares the one array (the
+// partials need no initial value), so calls that overlap on the GPU (two streams,
+// two threads) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "dp_gemm.h"
-#include "planner.h"
 
 namespace {
 
@@ -60,7 +58,5 @@ extern "C" dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const vo
   if (need > kScratchBytes) return DP_ERR_WORKSPACE;  // beyond the built-in 64 MiB scratch
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != DP_OK) return st;
-  if (need > 0 && cudaMemsetAsync(scratch, 0, dp::kCounterBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return DP_ERR_LAUNCH;
   return dp_gemm_wgrad_ex(dY, ldg, X, ldx, dW, ldw, T, N, K, out, deterministic, scratch, kScratchBytes, stream);
 }

@@ -54,8 +54,7 @@ struct GemmArgs {
   int64_t ldo;         // output leading dimension (elements)
   int32_t out_f32;     // 1: FP32 output, 0: BF16 output
   int32_t out_trans;   // 1: D[m][n] is stored at out[n * ldo + m] (swapped weight gradient)
-  float4* partials;    // split partial tiles: [split tile][split][BN/4][128] float4
-  uint32_t* counters;  // split arrival counters, one per split tile (self-resetting)
+  float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
 
@@ -105,10 +104,25 @@ struct TileCfg {
 struct Unit {
   int tm, tn;    // output tile coordinates
   int s;         // split index (0 for whole-K units)
-  int ptile;     // slot of a split tile in the partial / counter arrays
+  int ptile;     // index of a split tile among the split tiles (its partials' slot)
   int kb0, kb1;  // contraction blocks [kb0, kb1)
-  bool split;    // partial result: goes through the ordered reduction
+  bool split;    // partial result: summed by the ordered reduction kernel
 };
+
+// Output tile index -> (row tile, column tile) under the grouped raster.
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int* tm, int* tn) {
+  const int fast_tiles = a.raster_m ? a.tiles_m : a.tiles_n;  // dimension grouped, fastest
+  const int slow_tiles = a.raster_m ? a.tiles_n : a.tiles_m;
+  const int per_group = a.group * slow_tiles;
+  const int g = tile / per_group;
+  const int first = g * a.group;
+  const int width = min(a.group, fast_tiles - first);
+  const int local = tile - g * per_group;
+  const int fast = first + local % width;
+  const int slow = local / width;
+  *tm = a.raster_m ? fast : slow;
+  *tn = a.raster_m ? slow : fast;
+}
 
 __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
   Unit r;
@@ -130,17 +144,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
     r.kb1 = static_cast<int>(static_cast<int64_t>(r.s + 1) * a.nkb / a.splits);
     r.split = a.splits > 1;
   }
-  const int fast_tiles = a.raster_m ? a.tiles_m : a.tiles_n;  // dimension grouped, fastest
-  const int slow_tiles = a.raster_m ? a.tiles_n : a.tiles_m;
-  const int per_group = a.group * slow_tiles;
-  const int g = tile / per_group;
-  const int first = g * a.group;
-  const int width = min(a.group, fast_tiles - first);
-  const int local = tile - g * per_group;
-  const int fast = first + local % width;
-  const int slow = local / width;
-  r.tm = a.raster_m ? fast : slow;
-  r.tn = a.raster_m ? slow : fast;
+  tile_coords(a, tile, &r.tm, &r.tn);
   return r;
 }
 
@@ -247,100 +251,6 @@ __device__ __forceinline__ void store_block32(const GemmArgs& a, uint32_t buf, i
   flush_block32(a, buf, lane, m0, col0);
 }
 
-// Ordered reduction of one split tile's partials by its last-arriving CTA, for the
-// 32 rows [m0, m0 + 32) of one epilogue warp (rows wrow.. of the CTA's partial
-// tiles).  (Chunk, split) pairs qq = c * splits + sp are walked in order, two at a
-// time, with the next two pairs' loads issued before the current ones are added:
-// partials of one 32-column chunk are summed in ascending split order, in FP32,
-// rounded once, and four chunk-splits of loads are in flight per thread.
-// Lane layout: for the row-major output value i of a lane is row 4i + lane/8,
-// float4 column chunk lane%8 of the 32-column chunk, so each store instruction
-// writes four whole 128-byte row segments; for the transposed store it is row
-// `lane`, chunk i, so consecutive lanes write consecutive elements of each output
-// row.  Both are linear in i: row = r0 + i * dr, chunk = c0 + i * dc.
-template <int BN>
-__device__ __forceinline__ void reduce_split_tile(const GemmArgs& args, const float4* p0, int lane, int wrow,
-                                                  int64_t m0, int64_t n0) {
-  constexpr int BM = kBlockM;
-  const bool tr = args.out_trans != 0;
-  const int r0 = tr ? lane : (lane >> 3), dr = tr ? 0 : 4;
-  const int c0 = tr ? 0 : (lane & 7), dc = tr ? 1 : 0;
-  const int64_t rows_left = args.gm - m0;
-  const int S = args.splits;
-  int nch = BN / 32;
-  while (nch > 0 && n0 + (nch - 1) * 32 >= args.gn) --nch;
-  const int total = nch * S;
-  const size_t pstride = static_cast<size_t>(BM) * BN / 4;
-  const float4* lane_base = p0 + wrow + c0 * BM + r0;
-  const int istep = dc * BM + dr;  // float4 distance between a lane's values i and i + 1
-  float4 cur0[8], cur1[8], nxt0[8], nxt1[8];
-  // (padding rows of a thin tile hold no partials: their sums are never stored)
-  auto load = [&](float4(&dst)[8], int qq) {
-    if (qq < total) {
-      const int c = qq / S, sp = qq - (qq / S) * S;
-      const float4* src = lane_base + sp * pstride + static_cast<size_t>(c * 8) * BM;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = __ldcg(src + i * istep);
-    }
-  };
-  float4 acc[8];
-  auto consume = [&](const float4(&x)[8], int qq) {
-    if (qq < total) {
-      const int c = qq / S, sp = qq - (qq / S) * S;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (sp == 0) {
-          acc[i] = x[i];
-        } else {
-          acc[i].x += x[i].x;
-          acc[i].y += x[i].y;
-          acc[i].z += x[i].z;
-          acc[i].w += x[i].w;
-        }
-      }
-      if (sp == S - 1) {
-        const int64_t col = n0 + c * 32;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = r0 + i * dr;
-          const int64_t cc = col + 4 * (c0 + i * dc);
-          if (r >= rows_left || cc >= args.gn) continue;
-          if (tr) {
-            const float e[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int64_t o = (cc + t) * args.ldo + m0 + r;
-              if (args.out_f32)
-                static_cast<float*>(args.out)[o] = e[t];
-              else
-                static_cast<uint16_t*>(args.out)[o] = static_cast<uint16_t>(pack_bf16x2(e[t], 0.0f) & 0xFFFFu);
-            }
-          } else if (args.out_f32) {
-            *reinterpret_cast<float4*>(static_cast<float*>(args.out) + (m0 + r) * args.ldo + cc) = acc[i];
-          } else {
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(args.out) + (m0 + r) * args.ldo + cc) =
-                make_uint2(pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
-          }
-        }
-      }
-    }
-  };
-  load(cur0, 0);
-  load(cur1, 1);
-#pragma unroll 1
-  for (int qq = 0; qq < total; qq += 2) {
-    load(nxt0, qq + 2);
-    load(nxt1, qq + 3);
-    consume(cur0, qq);
-    consume(cur1, qq + 1);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      cur0[i] = nxt0[i];
-      cur1[i] = nxt1[i];
-    }
-  }
-}
-
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -367,7 +277,6 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + STAGES * C::STAGE_BYTES + SSTAGES * C::SA_BYTES +
                                                     C::EPI_BYTES + C::NUM_BARS * 8);
   volatile uint32_t* flag_wait = tmem_slot + 2;  // [2], double-buffered by unit parity
-  volatile uint32_t* flag_last = tmem_slot + 4;  // [2]
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -412,6 +321,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) pdl_launch_dependents();  // the split reduction may queue up behind this grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -765,22 +675,6 @@ __global__ void __launch_bounds__(256, 1)
                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
           }
         }
-        __threadfence();
-        named_sync(1, 128);
-        if (leader) {
-          const uint32_t before = atomicAdd(&args.counters[slot], 1u);
-          flag_last[local & 1] = (before == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
-        }
-        named_sync(1, 128);
-        if (flag_last[local & 1]) {
-          // Last split to arrive: sum all partials in ascending split order, round once.
-          __threadfence();
-          const float4* p0 = args.partials + static_cast<size_t>(slot) * args.splits * (C::BM * BN / 4);
-          if (m0 < args.gm) {
-            reduce_split_tile<BN>(args, p0, lane, row - lane, m0, n0);
-          }
-          if (leader) atomicExch(&args.counters[slot], 0u);  // ready for the next launch
-        }
       }
     }
   }
@@ -822,6 +716,9 @@ struct SplitJob {
   uint32_t lo_mask;     // bit s set: segment s holds lo = RNE(x - hi), else hi = RNE(x)
 };
 cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream);
+// Ordered sum of the split partials a GEMM launch wrote (split_reduce.cu): for each
+// split tile, partials s = 0..splits-1 added in that order in FP32, rounded once.
+cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t split_tiles, cudaStream_t stream);
 // Dynamic shared memory limits of each instantiation, on the current device.
 cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();

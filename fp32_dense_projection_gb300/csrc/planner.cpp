@@ -25,7 +25,8 @@ constexpr double kFlopPerNsPerSm = 12500.0;   // dense BF16 tensor rate per SM
 constexpr double kL2BytesPerNsPerSm = 160.0;  // operand bytes an SM pulls when they hit in L2
 constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
-constexpr double kReduceBytesPerNs = 50.0;    // last-arriver read of the split partials (one SM)
+constexpr double kReduceNs = 2000.0;          // the split reduction kernel's launch and one L2 round trip
+constexpr double kReduceBytesPerNs = 4000.0;  // partial bytes it sums per ns (whole GPU, L2-resident)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
@@ -103,8 +104,8 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
 
 // Modelled time of a plan: `full` whole-K units followed by (tiles - full) tiles
 // split `splits` ways, run by min(units, slots) persistent CTAs (or pairs); never
-// faster than the unique operand bytes cross from DRAM; split tiles end with one
-// CTA per (half) tile reading all of its partials.
+// faster than the unique operand bytes cross from DRAM; split plans add the
+// reduction kernel that sums the partials.
 double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes) {
   const int64_t slots = t.pair ? sm / 2 : sm;
   const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
@@ -125,9 +126,10 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
             unit_ns(v, t, ceil_div(nkb, splits), splits > 1, active_sms, reuse, out_bytes);
   const double t_dram = (unique + static_cast<double>(v.gm) * v.gn * out_bytes) / kHbmBytesPerNs;
   time = std::max(time, t_dram);
-  if (splits > 1 && split_units > 0)
-    time += splits * std::min<double>(kBlockM, a_rows) * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0 /
-            kReduceBytesPerNs;
+  if (splits > 1 && split_units > 0)  // every split tile's partials, summed by the reduction kernel
+    time += kReduceNs + static_cast<double>(tiles - full) * (t.pair ? 2 : 1) * splits *
+                            std::min<double>(kBlockM, a_rows) * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) *
+                            4.0 / kReduceBytesPerNs;
   return time;
 }
 
@@ -162,7 +164,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       if (o.bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
       const Tiling t = {bn, pair != 0};
       const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, bn);
-      const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // counters / partial slots: one per CTA tile
+      const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // partial slots: one per CTA tile
       // bounded accumulation length, unless the tiles are too many to split at all
       // (then whole K per tile: a longer running sum, the only case without the bound)
       // (kMaxAccumBlocks counts 64-element blocks of one MMA each; BF16x3 accumulates three)
@@ -173,7 +175,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0; ++s) {
         if (o.splits > 0 && s != std::min<int64_t>(o.splits, nkb)) continue;
         if (o.splits <= 0 && s > min_s && tiles * s > 4LL * slots) break;  // beyond 4 waves never pays
-        if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // one counter per CTA tile
+        if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // bounded partial workspace
         consider(t, s == 1 ? tiles : 0, s, model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes));
       }
       // whole-K tiles for the full waves, the last partial wave's tiles split
@@ -248,11 +250,9 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   const int64_t slots = plan.pair ? sm / 2 : sm;
   plan.grid = static_cast<int>(std::min<int64_t>(plan.units, slots) * (plan.pair ? 2 : 1));
 
-  // workspace layout: [counters | split partials | router's pre-split operands]
-  size_t off = kCounterBytes;
+  // workspace layout: [split partials | router's pre-split operands]
+  size_t off = 0;
   if (plan.splits > 1) {
-    plan.off_counters = 0;
-    plan.bytes_counters = kCounterBytes;
     // one FP32 partial per split of every split tile, per CTA of the tile
     plan.off_partials = off;
     plan.bytes_partials = static_cast<size_t>(tiles - plan.full_units) * (plan.pair ? 2 : 1) * plan.splits *

@@ -24,10 +24,9 @@ enum Op : int {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
-// The first kCounterBytes of every non-empty workspace hold the split arrival
-// counters (one uint32 per output tile of a split plan).  Nothing else is ever
-// written there, so one zero-filled workspace can serve every op in turn: each
-// split launch returns its counters to zero.
+// Most split tiles (tiles whose contraction is split, times CTAs per tile) a plan
+// may have; beyond that the whole contraction stays in each tile, which bounds the
+// workspace the FP32 partials take.
 constexpr int kMaxSplitTiles = 4096;
 // Longest contraction one TMEM accumulator sums, in 64-wide blocks (16384 tokens).
 // The tensor core rounds each FP32 accumulate toward zero, so the error of a
@@ -35,7 +34,6 @@ constexpr int kMaxSplitTiles = 4096;
 // output of the 65537-token weight gradient fell outside the pages' budget.
 // Longer contractions are split (fixed partition, partials summed in order).
 constexpr int kMaxAccumBlocks = 256;
-constexpr size_t kCounterBytes = kMaxSplitTiles * sizeof(uint32_t);
 
 struct Plan {
   int op = 0;
@@ -55,9 +53,8 @@ struct Plan {
   // units [0, full_units) are whole-K tiles; the remaining tiles are split
   // `splits` ways (all tiles when full_units = 0, the last partial wave otherwise)
   int64_t full_units = 0;
-  // workspace layout (byte offsets from the workspace base): counters first, in
-  // a fixed region of kCounterBytes, then split partials
-  size_t off_counters = 0, bytes_counters = 0;
+  // workspace layout (byte offsets from the workspace base): split partials, then
+  // the router's split operands
   size_t off_partials = 0, bytes_partials = 0;
   // router: bf16 hi/lo copies of the FP32 operands the kernel reads pre-split
   // (forward: W; weight gradient: dY; input gradient: both, in concatenated form)

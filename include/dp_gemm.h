@@ -38,10 +38,15 @@
  * Ownership.  The caller owns every buffer, the workspace and the stream.  The
  *   library never allocates device memory, never synchronises and never frees.
  * Workspace.  `workspace` is caller-provided device memory of at least
- *   dp_workspace_size(...) bytes (may be NULL when that size is 0).  It must be
- *   zero-filled once before its first use; the library leaves it reusable (the
- *   split counters it holds reset themselves).  One workspace must not be used by
- *   two calls that may run concurrently.
+ *   dp_workspace_size(...) bytes (may be NULL when that size is 0).  It is
+ *   scratch: FP32 partial tiles of split contractions and the router's bf16
+ *   hi/lo operand copies, written before they are read within the call, so it
+ *   needs no initial value.  One workspace must not be used by two calls that may
+ *   run concurrently.
+ * Launches.  Each call enqueues one GEMM kernel; a plan that splits contractions
+ *   adds the kernel that sums the partials (launched as a programmatic dependent
+ *   of the GEMM), and a router call adds the kernel that splits its reused FP32
+ *   operand into bf16 hi/lo before the GEMM.
  * Stream.  `stream` is a cudaStream_t (NULL = legacy default stream).  All work
  *   is enqueued on it; calls return before the GPU finishes.  Calls are legal
  *   inside CUDA stream capture after the first call on the device (which sets
@@ -141,16 +146,15 @@ dp_status dp_gemm_wgrad_ex(const void* dY, int64_t ldg, const void* X, int64_t l
  * while a step is captured into a CUDA graph, a serving runtime that reserves all
  * device memory at start-up, or a plugin whose host forbids cudaMalloc on its hot
  * path because it can synchronise the device.  This call computes exactly what
- * dp_gemm_wgrad_ex computes (same plan, same kernel, same bits) but keeps its
- * split partials and counters in a 64 MiB scratch array built into the library,
+ * dp_gemm_wgrad_ex computes (same plan, same kernels, same bits) but keeps its
+ * split partials in a 64 MiB scratch array built into the library,
  * which every GPU that loads the library holds until the process exits.  The
  * caller still passes dY, X and dW.  Arguments and errors as dp_gemm_wgrad_ex;
  * a shape whose plan needs more than 64 MiB of scratch returns DP_ERR_WORKSPACE
  * (dp_workspace_size(DP_OP_WGRAD, ...) tells beforehand).  The first call on each
  * device looks up the array's device address and should come before any stream
- * capture.  Every call shares the one array and clears its split counters on
- * `stream` before the kernel; calls that overlap on the GPU (different streams or
- * threads) race on it and must be serialised by the caller.  No cudaMalloc,
+ * capture.  Every call shares the one array; calls that overlap on the GPU
+ * (different streams or threads) race on it and must be serialised by the caller.  No cudaMalloc,
  * cudaFree or allocating library routine is called. */
 dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int64_t ldx,
                                 void* dW, int64_t ldw,

@@ -202,12 +202,21 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
         dp.lib()
 
 
-def test_workspace_keeps_a_fixed_counter_region():
-    # every non-empty workspace starts with the 16 KB split-counter region
+def test_workspace_only_when_needed():
+    # the workspace holds split partials (one 128 x block_n FP32 tile per split of each
+    # split tile and CTA) and the router's bf16 operand copies; plain unsplit plans need none
     for op in dp.OP_NAMES:
         for T, N, K in ((64, 1024, 4096), (1024, 256, 4096), (65537, 64, 4096), (16384, 12288, 4096)):
+            p = dp.plan(op, T, N, K, sm_count=SM)
             n = dp.workspace_size(op, T, N, K, sm_count=SM)
-            assert n == 0 or n >= 16384
+            tiles = p["tiles_m"] * p["tiles_n"]
+            partials = (tiles - p["full_units"]) * (2 if p["cta_pair"] else 1) * p["splits"] * 128 * p["block_n"] * 4
+            if op.startswith("router"):
+                assert n > partials
+            elif p["splits"] > 1:
+                assert n >= partials > 0
+            else:
+                assert n == 0
 
 
 @pytest.mark.parametrize("op", list(dp.OP_NAMES))
@@ -220,5 +229,5 @@ def test_accumulation_length_is_bounded(op, T):
     for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
         p = dp.plan(op, T, N, K, sm_count=SM)
         per_split = -(-p["k_blocks"] // p["splits"]) * p["block_k"]
-        if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else no counters: whole K
+        if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else whole K (bounded workspace)
             assert per_split * terms <= 16384 + p["block_k"] * terms, (op, T, N, K, p)

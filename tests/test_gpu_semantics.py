@@ -76,6 +76,22 @@ def test_graph_replay_matches_eager(op, T, N, K):
     no_device_fault()
 
 
+@pytest.mark.parametrize("op,T,N,K", CASES)
+def test_workspace_needs_no_initial_value(op, T, N, K):
+    # the workspace is scratch: a workspace full of NaN bit patterns gives the same
+    # bits as a zeroed one
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K).items()}
+    a, b = operands(op, c)
+    need = max(1, dp.workspace_size(op, T, N, K, out_f32=True))
+    clean = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    dirty = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    kw = {} if op.startswith("router") else {"out_dtype": torch.float32}
+    want = gpu(op, a, b, workspace=clean, **kw)
+    got = gpu(op, a, b, workspace=dirty, **kw)
+    assert torch.equal(got.view(torch.int32), want.view(torch.int32))
+    no_device_fault()
+
+
 @pytest.mark.parametrize("op,T,N,K", [("fwd", 200, 256, 512), ("dgrad", 200, 256, 512), ("wgrad", 200, 256, 512),
                                       ("wgrad", 4100, 64, 1024), ("router_fwd", 100, 256, 512),
                                       ("router_dgrad", 100, 256, 512), ("router_wgrad", 100, 256, 512)])
@@ -168,9 +184,9 @@ def test_status_codes():
 
 
 def test_one_workspace_serves_every_op_in_turn():
-    # Non-split router calls write operand copies into the workspace; split calls keep
-    # arrival counters in its first bytes.  A sequence mixing them on one zeroed
-    # workspace must give the same bits as each call on a fresh workspace.
+    # Router calls write bf16 operand copies into the workspace and split calls write
+    # FP32 partials.  A sequence mixing them on one workspace must give the same bits
+    # as each call on a fresh one: nothing a call reads is left over from another.
     seq = [("router_dgrad", 1024, 256, 4096), ("router_wgrad", 1024, 256, 4096), ("fwd", 64, 1024, 4096),
            ("router_fwd", 256, 256, 4096), ("wgrad", 16173, 64, 4096), ("router_wgrad", 1024, 256, 4096),
            ("fwd", 64, 1024, 4096)]

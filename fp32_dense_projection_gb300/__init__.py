@@ -46,7 +46,7 @@ class PlanInfo(ctypes.Structure):
         "block_m", "block_n", "block_k", "stages", "splits", "raster_group", "grid",
         "a_mn_major", "b_mn_major", "swap_ab", "cta_pair", "raster_rows", "reserved")] + [(n, ctypes.c_int64) for n in (
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
-        ("workspace_bytes", ctypes.c_uint64)]
+        ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double)]
 
 
 def lib():
@@ -171,11 +171,8 @@ def _stream(device: torch.device, stream):
 
 
 def _ws(op, T, N, K, out_f32, device, workspace):
-    need = workspace_size(op, T, N, K, out_f32)
-    if workspace is None:
-        buf = _default_workspace(device).get(need)
-    else:
-        buf = workspace
+    # a caller's workspace goes straight through (the library checks its size)
+    buf = _default_workspace(device).get(workspace_size(op, T, N, K, out_f32)) if workspace is None else workspace
     nbytes = 0 if buf is None else buf.numel() * buf.element_size()
     return buf, nbytes
 
@@ -197,17 +194,21 @@ def _gemm(op: int, name: str, a: torch.Tensor, b: torch.Tensor, out_shape, out, 
         raise ValueError(f"{name}: out must be {tuple(out_shape)} {out_dtype}")
     out_f32 = out.dtype == torch.float32
     buf, nbytes = _ws(op, T, N, K, out_f32, device, workspace)
-    L = lib()
-    with torch.cuda.device(device):
+    fn = getattr(lib(), name + "_ex")
+
+    def call():
         st = _stream(device, stream)
         if router:
-            fn = getattr(L, name + "_ex")
-            status = fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K, int(bool(deterministic)),
-                        _ptr(buf), nbytes, st)
-        else:
-            fn = getattr(L, name + "_ex")
-            status = fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K,
-                        DP_OUT_F32 if out_f32 else DP_OUT_BF16, int(bool(deterministic)), _ptr(buf), nbytes, st)
+            return fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K, int(bool(deterministic)),
+                      _ptr(buf), nbytes, st)
+        return fn(_ptr(a), _ld(a), _ptr(b), _ld(b), _ptr(out), _ld(out), T, N, K,
+                  DP_OUT_F32 if out_f32 else DP_OUT_BF16, int(bool(deterministic)), _ptr(buf), nbytes, st)
+
+    if device.index == torch.cuda.current_device():
+        status = call()
+    else:
+        with torch.cuda.device(device):
+            status = call()
     _check(status, name)
     return out
 

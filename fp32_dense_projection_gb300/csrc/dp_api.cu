@@ -97,8 +97,8 @@ EncodeTiledFn encode_fn() {
 // Map over a row-major [rows][cols] matrix (leading dimension ld elements) of bf16
 // (box = box_rows x 64 columns) or FP32 (box = box_rows x 32 columns): 128-byte
 // box rows, 128-byte swizzle, zero fill outside the matrix.
-bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
-              bool f32 = false, uint32_t box_cols = 0, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+                bool f32, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -108,6 +108,83 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
   return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over the same matrix for MN-major tiles: dimensions (inner, rows,
+// cols / inner) with strides (ld, inner) elements, box (inner, box_rows, groups):
+// a tile of `groups` column groups of `inner` columns arrives as [group][row][inner]
+// (the layout the kernel's MN-major tiles use) in one load.  Only for cols a
+// multiple of inner, so every group lies inside the rows.
+bool encode_map3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t inner,
+                 uint32_t box_rows, uint32_t groups, bool f32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || cols % inner != 0) return false;
+  const int es = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {inner, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / inner)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es, static_cast<cuuint64_t>(inner) * es};
+  const cuuint32_t box[3] = {inner, box_rows, groups};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Host-path caches.  A training or serving loop calls the same shapes on the same
+// buffers again and again; the plan (a pure function of the shape) and the tensor
+// maps (a pure function of pointer, shape, stride and box) are kept per thread in
+// small direct-mapped tables, so a repeated call skips the planner's search and
+// the driver's map encoding.  (FlashInfer page "cache the router entry points'
+// calls by their own tensors": the pages cache the router entry points' host work
+// per call signature for the same reason.)
+struct MapKey {
+  const void* ptr;
+  int64_t rows, cols, ld;
+  uint32_t box_rows, box_cols;
+  int f32, swizzle;
+  uint32_t groups;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows &&
+           box_cols == o.box_cols && f32 == o.f32 && swizzle == o.swizzle && groups == o.groups;
+  }
+};
+
+uint64_t mix(uint64_t h, uint64_t v) {
+  h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+  return h;
+}
+
+constexpr int kMapCacheSize = 256;  // entries per thread (power of two)
+constexpr int kPlanCacheSize = 64;
+
+struct MapEntry {
+  bool valid = false;
+  MapKey key;
+  CUtensorMap map;
+};
+thread_local MapEntry t_maps[kMapCacheSize];
+
+// groups > 0: the 3-D map of encode_map3 with inner = box_cols (or 64 / 32 columns).
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
+              bool f32 = false, uint32_t box_cols = 0, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+              uint32_t groups = 0) {
+  const MapKey k = {ptr, rows, cols, ld, box_rows, box_cols, f32 ? 1 : 0, static_cast<int>(swizzle), groups};
+  uint64_t h = mix(mix(mix(reinterpret_cast<uintptr_t>(ptr), static_cast<uint64_t>(rows)), static_cast<uint64_t>(cols)),
+                   static_cast<uint64_t>(ld));
+  h = mix(mix(h, box_rows | (static_cast<uint64_t>(box_cols) << 32)),
+          static_cast<uint64_t>(k.f32 * 16 + k.swizzle) | (static_cast<uint64_t>(groups) << 8));
+  MapEntry& e = t_maps[h & (kMapCacheSize - 1)];
+  if (e.valid && e.key == k) {
+    *map = e.map;
+    return true;
+  }
+  const bool ok = groups > 0 ? encode_map3(map, ptr, rows, cols, ld, box_cols ? box_cols : (f32 ? 32u : 64u), box_rows,
+                                            groups, f32)
+                             : encode_map(map, ptr, rows, cols, ld, box_rows, f32, box_cols, swizzle);
+  if (!ok) return false;
+  e.valid = true;
+  e.key = k;
+  e.map = *map;
+  return true;
 }
 
 // ------------------------------------------------------------ argument checks
@@ -134,6 +211,15 @@ int env_int(const char* name) {
 // DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS (> 0 forces), DP_FORCE_SWAP (0 or 1: the
 // weight-gradient orientation) and DP_FORCE_PAIR (0 or 1: single-CTA or CTA-pair
 // tiles).  Unset in normal use.
+struct PlanEntry {
+  bool valid = false;
+  int op, out_f32, sm;
+  int64_t T, N, K;
+  Overrides o;
+  Plan plan;
+};
+thread_local PlanEntry t_plans[kPlanCacheSize];
+
 bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan) {
   const char* sw = std::getenv("DP_FORCE_SWAP");
   const char* pr = std::getenv("DP_FORCE_PAIR");
@@ -143,7 +229,29 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
   o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
   o.swap = sw ? std::atoi(sw) : -1;
   o.pair = pr ? std::atoi(pr) : -1;
-  return make_plan(op, T, N, K, out_f32, sm, plan, o);
+  uint64_t h = mix(mix(mix(static_cast<uint64_t>(op), static_cast<uint64_t>(T)), static_cast<uint64_t>(N)),
+                   static_cast<uint64_t>(K));
+  h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
+          static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
+              (o.swap + 1) * 3 + (o.pair + 1));
+  PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
+  if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
+      e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
+      e.o.pair == o.pair) {
+    *plan = e.plan;
+    return true;
+  }
+  if (!make_plan(op, T, N, K, out_f32, sm, plan, o)) return false;
+  e.valid = true;
+  e.op = op;
+  e.T = T;
+  e.N = N;
+  e.K = K;
+  e.out_f32 = out_f32;
+  e.sm = sm;
+  e.o = o;
+  e.plan = *plan;
+  return true;
 }
 
 dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
@@ -171,14 +279,21 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   // operands boxes of 64 (bf16) or 32 (FP32) tile columns x bk contraction rows.
   const uint32_t kb_rows = static_cast<uint32_t>(p.bk);
   const uint32_t b_rows = static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn);
-  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, x3)
+  // MN-major tiles load as one 3-D box when the matrix's columns are whole groups
+  const uint32_t a_inner = x3 ? 32u : 64u;
+  const bool a3d = p.a_mn && p.gm % a_inner == 0;
+  const bool b3d = p.b_mn && p.gn % 64 == 0;
+  const uint32_t a_groups = a3d ? kBlockM / a_inner : 0u, b_groups = b3d ? b_rows / 64 : 0u;
+  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, x3, 0, CU_TENSOR_MAP_SWIZZLE_128B, a_groups)
                            : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, x3);
   bool ok_b;
   if (!x3) {
-    ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows) : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows);
+    ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, false, 0, CU_TENSOR_MAP_SWIZZLE_128B, b_groups)
+                  : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows);
     l.tmB2 = l.tmB;
   } else if (p.b_mn) {  // 64-column groups of 32 rows, 128-byte swizzle
-    ok_b = make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows) && make_map(&l.tmB2, B_lo, p.gk, p.gn, ldb, kb_rows);
+    ok_b = make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, false, 0, CU_TENSOR_MAP_SWIZZLE_128B, b_groups) &&
+           make_map(&l.tmB2, B_lo, p.gk, p.gn, ldb, kb_rows, false, 0, CU_TENSOR_MAP_SWIZZLE_128B, b_groups);
   } else {  // rows of 32 contraction elements (64 bytes), 64-byte swizzle
     ok_b = make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows, false, kb_rows, CU_TENSOR_MAP_SWIZZLE_64B) &&
            make_map(&l.tmB2, B_lo, p.gn, p.gk, ldb, b_rows, false, kb_rows, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -199,6 +314,8 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.ldo = ldo;
   a.out_f32 = p.out_f32;
   a.out_trans = p.swap ? 1 : 0;
+  a.a3d = a3d ? 1 : 0;
+  a.b3d = b3d ? 1 : 0;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;
@@ -418,6 +535,7 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
   info->units = p.units;
   info->full_units = p.full_units;
   info->workspace_bytes = T == 0 ? 0 : p.ws_bytes;
+  info->model_us = p.model_ns * 1e-3;
   return DP_OK;
 }
 
@@ -474,6 +592,6 @@ const char* dp_status_string(dp_status status) {
   }
 }
 
-int dp_version(void) { return 100; }
+int dp_version(void) { return 110; }
 
 }  // extern "C"

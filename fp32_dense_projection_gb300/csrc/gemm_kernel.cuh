@@ -54,6 +54,9 @@ struct GemmArgs {
   int64_t ldo;         // output leading dimension (elements)
   int32_t out_f32;     // 1: FP32 output, 0: BF16 output
   int32_t out_trans;   // 1: D[m][n] is stored at out[n * ldo + m] (swapped weight gradient)
+  // MN-major operands whose tensor map is 3-D, [column group][contraction row][128 B]:
+  // the groups of a tile arrive in one load instead of one load per group
+  int32_t a3d, b3d;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
@@ -80,6 +83,9 @@ struct TileCfg {
   static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // one FP32 staging tile of A (X3)
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EPI_BYTES = 4 * 4096;  // a 32 x 32 FP32 output block per epilogue warp
+  // X3: four converter warps (2, 3, 8, 9: one per SM sub-partition) split A
+  static constexpr int CONV_WARPS = X3 ? 4 : 0;
+  static constexpr int THREADS = X3 ? 320 : 256;
   // full, empty, tmem_full x2, tmem_empty x2, drain (+ staging full / empty for X3)
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SSTAGES;
   static constexpr int SMEM_BYTES =
@@ -252,7 +258,7 @@ __device__ __forceinline__ void store_block32(const GemmArgs& a, uint32_t buf, i
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
   using C = TileCfg<BN, PAIR, X3>;
@@ -291,12 +297,12 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), X3 ? 3 : 1);  // X3: the B loads' arrival and one per converter warp
+      mbar_init(full_bar(s), X3 ? 1 + C::CONV_WARPS : 1);  // X3: the B loads' arrival and one per converter warp
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(sfull_bar(s), 1);
-      mbar_init(sempty_bar(s), 2);
+      mbar_init(sempty_bar(s), C::CONV_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -334,26 +340,46 @@ __global__ void __launch_bounds__(256, 1)
       // per-stage bit masks of issued loads and their phases, for the final drain
       uint32_t issued = 0, issued_phase = 0, sissued = 0, sissued_phase = 0;
       bool ok = true;
-      for (int u = unit0; ok && u < args.units; u += unit_step) {
-        const Unit w = decode_unit(args, u);
-        const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
-        const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (X3) {
-            // FP32 staging tile of A; the converter warps split it into the bf16 stage
-            if (!mbar_wait(sempty_bar(sstage), sphase ^ 1u)) {
-              atomicOr(args.fault, kFaultProducerWait);
-              ok = false;
-              break;
-            }
+      if (X3) {
+        // Two cursors walk the same (unit, k-block) sequence: the FP32 staging loads
+        // of A run ahead as far as the staging ring allows (DRAM latency), B's bf16
+        // hi/lo loads as far as the MMA ring allows; neither waits for the other.
+        struct Cursor {
+          int u, kb, kb1, tm, tn;
+        };
+        auto seek = [&](Cursor& c, int u) {
+          for (c.u = u; c.u < args.units; c.u += unit_step) {
+            const Unit w = decode_unit(args, c.u);
+            c.kb = w.kb0;
+            c.kb1 = w.kb1;
+            c.tm = w.tm;
+            c.tn = w.tn;
+            if (c.kb < c.kb1) break;
+          }
+        };
+        auto next = [&](Cursor& c) {
+          if (++c.kb == c.kb1) seek(c, c.u + unit_step);
+        };
+        Cursor xc, bc;
+        seek(xc, unit0);
+        seek(bc, unit0);
+        uint32_t idle = 0;
+        uint64_t t_idle = 0;
+        while (xc.u < args.units || bc.u < args.units) {
+          bool progressed = false;
+          if (xc.u < args.units && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
             const uint32_t xa = sbase + sstage * C::SA_BYTES;
             const uint32_t xf = sfull_bar(sstage);
+            const int a_row0 = xc.tm * C::TM;
             mbar_expect_tx(xf, C::SA_BYTES);
-            if (A_MN) {
+            if (A_MN && args.a3d) {
+              tma_load_3d(xa, &tmA, xf, 0, xc.kb * C::BK, a_row0 / 32);
+            } else if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < C::BM / 32; ++j) tma_load_2d(xa + 4096 * j, &tmA, xf, a_row0 + 32 * j, kb * C::BK);
+              for (int j = 0; j < C::BM / 32; ++j)
+                tma_load_2d(xa + 4096 * j, &tmA, xf, a_row0 + 32 * j, xc.kb * C::BK);
             } else {
-              tma_load_2d(xa, &tmA, xf, kb * C::BK, a_row0);
+              tma_load_2d(xa, &tmA, xf, xc.kb * C::BK, a_row0);
             }
             sissued |= 1u << sstage;
             sissued_phase = (sissued_phase & ~(1u << sstage)) | (sphase << sstage);
@@ -361,26 +387,28 @@ __global__ void __launch_bounds__(256, 1)
               sstage = 0;
               sphase ^= 1u;
             }
-            // B's bf16 hi and lo tiles straight into the MMA stage
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
-              atomicOr(args.fault, kFaultProducerWait);
-              ok = false;
-              break;
-            }
+            next(xc);
+            progressed = true;
+          }
+          if (bc.u < args.units && mbar_peek(empty_bar(stage), phase ^ 1u)) {
             const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
             const uint32_t fb = full_bar(stage);
+            const int b_row0 = bc.tn * BN;
             mbar_expect_tx(fb, C::B_BYTES);
-            if (B_MN) {
-              // 64-column groups of 32 contraction rows (4 KB, 128-byte swizzle)
+            if (B_MN && args.b3d) {
+              // 64-column groups of 32 contraction rows (4 KB each, 128-byte swizzle)
+              tma_load_3d(sb, &tmB, fb, 0, bc.kb * C::BK, b_row0 / 64);
+              tma_load_3d(sb + C::B_HALF, &tmB2, fb, 0, bc.kb * C::BK, b_row0 / 64);
+            } else if (B_MN) {
 #pragma unroll
               for (int j = 0; j < C::BNH / 64; ++j) {
-                tma_load_2d(sb + 4096 * j, &tmB, fb, b_row0 + 64 * j, kb * C::BK);
-                tma_load_2d(sb + C::B_HALF + 4096 * j, &tmB2, fb, b_row0 + 64 * j, kb * C::BK);
+                tma_load_2d(sb + 4096 * j, &tmB, fb, b_row0 + 64 * j, bc.kb * C::BK);
+                tma_load_2d(sb + C::B_HALF + 4096 * j, &tmB2, fb, b_row0 + 64 * j, bc.kb * C::BK);
               }
             } else {
               // rows of 32 contraction elements (64 bytes, 64-byte swizzle)
-              tma_load_2d(sb, &tmB, fb, kb * C::BK, b_row0);
-              tma_load_2d(sb + C::B_HALF, &tmB2, fb, kb * C::BK, b_row0);
+              tma_load_2d(sb, &tmB, fb, bc.kb * C::BK, b_row0);
+              tma_load_2d(sb + C::B_HALF, &tmB2, fb, bc.kb * C::BK, b_row0);
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -388,8 +416,29 @@ __global__ void __launch_bounds__(256, 1)
               stage = 0;
               phase ^= 1u;
             }
-            continue;
+            next(bc);
+            progressed = true;
           }
+          // bounded: give up once neither ring has moved for kWaitLimitNs
+          if (progressed) {
+            idle = 0;
+          } else if ((++idle & 255u) == 1u) {
+            const uint64_t now = globaltimer_ns();
+            if (idle == 1u) {
+              t_idle = now;
+            } else if (now - t_idle > kWaitLimitNs) {
+              atomicOr(args.fault, kFaultProducerWait);
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+      for (int u = unit0; !X3 && ok && u < args.units; u += unit_step) {
+        const Unit w = decode_unit(args, u);
+        const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
+        const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
@@ -406,13 +455,24 @@ __global__ void __launch_bounds__(256, 1)
             else
               tma_load_2d(dst, map, fb, x, y);
           };
-          if (A_MN) {
+          auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z) {
+            if (PAIR)
+              tma_load_3d_pair(dst, map, fb, 0, y, z);
+            else
+              tma_load_3d(dst, map, fb, 0, y, z);
+          };
+          // MN-major: 64-column groups of 64 contraction rows (8 KB each)
+          if (A_MN && args.a3d) {
+            load3(sa, &tmA, kb * C::BK, a_row0 / 64);
+          } else if (A_MN) {
             load(sa, &tmA, a_row0, kb * C::BK);
             load(sa + 8192, &tmA, a_row0 + 64, kb * C::BK);
           } else {
             load(sa, &tmA, kb * C::BK, a_row0);
           }
-          if (B_MN) {
+          if (B_MN && args.b3d) {
+            load3(sb, &tmB, kb * C::BK, b_row0 / 64);
+          } else if (B_MN) {
 #pragma unroll
             for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, &tmB, b_row0 + 64 * j, kb * C::BK);
           } else {
@@ -521,62 +581,46 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) atomicOr(args.fault, kFaultDrainWait);
     }
-  } else if (X3 && (warp == 2 || warp == 3)) {
+  } else if (X3 && (warp == 2 || warp == 3 || warp == 8 || warp == 9)) {
     // ------------------------------------------------------------ converter (X3)
     // Turns each FP32 staging tile of A into the bf16 hi/lo A tiles of an MMA stage:
-    // hi = RNE(x), lo = RNE(x - hi), written in the tensor core's swizzled layout.
-    const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..63
+    // hi = RNE(x), lo = RNE(x - hi) (x - hi is exact), written in the tensor core's
+    // swizzled layout.  A task is one 16-byte bf16 chunk (8 elements) of A, read
+    // from two 16-byte FP32 chunks:
+    //   K-major: FP32 rows of 128 B (128-byte swizzle) -> bf16 rows of 64 B
+    //            (64-byte swizzle); chunk c of row r <- FP32 chunks 2c, 2c+1 of row r;
+    //   MN-major: FP32 boxes of 32 elements x 32 contraction rows (4 KB, 128-byte
+    //            swizzle) -> bf16 groups of 64 elements x 32 rows (4 KB, 128-byte
+    //            swizzle).
+    // The 512 tasks of a stage are dealt round-robin to the 128 converter threads;
+    // their shared-memory offsets do not depend on the stage, so they are computed
+    // once, and each thread loads all of its chunks before converting any.
+    constexpr int NCT = (X3 ? C::CONV_WARPS : 4) * 32;  // (the branch only runs with X3)
+    constexpr int kTasks = 512 / NCT;
+    static_assert(512 % NCT == 0, "converter tasks");
+    const int ctid = (warp < 4 ? warp - 2 : warp - 6) * 32 + lane;
+    uint32_t src0[kTasks], src1[kTasks], dsto[kTasks];
+#pragma unroll
+    for (int b = 0; b < kTasks; ++b) {
+      const int t = ctid + NCT * b;
+      if (A_MN) {
+        const int k = t >> 4, q = t & 15;  // contraction row, chunk along the 128 rows
+        const int g = q >> 3, c = q & 7;
+        const uint32_t row = (2 * g + (c >> 2)) * 4096 + k * 128;
+        const int j0 = 2 * (c & 3);
+        src0[b] = row + ((j0 ^ (k & 7)) << 4);
+        src1[b] = row + (((j0 + 1) ^ (k & 7)) << 4);
+        dsto[b] = g * 4096 + k * 128 + ((c ^ (k & 7)) << 4);
+      } else {
+        const int r = t >> 2, c = t & 3;
+        src0[b] = r * 128 + (((2 * c) ^ (r & 7)) << 4);
+        src1[b] = r * 128 + (((2 * c + 1) ^ (r & 7)) << 4);
+        dsto[b] = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+      }
+    }
     int stage = 0, sstage = 0;
     uint32_t phase = 0, sphase = 0;
     bool ok = true;
-    // 16-byte chunk c of bf16 row r (8 elements) <- FP32 chunks 2c, 2c+1 of FP32 row r.
-    // K-major: FP32 rows of 128 B (128-byte swizzle), bf16 rows of 64 B (64-byte swizzle).
-    // MN-major: FP32 boxes of 32 elements x 32 contraction rows (4 KB each, 128-byte
-    // swizzle); bf16 groups of 64 elements x 32 rows (4 KB each, 128-byte swizzle).
-    // Each thread handles kBatch tasks at a time, all loads first, so the shared-
-    // memory latency of one task overlaps the others.
-    constexpr int kBatch = 4;
-    auto convert = [&](bool mn, uint32_t src, uint32_t hi, uint32_t lo, int extent) {
-      const int per_row = mn ? extent / 8 : 4;  // 16-byte bf16 chunks per row
-      const int total = mn ? 32 * per_row : extent * 4;
-      for (int t0 = tid; t0 < total; t0 += 64 * kBatch) {
-        float4 x0[kBatch], x1[kBatch];
-        uint32_t dst[kBatch];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int t = t0 + 64 * b;
-          if (t < total) {
-            uint32_t a0, a1;
-            if (mn) {
-              const int k = t / per_row, q = t - (t / per_row) * per_row;
-              const int g = q >> 3, c = q & 7;
-              const uint32_t row = src + (2 * g + (c >> 2)) * 4096 + k * 128;
-              const int j0 = 2 * (c & 3);
-              a0 = row + ((j0 ^ (k & 7)) << 4);
-              a1 = row + (((j0 + 1) ^ (k & 7)) << 4);
-              dst[b] = g * 4096 + k * 128 + ((c ^ (k & 7)) << 4);
-            } else {
-              const int r = t >> 2, c = t & 3;
-              const uint32_t row = src + r * 128;
-              a0 = row + (((2 * c) ^ (r & 7)) << 4);
-              a1 = row + (((2 * c + 1) ^ (r & 7)) << 4);
-              dst[b] = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-            }
-            x0[b] = ld_shared_f4(a0);
-            x1[b] = ld_shared_f4(a1);
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          if (t0 + 64 * b < total) {
-            uint4 h, l;
-            split8_bf16x3(x0[b], x1[b], h, l);
-            st_shared_u4(hi + dst[b], h);
-            st_shared_u4(lo + dst[b], l);
-          }
-        }
-      }
-    };
     for (int u = unit0; ok && u < args.units; u += unit_step) {
       const Unit w = decode_unit(args, u);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -587,8 +631,21 @@ __global__ void __launch_bounds__(256, 1)
           ok = false;
           break;
         }
-        const uint32_t sa = base + stage * C::STAGE_BYTES;
-        convert(A_MN, sbase + sstage * C::SA_BYTES, sa, sa + C::A_HALF, C::BM);
+        const uint32_t xs = sbase + sstage * C::SA_BYTES;
+        const uint32_t ah = base + stage * C::STAGE_BYTES, al = ah + C::A_HALF;
+        float4 x0[kTasks], x1[kTasks];
+#pragma unroll
+        for (int b = 0; b < kTasks; ++b) {
+          x0[b] = ld_shared_f4(xs + src0[b]);
+          x1[b] = ld_shared_f4(xs + src1[b]);
+        }
+#pragma unroll
+        for (int b = 0; b < kTasks; ++b) {
+          uint4 h, l;
+          split8_bf16x3(x0[b], x1[b], h, l);
+          st_shared_u4(ah + dsto[b], h);
+          st_shared_u4(al + dsto[b], l);
+        }
         fence_proxy_async_shared();  // the tensor core reads what this thread wrote
         __syncwarp();
         if (lane == 0) {
@@ -605,7 +662,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // TMEM sub-partition this warp may read
     const int row = q * 32 + lane;   // accumulator row == TMEM lane
@@ -728,7 +785,7 @@ template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
 cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(TileCfg<BN, PAIR, X3>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = TileCfg<BN, PAIR, X3>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -232,6 +232,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.gm = v.gm;
   plan.gn = v.gn;
   plan.gk = v.gk;
+  plan.model_ns = c.have ? c.t : 0.0;
   plan.pair = c.tiling.pair;
   plan.bm = static_cast<int>(c.tiling.rows());
   plan.bn = c.tiling.bn;

@@ -62,6 +62,7 @@ struct Plan {
   size_t off_split_b = 0, bytes_split_b = 0;
   int64_t ld_split_a = 0, ld_split_b = 0;  // their leading dimensions (elements)
   size_t ws_bytes = 0;
+  double model_ns = 0.0;  // the cost model's estimate for the chosen plan
 };
 
 // Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows

@@ -199,7 +199,8 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
 typedef struct dp_plan_info {
     int32_t block_m;          /* output tile rows (128, or 256 for a CTA pair) */
     int32_t block_n;          /* output tile columns (64, 128 or 256) */
-    int32_t block_k;          /* contraction block (64 elements = 64 tokens for wgrad) */
+    int32_t block_k;          /* contraction block (64 elements = 64 tokens for wgrad; 32 for
+                                 the router's forward and weight gradient) */
     int32_t stages;           /* shared-memory pipeline depth */
     int32_t splits;           /* contraction splits per output tile (1 = whole K per tile) */
     int32_t raster_group;     /* tiles per raster group (columns, or rows if raster_rows) */
@@ -213,13 +214,15 @@ typedef struct dp_plan_info {
     int32_t reserved;
     int64_t gemm_m;           /* output rows of the contraction */
     int64_t gemm_n;           /* output columns */
-    int64_t gemm_k;           /* contraction length (3x for the router's BF16x3 terms) */
+    int64_t gemm_k;           /* contraction length (3N for the router's input gradient,
+                                 which contracts concatenated [lo|hi|hi] x [hi;lo;hi] copies) */
     int64_t tiles_m;
     int64_t tiles_n;
     int64_t k_blocks;         /* ceil(gemm_k / block_k) */
     int64_t units;            /* full_units + (tiles_m * tiles_n - full_units) * splits */
     int64_t full_units;       /* leading whole-K units; the remaining tiles are split */
     uint64_t workspace_bytes; /* == dp_workspace_size() */
+    double model_us;          /* the planner's modelled duration of the call (diagnostic) */
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs

@@ -55,6 +55,8 @@ dp_status init_device(int dev, DeviceState** out) {
       cudaError_t e = set_attributes_kk();
       if (e == cudaSuccess) e = set_attributes_km();
       if (e == cudaSuccess) e = set_attributes_mm();
+      if (e == cudaSuccess) e = set_attributes_split();
+      if (e == cudaSuccess) e = set_attributes_reduce();
       if (e == cudaSuccess) e = cudaGetSymbolAddress(&fault, g_fault_word);
       if (cur != dev) cudaSetDevice(cur);
       if (e != cudaSuccess) return DP_ERR_LAUNCH;
@@ -322,6 +324,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   l.grid = p.grid;
   l.pair = p.pair;
   l.x3 = x3;
+  l.pdl = p.op >= kOpRouterFwd;  // right behind the kernel that split the router's operands
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);

@@ -294,6 +294,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(threadIdx.x) & 31;
+  if (threadIdx.x == 0) {  // descriptors on their way while the CTA sets up
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+    if (X3) tma_prefetch_map(&tmB2);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -332,9 +337,6 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB);
-      if (X3) tma_prefetch_map(&tmB2);
       int stage = 0, sstage = 0;
       uint32_t phase = 0, sphase = 0;
       // per-stage bit masks of issued loads and their phases, for the final drain
@@ -365,7 +367,12 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         seek(bc, unit0);
         uint32_t idle = 0;
         uint64_t t_idle = 0;
+        // The staging ring is filled first: A (FP32, the caller's) does not depend on
+        // the split kernel, so its loads overlap that kernel's tail.
+        bool b_ready = false;
+        int issued_x = 0;
         while (xc.u < args.units || bc.u < args.units) {
+          if (xc.u >= args.units) issued_x = SSTAGES;  // (fewer blocks than staging slots)
           bool progressed = false;
           if (xc.u < args.units && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
             const uint32_t xa = sbase + sstage * C::SA_BYTES;
@@ -388,9 +395,14 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
               sphase ^= 1u;
             }
             next(xc);
+            ++issued_x;
             progressed = true;
           }
-          if (bc.u < args.units && mbar_peek(empty_bar(stage), phase ^ 1u)) {
+          if (bc.u < args.units && !b_ready && issued_x >= SSTAGES) {
+            pdl_wait();  // B's planes come from the split kernel launched before this grid
+            b_ready = true;
+          }
+          if (b_ready && bc.u < args.units && mbar_peek(empty_bar(stage), phase ^ 1u)) {
             const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
             const uint32_t fb = full_bar(stage);
             const int b_row0 = bc.tn * BN;
@@ -434,6 +446,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           }
         }
       }
+      if (!X3) pdl_wait();  // (the router's input gradient reads the split kernel's operands)
       for (int u = unit0; !X3 && ok && u < args.units; u += unit_step) {
         const Unit w = decode_unit(args, u);
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
@@ -759,6 +772,7 @@ struct GemmLaunch {
   int grid;   // CTAs (twice the number of pairs for a paired plan)
   bool pair;  // clusters of two CTAs share each tile
   bool x3;    // router BF16x3 mode: FP32 A split in the kernel, B from pre-split planes
+  bool pdl;   // launched as a programmatic dependent of the operand-split kernel
 };
 
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
@@ -776,6 +790,9 @@ cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaS
 // Ordered sum of the split partials a GEMM launch wrote (split_reduce.cu): for each
 // split tile, partials s = 0..splits-1 added in that order in FP32, rounded once.
 cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t split_tiles, cudaStream_t stream);
+// Shared-memory carveout of the split and reduction kernels (set once per device).
+cudaError_t set_attributes_split();
+cudaError_t set_attributes_reduce();
 // Dynamic shared memory limits of each instantiation, on the current device.
 cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();
@@ -788,20 +805,33 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cfg.blockDim = dim3(TileCfg<BN, PAIR, X3>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = TileCfg<BN, PAIR, X3>::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (PAIR) {  // single-CTA tiles launch without a cluster
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (l.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;  // single-CTA tiles launch without a cluster
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.tmB2, l.args);
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
 cudaError_t set_attr_t() {
-  return cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, PAIR, X3>::SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, PAIR, X3>::SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 }  // namespace dp

@@ -7,10 +7,11 @@
 // output type.  The order depends on nothing but the plan, so the result is
 // bitwise repeatable (FlashInfer page "... restore the K1 weight-gradient routes
 // ...": deterministic weight gradients over a fixed split of the 64-token blocks).
-// Every slice of every tile is summed by its own CTA, so the sum costs about one
-// round trip to L2 instead of S of them in a single CTA.  It is launched as a
-// programmatic dependent of the GEMM: its launch overlaps the GEMM's tail and
-// griddepcontrol.wait holds it until the partials are complete and visible.
+// Every float4 of every split tile has its own thread, which issues the loads of
+// all its splits at once, so the sum costs about one round trip to L2.  It is
+// launched as a programmatic dependent of the GEMM: its launch overlaps the GEMM's
+// tail and griddepcontrol.wait holds it until the partials are complete and
+// visible.
 #include "gemm_kernel.cuh"
 
 namespace dp {
@@ -25,78 +26,70 @@ struct ReduceArgs {
   int32_t chunks;          // 32-column chunks per tile
 };
 
-// One CTA of four warps per (slot, 32-column chunk); warp w sums rows
-// [32w, 32w + 32) of the slot.  Partial layout: [slot][split][bn/4][128] float4.
-// Lane layout: for the row-major output value i of a lane is row 4i + lane/8,
-// float4 chunk lane%8, so each store instruction writes four whole 128-byte row
-// segments; for the transposed store (swapped weight gradient) it is row `lane`,
-// chunk i, so consecutive lanes write consecutive elements of each output row.
-__global__ void __launch_bounds__(128) split_reduce_kernel(const __grid_constant__ ReduceArgs ra) {
+// One thread per float4 of the split tiles: thread t of the (slot, 32-column chunk)
+// handles row t % 128 and float4 column t / 128 of the chunk, so a warp's loads are
+// 512 contiguous bytes of each partial, and loads all splits (up to 16 at a time)
+// before adding them in order.  Partial layout: [slot][split][bn/4][128] float4.
+// A thread stores its 4 values to the row-major output as one 16-byte store (or 8
+// bytes of bf16), or to the transposed output (swapped weight gradient) as 4
+// elements, each next to its neighbouring rows' (consecutive lanes, consecutive m).
+constexpr int kReduceThreads = 128;
+constexpr int kReduceBatch = 16;
+
+__global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __grid_constant__ ReduceArgs ra) {
   pdl_wait();  // the GEMM's partials are complete and visible
   const GemmArgs& a = ra.g;
-  const int chunk = static_cast<int>(blockIdx.x) % ra.chunks;
-  const int slot = static_cast<int>(blockIdx.x) / ra.chunks;
+  const int per_slice = kBlockM * 8 / kReduceThreads;  // CTAs per (slot, chunk): 1024 float4
+  const int cta = static_cast<int>(blockIdx.x);
+  const int slice = cta / per_slice;
+  const int t = (cta - slice * per_slice) * kReduceThreads + static_cast<int>(threadIdx.x);  // 0..1023
+  const int chunk = slice % ra.chunks;
+  const int slot = slice / ra.chunks;
   const int ptile = slot / ra.slots_per_tile, rank = slot - ptile * ra.slots_per_tile;
   int tm, tn;
   tile_coords(a, a.full_units + ptile, &tm, &tn);
-  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  const int64_t m0 = static_cast<int64_t>(tm) * ra.tile_rows + rank * kBlockM + warp * 32;
-  const int64_t col = static_cast<int64_t>(tn) * ra.bn + chunk * 32;
-  if (m0 >= a.gm || col >= a.gn) return;
-  const bool tr = a.out_trans != 0;
-  const int r0 = tr ? lane : (lane >> 3), dr = tr ? 0 : 4;
-  const int c0 = tr ? 0 : (lane & 7), dc = tr ? 1 : 0;
-  const int istep = dc * kBlockM + dr;  // float4 distance between a lane's values i and i + 1
-  const int64_t rows_left = a.gm - m0;
+  const int row = t & (kBlockM - 1), j = t >> 7;  // row of the slot, float4 column in the chunk
+  const int64_t m = static_cast<int64_t>(tm) * ra.tile_rows + rank * kBlockM + row;
+  const int64_t col = static_cast<int64_t>(tn) * ra.bn + chunk * 32 + 4 * j;
+  if (m >= a.gm || col >= a.gn) return;
   const size_t pstride = static_cast<size_t>(kBlockM) * ra.bn / 4;  // float4 per partial tile
-  // (rows past the output's end hold no partials; their sums are never stored)
   const float4* src = a.partials + static_cast<size_t>(slot) * a.splits * pstride +
-                      static_cast<size_t>(chunk) * 8 * kBlockM + warp * 32 + c0 * kBlockM + r0;
-  float4 acc[8];
-  // splits in ascending order, four in flight at a time
-  for (int sp = 0; sp < a.splits; sp += 4) {
-    float4 x[4][8];
+                      static_cast<size_t>(chunk * 8 + j) * kBlockM + row;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // splits in ascending order: acc = p_0, then acc += p_s
+  for (int s0 = 0; s0 < a.splits; s0 += kReduceBatch) {
+    float4 x[kReduceBatch];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (sp + k < a.splits)
+    for (int k = 0; k < kReduceBatch; ++k)
+      if (s0 + k < a.splits) x[k] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[k][i] = __ldcg(src + (sp + k) * pstride + i * istep);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (sp + k < a.splits)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (sp + k == 0) {
-            acc[i] = x[k][i];
-          } else {
-            acc[i].x += x[k][i].x;
-            acc[i].y += x[k][i].y;
-            acc[i].z += x[k][i].z;
-            acc[i].w += x[k][i].w;
-          }
+    for (int k = 0; k < kReduceBatch; ++k)
+      if (s0 + k < a.splits) {
+        if (s0 + k == 0) {
+          acc = x[k];
+        } else {
+          acc.x += x[k].x;
+          acc.y += x[k].y;
+          acc.z += x[k].z;
+          acc.w += x[k].w;
         }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = r0 + i * dr;
-    const int64_t cc = col + 4 * (c0 + i * dc);
-    if (r >= rows_left || cc >= a.gn) continue;
-    if (tr) {
-      const float e[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int64_t o = (cc + t) * a.ldo + m0 + r;
-        if (a.out_f32)
-          static_cast<float*>(a.out)[o] = e[t];
-        else
-          static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(e[t], 0.0f) & 0xFFFFu);
       }
-    } else if (a.out_f32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (m0 + r) * a.ldo + cc) = acc[i];
-    } else {
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + (m0 + r) * a.ldo + cc) =
-          make_uint2(pack_bf16x2(acc[i].x, acc[i].y), pack_bf16x2(acc[i].z, acc[i].w));
+  }
+  if (a.out_trans) {
+    const float e[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t o = (col + q) * a.ldo + m;
+      if (a.out_f32)
+        static_cast<float*>(a.out)[o] = e[q];
+      else
+        static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(e[q], 0.0f) & 0xFFFFu);
     }
+  } else if (a.out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + m * a.ldo + col) = acc;
+  } else {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + m * a.ldo + col) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
 }
 
@@ -109,12 +102,12 @@ cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t 
   ra.tile_rows = pair ? 2 * kBlockM : kBlockM;
   ra.slots_per_tile = pair ? 2 : 1;
   ra.chunks = bn / 32;
-  const int64_t blocks = split_tiles * ra.slots_per_tile * ra.chunks;
+  const int64_t blocks = split_tiles * ra.slots_per_tile * ra.chunks * (kBlockM * 8 / kReduceThreads);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(kReduceThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -123,6 +116,13 @@ cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, split_reduce_kernel, ra);
+}
+
+cudaError_t set_attributes_reduce() {
+  // the same shared-memory carveout as the GEMM kernels, so switching between them
+  // does not reconfigure the SMs
+  return cudaFuncSetAttribute(split_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
 }  // namespace dp

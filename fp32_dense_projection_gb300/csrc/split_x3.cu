@@ -12,8 +12,8 @@
 //   concatenated three segments per row or per matrix, so that one plain BF16
 //                contraction over 3x the length sums lo*hi + hi*lo + hi*hi
 //                (input gradient: dY as [lo | hi | hi] columns, W as [hi; lo; hi] rows).
-// Each thread converts four consecutive FP32 values (one 16-byte load) and writes
-// four bf16 per segment (8-byte stores); the pass is HBM-bound.
+// A quad of four consecutive FP32 values (one 16-byte load) becomes four bf16 per
+// segment (8-byte stores); the pass is HBM-bound.
 #include <algorithm>
 
 #include "gemm_kernel.cuh"
@@ -28,24 +28,58 @@ struct SplitJobs {
   int njobs;
 };
 
-__global__ void __launch_bounds__(256) split_x3_kernel(const __grid_constant__ SplitJobs jobs) {
-  const int64_t total = jobs.quads[0] + (jobs.njobs > 1 ? jobs.quads[1] : 0);
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
-    const int j = i < jobs.quads[0] ? 0 : 1;
-    const SplitJob& s = jobs.job[j];
-    const int64_t q = j == 0 ? i : i - jobs.quads[0];
-    const int64_t per_row = s.cols / 4;
-    const int64_t r = q / per_row;
-    const int64_t c = (q - r * per_row) * 4;
-    const float4 x = __ldg(reinterpret_cast<const float4*>(s.x + r * s.ldx + c));
-    const uint32_t h01 = pack_bf16x2(x.x, x.y), h23 = pack_bf16x2(x.z, x.w);
-    const uint32_t l01 = pack_bf16x2(x.x - __uint_as_float(h01 << 16), x.y - __uint_as_float(h01 & 0xFFFF0000u));
-    const uint32_t l23 = pack_bf16x2(x.z - __uint_as_float(h23 << 16), x.w - __uint_as_float(h23 & 0xFFFF0000u));
-    const uint2 hi = make_uint2(h01, h23), lo = make_uint2(l01, l23);
-    uint16_t* o = s.out + r * s.ldo + c;
-    for (int seg = 0; seg < s.nseg; ++seg)
-      *reinterpret_cast<uint2*>(o + seg * s.seg_stride) = ((s.lo_mask >> seg) & 1u) ? lo : hi;
+// Each thread converts four quads spaced one grid apart, all four loads issued
+// before any store; row and column of a quad come from a 32-bit division when the
+// job is small enough (always, for the router's sizes).
+constexpr int kSplitThreads = 256;
+constexpr int kSplitQuads = 4;
+
+__device__ __forceinline__ void locate(const SplitJobs& jobs, uint64_t i, const SplitJob** s, int64_t* r,
+                                       int64_t* c) {
+  const int j = i < static_cast<uint64_t>(jobs.quads[0]) ? 0 : 1;
+  *s = &jobs.job[j];
+  const uint64_t q = j == 0 ? i : i - static_cast<uint64_t>(jobs.quads[0]);
+  const uint64_t per_row = static_cast<uint64_t>((*s)->cols / 4);
+  uint64_t row;
+  if (q < (1ull << 32) && per_row < (1ull << 32))
+    row = static_cast<uint32_t>(q) / static_cast<uint32_t>(per_row);
+  else
+    row = q / per_row;
+  *r = static_cast<int64_t>(row);
+  *c = static_cast<int64_t>(q - row * per_row) * 4;
+}
+
+__global__ void __launch_bounds__(kSplitThreads) split_x3_kernel(const __grid_constant__ SplitJobs jobs) {
+  pdl_launch_dependents();  // the GEMM may start staging its other operand meanwhile
+  const uint64_t total =
+      static_cast<uint64_t>(jobs.quads[0]) + (jobs.njobs > 1 ? static_cast<uint64_t>(jobs.quads[1]) : 0);
+  const uint64_t step = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i0 = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+       i0 += kSplitQuads * step) {
+    float4 x[kSplitQuads];
+    const SplitJob* sj[kSplitQuads];
+    int64_t r[kSplitQuads], c[kSplitQuads];
+#pragma unroll
+    for (int k = 0; k < kSplitQuads; ++k) {
+      const uint64_t i = i0 + k * step;
+      if (i < total) {
+        locate(jobs, i, &sj[k], &r[k], &c[k]);
+        x[k] = __ldg(reinterpret_cast<const float4*>(sj[k]->x + r[k] * sj[k]->ldx + c[k]));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kSplitQuads; ++k) {
+      if (i0 + k * step >= total) continue;
+      const uint32_t h01 = pack_bf16x2(x[k].x, x[k].y), h23 = pack_bf16x2(x[k].z, x[k].w);
+      const uint32_t l01 =
+          pack_bf16x2(x[k].x - __uint_as_float(h01 << 16), x[k].y - __uint_as_float(h01 & 0xFFFF0000u));
+      const uint32_t l23 =
+          pack_bf16x2(x[k].z - __uint_as_float(h23 << 16), x[k].w - __uint_as_float(h23 & 0xFFFF0000u));
+      const uint2 hi = make_uint2(h01, h23), lo = make_uint2(l01, l23);
+      uint16_t* o = sj[k]->out + r[k] * sj[k]->ldo + c[k];
+      for (int seg = 0; seg < sj[k]->nseg; ++seg)
+        *reinterpret_cast<uint2*>(o + seg * sj[k]->seg_stride) = ((sj[k]->lo_mask >> seg) & 1u) ? lo : hi;
+    }
   }
 }
 
@@ -68,9 +102,17 @@ cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaS
   }
   p.njobs = njobs;
   if (total == 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sm_count) * 8);
-  split_x3_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  const int64_t per_block = kSplitThreads * kSplitQuads;
+  const int64_t blocks = std::min<int64_t>((total + per_block - 1) / per_block, static_cast<int64_t>(sm_count) * 8);
+  split_x3_kernel<<<static_cast<unsigned>(blocks), kSplitThreads, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t set_attributes_split() {
+  // the same shared-memory carveout as the GEMM kernels, so switching between them
+  // does not reconfigure the SMs
+  return cudaFuncSetAttribute(split_x3_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
 }  // namespace dp

@@ -65,16 +65,17 @@ struct GemmArgs {
 // hi and lo halves of a 32-wide contraction block of each operand
 // ([A_hi | A_lo | B_hi | B_lo]).  A's halves are written by converter warps from an
 // FP32 staging tile that TMA loads into a separate, one-stage-deeper ring; B's
-// halves are loaded by TMA from two bf16 planes split before the launch.
+// halves are loaded by TMA from two bf16 planes split before the launch.  With
+// PAIR, each CTA of the pair splits its own 128 rows of A and loads half of B, and
+// both CTAs' converters arrive on the leader's full barrier.
 template <int BN, bool PAIR = false, bool X3 = false>
 struct TileCfg {
-  static_assert(!(PAIR && X3), "the BF16x3 mode uses single-CTA tiles");
   static constexpr int BM = kBlockM;             // accumulator rows per CTA
   static constexpr int TM = PAIR ? 2 * BM : BM;  // output tile rows (a CTA pair splits them)
   static constexpr int BNH = PAIR ? BN / 2 : BN; // B rows each CTA loads
   static constexpr int BK = X3 ? kRouterBlockK : kBlockK;
-  static constexpr int STAGES = X3 ? stages_x3(BN) : stages_for(BN, PAIR);
-  static constexpr int SSTAGES = X3 ? staging_stages_x3(BN) : 0;  // FP32 staging ring (X3)
+  static constexpr int STAGES = X3 ? stages_x3(BN, PAIR) : stages_for(BN, PAIR);
+  static constexpr int SSTAGES = X3 ? staging_stages_x3(BN, PAIR) : 0;  // FP32 staging ring (X3)
   static constexpr int A_HALF = BM * BK * 2;     // one bf16 copy of the A tile
   static constexpr int B_HALF = BNH * BK * 2;
   static constexpr int A_BYTES = X3 ? 2 * A_HALF : A_HALF;
@@ -93,7 +94,7 @@ struct TileCfg {
   static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(STAGE_BYTES % 1024 == 0 && SA_BYTES % 1024 == 0, "swizzle alignment");
-  static_assert(!X3 || (STAGE_BYTES == x3_stage_bytes(BN) && SA_BYTES == kX3StagingBytes), "planner sizes");
+  static_assert(!X3 || (STAGE_BYTES == x3_stage_bytes(BN, PAIR) && SA_BYTES == kX3StagingBytes), "planner sizes");
 };
 
 // Work unit u -> output tile, contraction range and, for split units, the split
@@ -302,7 +303,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), X3 ? 1 + C::CONV_WARPS : 1);  // X3: the B loads' arrival and one per converter warp
+      // X3: the B loads' arrival and one per converter warp (of both CTAs of a pair)
+      mbar_init(full_bar(s), X3 ? 1 + (PAIR ? 2 : 1) * C::CONV_WARPS : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < SSTAGES; ++s) {
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           if (xc.u < args.units && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
             const uint32_t xa = sbase + sstage * C::SA_BYTES;
             const uint32_t xf = sfull_bar(sstage);
-            const int a_row0 = xc.tm * C::TM;
+            const int a_row0 = xc.tm * C::TM + static_cast<int>(rank) * C::BM;
             mbar_expect_tx(xf, C::SA_BYTES);
             if (A_MN && args.a3d) {
               tma_load_3d(xa, &tmA, xf, 0, xc.kb * C::BK, a_row0 / 32);
@@ -402,25 +404,39 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             pdl_wait();  // B's planes come from the split kernel launched before this grid
             b_ready = true;
           }
-          if (b_ready && bc.u < args.units && mbar_peek(empty_bar(stage), phase ^ 1u)) {
+          if (b_ready && bc.u < args.units &&
+              (PAIR ? mbar_peek_cluster(empty_bar(stage), phase ^ 1u) : mbar_peek(empty_bar(stage), phase ^ 1u))) {
             const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
-            const uint32_t fb = full_bar(stage);
-            const int b_row0 = bc.tn * BN;
-            mbar_expect_tx(fb, C::B_BYTES);
+            // a pair's B loads all complete on the leader's full barrier
+            const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
+            const int b_row0 = bc.tn * BN + static_cast<int>(rank) * C::BNH;
+            if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::B_BYTES);
+            auto load2 = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+              if (PAIR)
+                tma_load_2d_pair(dst, map, fb, x, y);
+              else
+                tma_load_2d(dst, map, fb, x, y);
+            };
+            auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z) {
+              if (PAIR)
+                tma_load_3d_pair(dst, map, fb, 0, y, z);
+              else
+                tma_load_3d(dst, map, fb, 0, y, z);
+            };
             if (B_MN && args.b3d) {
               // 64-column groups of 32 contraction rows (4 KB each, 128-byte swizzle)
-              tma_load_3d(sb, &tmB, fb, 0, bc.kb * C::BK, b_row0 / 64);
-              tma_load_3d(sb + C::B_HALF, &tmB2, fb, 0, bc.kb * C::BK, b_row0 / 64);
+              load3(sb, &tmB, bc.kb * C::BK, b_row0 / 64);
+              load3(sb + C::B_HALF, &tmB2, bc.kb * C::BK, b_row0 / 64);
             } else if (B_MN) {
 #pragma unroll
               for (int j = 0; j < C::BNH / 64; ++j) {
-                tma_load_2d(sb + 4096 * j, &tmB, fb, b_row0 + 64 * j, bc.kb * C::BK);
-                tma_load_2d(sb + C::B_HALF + 4096 * j, &tmB2, fb, b_row0 + 64 * j, bc.kb * C::BK);
+                load2(sb + 4096 * j, &tmB, b_row0 + 64 * j, bc.kb * C::BK);
+                load2(sb + C::B_HALF + 4096 * j, &tmB2, b_row0 + 64 * j, bc.kb * C::BK);
               }
             } else {
               // rows of 32 contraction elements (64 bytes, 64-byte swizzle)
-              tma_load_2d(sb, &tmB, fb, bc.kb * C::BK, b_row0);
-              tma_load_2d(sb + C::B_HALF, &tmB2, fb, bc.kb * C::BK, b_row0);
+              load2(sb, &tmB, bc.kb * C::BK, b_row0);
+              load2(sb + C::B_HALF, &tmB2, bc.kb * C::BK, b_row0);
             }
             issued |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -556,9 +572,15 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
               const uint64_t a_hi = d_a(sa), a_lo = d_a(sa + C::A_HALF);
               const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
               // x*w ~ lo_x*hi_w + hi_x*lo_w + hi_x*hi_w (lo*lo dropped), small terms first
-              mma_bf16(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
-              mma_bf16(d_tmem, a_hi, b_lo, IDESC, 1u);
-              mma_bf16(d_tmem, a_hi, b_hi, IDESC, 1u);
+              if (PAIR) {
+                mma_bf16_pair(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                mma_bf16_pair(d_tmem, a_hi, b_lo, IDESC, 1u);
+                mma_bf16_pair(d_tmem, a_hi, b_hi, IDESC, 1u);
+              } else {
+                mma_bf16(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                mma_bf16(d_tmem, a_hi, b_lo, IDESC, 1u);
+                mma_bf16(d_tmem, a_hi, b_hi, IDESC, 1u);
+              }
               continue;
             }
             // K-major: step 16 elements (32 bytes) along the swizzled row;
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       const Unit w = decode_unit(args, u);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         // every lane waits itself; the warp leaves together if any wait gives up
-        const bool mine = mbar_wait(sfull_bar(sstage), sphase) && mbar_wait(empty_bar(stage), phase ^ 1u);
+        const bool mine = mbar_wait(sfull_bar(sstage), sphase) && mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u);
         if (!__all_sync(0xffffffffu, mine)) {
           if (lane == 0) atomicOr(args.fault, kFaultProducerWait);
           ok = false;
@@ -663,7 +685,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(sempty_bar(sstage));  // staging tile may be reloaded
-          mbar_arrive(full_bar(stage));     // A half of the bf16 stage ready for the MMAs
+          // A half of the bf16 stage ready for the MMAs (the leader's, for a pair)
+          if (PAIR)
+            mbar_arrive_cluster(map_shared_rank(full_bar(stage), 0));
+          else
+            mbar_arrive(full_bar(stage));
         }
         if (++sstage == SSTAGES) {
           sstage = 0;

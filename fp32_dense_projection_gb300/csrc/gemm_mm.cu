@@ -2,12 +2,22 @@
 // One translation unit per operand-major combination so the builds run in parallel.
 // BF16 operands: single-CTA tiles 128 x {64, 128, 256}, CTA-pair tiles 256 x {128, 256}.
 // Router BF16x3 (swapped weight gradient: FP32 X split in the kernel, dY from pre-split
-// planes): single-CTA tiles 128 x {64, 128, 256}.
+// planes): single-CTA tiles 128 x {64, 128, 256}, CTA-pair tiles 256 x {128, 256}.
 #include "gemm_kernel.cuh"
 
 namespace dp {
 
 cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream) {
+  if (l.x3 && l.pair) {
+    switch (bn) {
+      case 128:
+        return launch_gemm_t<128, true, true, true, true>(l, stream);
+      case 256:
+        return launch_gemm_t<256, true, true, true, true>(l, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   if (l.x3) {
     switch (bn) {
       case 64:
@@ -51,6 +61,8 @@ cudaError_t set_attributes_mm() {
   if (e == cudaSuccess) e = set_attr_t<64, true, true, false, true>();
   if (e == cudaSuccess) e = set_attr_t<128, true, true, false, true>();
   if (e == cudaSuccess) e = set_attr_t<256, true, true, false, true>();
+  if (e == cudaSuccess) e = set_attr_t<128, true, true, true, true>();
+  if (e == cudaSuccess) e = set_attr_t<256, true, true, true, true>();
   return e;
 }
 

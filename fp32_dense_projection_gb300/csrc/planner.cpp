@@ -24,11 +24,12 @@ namespace {
 constexpr double kFlopPerNsPerSm = 12500.0;   // dense BF16 tensor rate per SM
 constexpr double kL2BytesPerNsPerSm = 160.0;  // operand bytes an SM pulls when they hit in L2
 constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
-constexpr double kSmDramBytesPerNs = 64.0;    // most DRAM bandwidth one SM's TMA stream sustains
+constexpr double kSmDramBytesPerNs = 45.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceNs = 2000.0;          // the split reduction kernel's launch and one L2 round trip
 constexpr double kReduceBytesPerNs = 4000.0;  // partial bytes it sums per ns (whole GPU, L2-resident)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
+constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -93,7 +94,7 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   const double flop_per_kb = 2.0 * kBlockM * t.bn * v.bk * v.terms;  // per SM, tensor-pipe work
   const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0);
   // BF16x3: the converter warps split every A element of the block
-  const double t_split = v.terms > 1 ? kb * kBlockM * v.bk / kX3SplitPerNs : 0.0;
+  const double t_split = v.terms > 1 ? kb * std::max(kBlockM * v.bk / kX3SplitPerNs, kX3BlockNs) : 0.0;
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
   const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
@@ -156,7 +157,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
     if (o.pair >= 0 && pair != o.pair) continue;
     if (pair && !kAutoPair && o.pair != 1) continue;
     if (pair && (sm < 2 || v.gm <= kBlockM)) continue;  // a pair needs two row blocks of work
-    if (pair && v.terms > 1) continue;                  // the BF16x3 mode is single-CTA
+    if (pair && v.terms > 1 && o.pair != 1) continue;  // BF16x3 pairs only when forced (measured slower)
     const int64_t slots = pair ? sm / 2 : sm;
     for (int bn : {256, 128, 64}) {
       if (pair && bn < 128) continue;  // each CTA of a pair holds bn / 2 >= 64 columns of B
@@ -237,7 +238,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.bm = static_cast<int>(c.tiling.rows());
   plan.bn = c.tiling.bn;
   plan.splits = static_cast<int>(c.splits);
-  plan.stages = v.terms > 1 ? stages_x3(plan.bn) : stages_for(plan.bn, plan.pair);
+  plan.stages = v.terms > 1 ? stages_x3(plan.bn, plan.pair) : stages_for(plan.bn, plan.pair);
   plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
   const int64_t tiles = plan.tiles_m * plan.tiles_n;

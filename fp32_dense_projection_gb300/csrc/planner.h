@@ -83,13 +83,14 @@ constexpr int stages_for(int bn, bool pair = false) { return stages_for_rows(pai
 // The staging ring is one stage deeper than the MMA ring; both fit in 208 KB.
 constexpr int kRouterBlockK = 32;
 constexpr int kX3StagingBytes = kBlockM * kRouterBlockK * 4;
-constexpr int x3_stage_bytes(int bn) { return (kBlockM + bn) * kRouterBlockK * 4; }
-constexpr int stages_x3(int bn) {
-  return (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn) + kX3StagingBytes) < 6
-             ? (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn) + kX3StagingBytes)
+// (a CTA of a pair holds half of B's rows)
+constexpr int x3_stage_bytes(int bn, bool pair = false) { return (kBlockM + (pair ? bn / 2 : bn)) * kRouterBlockK * 4; }
+constexpr int stages_x3(int bn, bool pair = false) {
+  return (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes) < 6
+             ? (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes)
              : 6;
 }
-constexpr int staging_stages_x3(int bn) { return stages_x3(bn) + 1; }
+constexpr int staging_stages_x3(int bn, bool pair = false) { return stages_x3(bn, pair) + 1; }
 
 // Overrides of the planner's choices, for tests and tuning (all unset in normal
 // use): > 0 forces the tile width / uniform split count / last-wave split count;

@@ -232,6 +232,40 @@ def test_pair_integer_exact(monkeypatch, op, T, N, K, bn):
     no_device_fault()
 
 
+@pytest.mark.parametrize("op,T,N,K", [("router_fwd", 257, 256, 192), ("router_fwd", 600, 136, 520),
+                                      ("router_wgrad", 300, 256, 264), ("router_wgrad", 77, 136, 520)])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_router_pair_integer_exact(monkeypatch, op, T, N, K, bn):
+    # BF16x3 over CTA pairs: each CTA splits its own 128 rows of A, B comes in halves
+    monkeypatch.setenv("DP_FORCE_PAIR", "1")
+    monkeypatch.setenv("DP_FORCE_BN", str(bn))
+    p = dp.plan(op, T, N, K)
+    if not p["cta_pair"]:
+        pytest.skip(f"no pair plan for this shape: {p}")
+    c = inputs.integer_case(T, N, K, seed=T + N + K + bn, dtype=torch.float32)
+    a, b = operands(op, c)
+    ref = full_ref(op, a, b)
+    got = as_f64(gpu(op, *operands(op, to_dev(c))))
+    assert np.array_equal(got, ref), (op, T, N, K, bn, p)
+    no_device_fault()
+
+
+@pytest.mark.parametrize("op", ["router_fwd", "router_wgrad"])
+@pytest.mark.parametrize("T,splits", [(1024, 0), (1024, 4), (4031, 0)])
+def test_router_pair_budget(monkeypatch, op, T, splits):
+    monkeypatch.setenv("DP_FORCE_PAIR", "1")
+    monkeypatch.setenv("DP_FORCE_BN", "256")
+    if splits:
+        monkeypatch.setenv("DP_FORCE_SPLITS", str(splits))
+    p = dp.plan(op, T, 256, 4096)
+    assert p["cta_pair"], p
+    c = inputs.router(T, 4096, seed=T + splits, experts=256)
+    ref = full_ref(op, *operands(op, c))
+    got = as_f64(gpu(op, *operands(op, to_dev(c))))
+    assert_budget(got, ref, "f32", f"pair {op} T={T} {p['splits']} splits")
+    no_device_fault()
+
+
 @pytest.mark.parametrize("op,T,N,K,tail", [("fwd", 2048, 2560, 2048, 2), ("dgrad", 2048, 2048, 2560, 3),
                                            ("wgrad", 4096, 2048, 2560, 0), ("wgrad", 16173, 512, 1024, 0)])
 def test_pair_split_plans(monkeypatch, op, T, N, K, tail):

@@ -17,6 +17,7 @@ own replica of the workload ("scaling": "weak"); no data crosses ranks.
 host cores on a bounded sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --suite cfg1,cfg2,cfg3,cfg4,cfg5     # per-op table of every configuration
 """
 from __future__ import annotations
 
@@ -203,7 +204,7 @@ def run_gpu(args, world, rank, local):
     flush = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     plans = {op: dp.plan(op, T_TOK, N_OUT, K_IN) for op in ("fwd", "dgrad", "wgrad")}
-    launches_per_step = 3  # one persistent GEMM launch per op (no split reduction at this size)
+    launches_per_step = sum(kernel_launches(op, plans[op]) for op in plans)
 
     def step(ev=None):
         if ev is not None:
@@ -315,6 +316,13 @@ def run_gpu(args, world, rank, local):
     return result if rank == 0 else None
 
 
+def kernel_launches(op: str, p: dict) -> int:
+    """Kernels one call enqueues: the GEMM, the split reduction when the plan splits
+    any tile, and the operand split of a router call."""
+    split = p["splits"] > 1 and p["tiles_m"] * p["tiles_n"] > p["full_units"]
+    return 1 + int(split) + int(str(op).startswith("router"))
+
+
 def load_traffic(op: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -409,6 +417,170 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------------------ measurement suite
+
+def run_suite(args, local):
+    """Every configuration of the workload set, per op, eager and CUDA-graph launch,
+    cold L2 before every call: microseconds, TFLOP/s, algorithmic GB/s and the
+    fraction of the bounding roofline (tensor for arithmetic intensity above the
+    ridge, HBM below).  One JSON line per case."""
+    import fp32_dense_projection_gb300 as dp
+    from fp32_dense_projection_gb300 import build as dpbuild
+
+    dpbuild.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dp.init(local)
+    peaks, peak_src = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    flush = torch.empty(2 * torch.cuda.get_device_properties(device).L2_cache_size, dtype=torch.uint8, device=device)
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(11)
+    reps = args.suite_reps
+
+    def eager(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    def graph(fn):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gr.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        del gr
+        return statistics.median(ts)
+
+    def report(cfg, case, flop, tc_flop, nbytes, fn, plans=None):
+        # flop: 2TNK of the op(s); tc_flop: tensor-pipe work (3x for BF16x3); nbytes: algorithmic bytes
+        ai = tc_flop / nbytes
+        bound = "tensor" if ai > ridge else "hbm"
+        for mode, timer in (("eager", eager), ("graph", graph)):
+            us = timer(fn)
+            tflops = flop / us / 1e6
+            gbs = nbytes / us / 1e3
+            frac = (tc_flop / us / 1e6) / tc_peak if bound == "tensor" else gbs / hbm_peak
+            line = {"suite": cfg, "case": case, "mode": mode, "us": round(us, 2), "tflops": round(tflops, 1),
+                    "gbs": round(gbs, 1), "bound": bound, "frac": round(frac, 3),
+                    "of": f"{peak_src} {'bf16 burst' if bound == 'tensor' else 'HBM copy'} peak"}
+            if plans:
+                line["plan"] = plans
+            print(json.dumps(line), flush=True)
+
+    def plan_brief(op, T, N, K, f32):
+        p = dp.plan(op, T, N, K, f32)
+        return {k: p[k] for k in ("cta_pair", "block_n", "splits", "full_units", "swap_ab")}
+
+    def bf(*shape, scale=1.0):
+        return (torch.randn(*shape, generator=g, device=device) * scale).to(torch.bfloat16)
+
+    def f32(*shape, scale=1.0):
+        return torch.randn(*shape, generator=g, device=device) * scale
+
+    def dense_ops(T, N, K, X, W, dY, od):
+        e = 4 if od == torch.float32 else 2
+        return {
+            "fwd": (lambda: dp.dp_gemm_fwd(X, W, out_dtype=od, workspace=ws), 2 * T * K + 2 * N * K + e * T * N),
+            "dgrad": (lambda: dp.dp_gemm_dgrad(dY, W, out_dtype=od, workspace=ws), 2 * T * N + 2 * N * K + e * T * K),
+            "wgrad": (lambda: dp.dp_gemm_wgrad(dY, X, out_dtype=od, workspace=ws), 2 * T * N + 2 * T * K + e * N * K),
+        }
+
+    which = set(args.suite.split(","))
+    if "cfg1" in which:  # dense 4096 -> 1024 at T = 64, BF16 and FP32 output
+        T, N, K = 64, 1024, 4096
+        X, W, dY = bf(T, K), bf(N, K, scale=1 / 64), bf(T, N)
+        for od, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+            for op, (fn, nb) in dense_ops(T, N, K, X, W, dY, od).items():
+                report("cfg1", f"{op} T={T} {K}->{N} {name}", 2 * T * N * K, 2 * T * N * K, nb, fn,
+                       plan_brief(op, T, N, K, od == torch.float32))
+    if "cfg2" in which:  # FP32 router 4096 -> 256 at T in {64, 256, 1024}
+        K, N = 4096, 256
+        for T in (64, 256, 1024):
+            X, W, dY = f32(T, K), f32(N, K, scale=0.02), f32(T, N)
+            ops = {"router_fwd": (lambda: dp.router_fwd(X, W, workspace=ws), 4 * (T * K + N * K + T * N)),
+                   "router_dgrad": (lambda: dp.router_dgrad(dY, W, workspace=ws), 4 * (T * N + N * K + T * K)),
+                   "router_wgrad": (lambda: dp.router_wgrad(dY, X, workspace=ws), 4 * (T * N + T * K + N * K))}
+            for op, (fn, nb) in ops.items():
+                report("cfg2", f"{op} T={T}", 2 * T * N * K, 3 * 2 * T * N * K, nb, fn, plan_brief(op, T, N, K, True))
+            del X, W, dY
+    if "cfg3" in which:  # wide 4096 -> 12288, BF16 out
+        N, K = 12288, 4096
+        for T in (16384, 16231):
+            X, W, dY = bf(T, K), bf(N, K, scale=1 / 64), bf(T, N)
+            for op, (fn, nb) in dense_ops(T, N, K, X, W, dY, torch.bfloat16).items():
+                report("cfg3", f"{op} T={T}", 2 * T * N * K, 2 * T * N * K, nb, fn, plan_brief(op, T, N, K, False))
+            del X, W, dY
+    if "cfg4" in which:  # thin-N weight gradient
+        for T in (1025, 16173, 65537):
+            Xf = bf(T, 5120)
+            for K, N in ((4096, 64), (4096, 128), (4096, 512), (5120, 48), (5120, 64)):
+                X = Xf[:, :K]
+                dY = bf(T, N)
+                for od, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+                    e = 4 if od == torch.float32 else 2
+                    out = torch.empty(N, K, dtype=od, device=device)
+                    fn = (lambda dY=dY, X=X, out=out, od=od: dp.dp_gemm_wgrad(dY, X, out=out, out_dtype=od, workspace=ws))
+                    report("cfg4", f"wgrad T={T} {K}->{N} {name}", 2 * T * N * K, 2 * T * N * K,
+                           2 * T * N + 2 * T * K + e * N * K, fn, plan_brief("wgrad", T, N, K, od == torch.float32))
+            del Xf
+    if "cfg5" in which:  # checkpointed step: fwd, recompute fwd, dgrad, wgrad
+        for T in (1024, 4031, 16384):
+            for N in (1024, 12288):
+                K = 4096
+                X, W, dY = bf(T, K), bf(N, K, scale=1 / 64), bf(T, N)
+                Y = torch.empty(T, N, dtype=torch.bfloat16, device=device)
+                dX = torch.empty(T, K, dtype=torch.bfloat16, device=device)
+                dW = torch.empty(N, K, dtype=torch.bfloat16, device=device)
+
+                def step(X=X, W=W, dY=dY, Y=Y, dX=dX, dW=dW):
+                    dp.dp_gemm_fwd(X, W, out=Y, workspace=ws)
+                    dp.dp_gemm_fwd(X, W, out=Y, workspace=ws)
+                    dp.dp_gemm_dgrad(dY, W, out=dX, workspace=ws)
+                    dp.dp_gemm_wgrad(dY, X, out=dW, workspace=ws)
+                nb = 2 * (2 * T * K + 2 * N * K + 2 * T * N) + (2 * T * N + 2 * N * K + 2 * T * K) * 2
+                report("cfg5", f"2fwd+bwd T={T} {K}->{N} bf16", 4 * 2 * T * N * K, 4 * 2 * T * N * K, nb, step)
+                del X, W, dY, Y, dX, dW
+            K, N = 4096, 256
+            X, W, dY = f32(T, K), f32(N, K, scale=0.02), f32(T, N)
+            Y, dX, dW = torch.empty(T, N, device=device), torch.empty(T, K, device=device), torch.empty(N, K, device=device)
+
+            def rstep(X=X, W=W, dY=dY, Y=Y, dX=dX, dW=dW):
+                dp.router_fwd(X, W, out=Y, workspace=ws)
+                dp.router_fwd(X, W, out=Y, workspace=ws)
+                dp.router_dgrad(dY, W, out=dX, workspace=ws)
+                dp.router_wgrad(dY, X, out=dW, workspace=ws)
+            nb = 4 * (2 * (T * K + N * K + T * N) + 2 * (T * N + N * K + T * K))
+            report("cfg5", f"router 2fwd+bwd T={T} {K}->{N} f32", 4 * 2 * T * N * K, 3 * 4 * 2 * T * N * K, nb, rstep)
+            del X, W, dY, Y, dX, dW
+    assert dp.device_error() == 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,10 +595,16 @@ def main():
     ap.add_argument("--profile-N", type=int, default=0)
     ap.add_argument("--profile-K", type=int, default=0)
     ap.add_argument("--profile-f32", action="store_true")
+    ap.add_argument("--suite", default=None,
+                    help="comma list of cfg1..cfg5: per-op eager/graph measurements of those configurations")
+    ap.add_argument("--suite-reps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_env()
+    if args.suite:
+        run_suite(args, local)
+        return
     if args.profile_op:
         print(json.dumps(run_profile_case(args, local)), flush=True)
         return

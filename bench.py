@@ -420,10 +420,13 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------ measurement suite
 
 def run_suite(args, local):
-    """Every configuration of the workload set, per op, eager and CUDA-graph launch,
-    cold L2 before every call: microseconds, TFLOP/s, algorithmic GB/s and the
+    """Every configuration of the workload set, per op, cold L2 before every call,
+    timed three ways: CUDA events around an eager call, events around a CUDA-graph
+    replay, and the kernel span of an eager call from the CUPTI trace (first start
+    to last end of this library's kernels, excluding the launch latency that the
+    events include).  Reported: microseconds, TFLOP/s, algorithmic GB/s and the
     fraction of the bounding roofline (tensor for arithmetic intensity above the
-    ridge, HBM below).  One JSON line per case."""
+    ridge, HBM below).  One JSON line per case and timing."""
     import fp32_dense_projection_gb300 as dp
     from fp32_dense_projection_gb300 import build as dpbuild
 
@@ -477,11 +480,38 @@ def run_suite(args, local):
         del gr
         return statistics.median(ts)
 
+    def span(fn):
+        # kernel span as a CUPTI trace records it: first start to last end of this
+        # library's kernels in one call (cold L2 before each call), median over calls
+        from torch.profiler import ProfilerActivity, profile
+        fn()
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(reps):
+                flush.zero_()
+                fn()
+            torch.cuda.synchronize()
+        mine = ("gemm_bf16_kernel", "split_reduce_kernel", "split_x3_kernel")
+        calls, cur = [], None
+        for e in sorted((e for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA),
+                        key=lambda e: e.time_range.start):
+            if any(k in e.name for k in mine):
+                if cur is None:
+                    cur = [e.time_range.start, e.time_range.end]
+                else:
+                    cur[1] = max(cur[1], e.time_range.end)
+            elif cur is not None:
+                calls.append(cur[1] - cur[0])
+                cur = None
+        if cur is not None:
+            calls.append(cur[1] - cur[0])
+        return statistics.median(calls) if calls else float("nan")
+
     def report(cfg, case, flop, tc_flop, nbytes, fn, plans=None):
         # flop: 2TNK of the op(s); tc_flop: tensor-pipe work (3x for BF16x3); nbytes: algorithmic bytes
         ai = tc_flop / nbytes
         bound = "tensor" if ai > ridge else "hbm"
-        for mode, timer in (("eager", eager), ("graph", graph)):
+        for mode, timer in (("eager", eager), ("graph", graph), ("kernel span", span)):
             us = timer(fn)
             tflops = flop / us / 1e6
             gbs = nbytes / us / 1e3
@@ -511,6 +541,10 @@ def run_suite(args, local):
             "wgrad": (lambda: dp.dp_gemm_wgrad(dY, X, out_dtype=od, workspace=ws), 2 * T * N + 2 * T * K + e * N * K),
         }
 
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]):  # CUPTI warm-up: the first session can miss kernels
+        flush.zero_()
+        torch.cuda.synchronize()
     which = set(args.suite.split(","))
     if "cfg1" in which:  # dense 4096 -> 1024 at T = 64, BF16 and FP32 output
         T, N, K = 64, 1024, 4096

@@ -9,6 +9,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "dp_gemm.h"
 #include "gemm_kernel.cuh"
@@ -209,7 +211,8 @@ int env_int(const char* name) {
   return v ? std::atoi(v) : 0;
 }
 
-// Plan overrides for tuning and tests, read on every call: DP_FORCE_BN,
+// Plan overrides for tuning and tests, read on every call (DP_FORCE_CLUSTER_SUM=0,
+// read in cluster_fixup, keeps split sums in the reduction kernel): DP_FORCE_BN,
 // DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS (> 0 forces), DP_FORCE_SWAP (0 or 1: the
 // weight-gradient orientation) and DP_FORCE_PAIR (0 or 1: single-CTA or CTA-pair
 // tiles).  Unset in normal use.
@@ -267,6 +270,43 @@ dp_status check_sizes(int64_t T, int64_t N, int64_t K, int op) {
 
 // ------------------------------------------------------------ one GEMM launch
 
+// In-cluster sum of split partials: for plans of single-CTA tiles that split every
+// tile S <= 8 ways with one unit per CTA, the GEMM runs as clusters of S CTAs and
+// each cluster sums its tile's partials after the main loop (no second kernel).
+// Used only if the device runs all those clusters at once (clusters live inside one
+// GPC); otherwise the reduction kernel does the same sum.  Both give the same bits.
+struct ClusterKey {
+  int dev, view, bn, x3, size;
+};
+std::mutex g_cluster_mutex;
+std::vector<std::pair<ClusterKey, int>> g_cluster_capacity;
+
+int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
+  if (p.pair || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid) return 0;
+  const char* off = std::getenv("DP_FORCE_CLUSTER_SUM");  // "0": always the reduction kernel (tests)
+  if (off && std::atoi(off) == 0) return 0;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return 0;
+  const int view = p.a_mn ? 2 : (p.b_mn ? 1 : 0);
+  const ClusterKey k = {cur, view, p.bn, x3 ? 1 : 0, p.splits};
+  int cap = -1;
+  {
+    std::lock_guard<std::mutex> lock(g_cluster_mutex);
+    for (const auto& kv : g_cluster_capacity)
+      if (kv.first.dev == k.dev && kv.first.view == k.view && kv.first.bn == k.bn && kv.first.x3 == k.x3 &&
+          kv.first.size == k.size)
+        cap = kv.second;
+    if (cap < 0) {
+      const int grid = dev.sm_count - dev.sm_count % p.splits;
+      cap = view == 0 ? max_clusters_kk(p.bn, x3, p.splits, grid)
+                      : (view == 1 ? (x3 ? 0 : max_clusters_km(p.bn, p.splits, grid))
+                                   : max_clusters_mm(p.bn, x3, p.splits, grid));
+      g_cluster_capacity.push_back({k, cap});
+    }
+  }
+  return static_cast<int64_t>(cap) * p.splits >= p.grid ? p.splits : 0;
+}
+
 // A: operand (m, k) -- K-major: [gm][gk] matrix; MN-major: [gk][gm] matrix.
 // B: operand (n, k) -- K-major: [gn][gk] matrix; MN-major: [gk][gn] matrix.
 // Router BF16x3 plans (x3): A is FP32, B and B_lo are B's bf16 hi and lo planes.
@@ -318,6 +358,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.out_trans = p.swap ? 1 : 0;
   a.a3d = a3d ? 1 : 0;
   a.b3d = b3d ? 1 : 0;
+  a.cluster_fixup = cluster_fixup(p, x3, dev);
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;
@@ -332,9 +373,11 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
     e = launch_gemm_km(p.bn, l, stream);
   else if (p.a_mn && p.b_mn)
     e = launch_gemm_mm(p.bn, l, stream);
-  // split tiles: the ordered sum of their partials, queued behind the GEMM
+  // split tiles: the ordered sum of their partials, queued behind the GEMM (unless
+  // the GEMM's clusters sum them themselves)
   const int64_t split_tiles = p.tiles_m * p.tiles_n - p.full_units;
-  if (e == cudaSuccess && p.splits > 1 && split_tiles > 0) e = launch_split_reduce(l, p.bn, p.pair, split_tiles, stream);
+  if (e == cudaSuccess && p.splits > 1 && split_tiles > 0 && a.cluster_fixup <= 1)
+    e = launch_split_reduce(l, p.bn, p.pair, split_tiles, stream);
   return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
 }
 

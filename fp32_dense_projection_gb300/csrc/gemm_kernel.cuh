@@ -57,6 +57,9 @@ struct GemmArgs {
   // MN-major operands whose tensor map is 3-D, [column group][contraction row][128 B]:
   // the groups of a tile arrive in one load instead of one load per group
   int32_t a3d, b3d;
+  // > 1: launched as clusters of `splits` CTAs, one split tile per cluster and one
+  // unit per CTA; the cluster sums its partials itself after the main loop
+  int32_t cluster_fixup;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
@@ -256,6 +259,66 @@ __device__ __forceinline__ void store_block32(const GemmArgs& a, uint32_t buf, i
   }
   stage_block32(a, buf, lane, v);
   flush_block32(a, buf, lane, m0, col0);
+}
+
+// In-kernel ordered sum for cluster plans: the S CTAs of a cluster computed the S
+// splits of one tile (CTA rank r = split r, one unit each) and wrote their FP32
+// partials.  After a cluster barrier (release / acquire, so every partial is
+// visible), CTA r sums rows [r*128/S, (r+1)*128/S) of the tile over all S partials
+// in ascending split order and rounds once: the same arithmetic as the reduction
+// kernel, so the two give the same bits.  One float4 per step, its S loads issued
+// together; consecutive threads take consecutive rows (512-byte partial reads).
+template <int BN>
+__device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthreads) {
+  __threadfence();
+  cluster_sync();
+  const int S = a.splits;
+  const int u = static_cast<int>(blockIdx.x);  // this CTA's only unit
+  const Unit w = decode_unit(a, u);
+  const int r0 = w.s * kBlockM / S, r1 = (w.s + 1) * kBlockM / S, rows = r1 - r0;
+  const int64_t m_tile = static_cast<int64_t>(w.tm) * kBlockM, n0 = static_cast<int64_t>(w.tn) * BN;
+  const size_t pstride = static_cast<size_t>(kBlockM) * BN / 4;
+  const float4* p0 = a.partials + static_cast<size_t>(w.ptile) * S * pstride;
+  const int total = rows * (BN / 4);
+  for (int e = static_cast<int>(threadIdx.x); e < total; e += nthreads) {
+    const int j4 = e / rows, row = r0 + (e - j4 * rows);
+    const int64_t m = m_tile + row, col = n0 + 4 * j4;
+    if (m >= a.gm || col >= a.gn) continue;
+    const float4* src = p0 + static_cast<size_t>(j4) * kBlockM + row;
+    float4 x[8];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < S) x[k] = __ldcg(src + k * pstride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < S) {
+        if (k == 0) {
+          acc = x[k];
+        } else {
+          acc.x += x[k].x;
+          acc.y += x[k].y;
+          acc.z += x[k].z;
+          acc.w += x[k].w;
+        }
+      }
+    if (a.out_trans) {
+      const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t o = (col + t) * a.ldo + m;
+        if (a.out_f32)
+          static_cast<float*>(a.out)[o] = v[t];
+        else
+          static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(v[t], 0.0f) & 0xFFFFu);
+      }
+    } else if (a.out_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + m * a.ldo + col) = acc;
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + m * a.ldo + col) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+  }
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
@@ -788,6 +851,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if (!PAIR && args.cluster_fixup > 1) cluster_fixup_sum<BN>(args, C::THREADS);
 }
 
 // Host-side launch of one instantiation (defined in the per-view .cu files).
@@ -801,6 +865,10 @@ struct GemmLaunch {
   bool pdl;   // launched as a programmatic dependent of the operand-split kernel
 };
 
+// Clusters of `cluster` single-CTA tiles of width bn that run at once (0 if none).
+int max_clusters_kk(int bn, bool x3, int cluster, int grid);
+int max_clusters_km(int bn, int cluster, int grid);
+int max_clusters_mm(int bn, bool x3, int cluster, int grid);
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
 cudaError_t launch_gemm_km(int bn, const GemmLaunch& l, cudaStream_t stream);  // input gradient
 cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream);  // weight gradient
@@ -833,9 +901,10 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (PAIR) {  // single-CTA tiles launch without a cluster
+  const int cluster = PAIR ? 2 : (l.args.cluster_fixup > 1 ? l.args.cluster_fixup : 1);
+  if (cluster > 1) {  // CTA pairs, or the split CTAs of a tile for an in-cluster sum
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -848,6 +917,29 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.tmB2, l.args);
+}
+
+// How many clusters of `cluster` CTAs of this instantiation the device runs at once
+// (clusters live inside one GPC, so this can be fewer than SMs / cluster).
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
+int max_active_clusters_t(int cluster, int grid) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(TileCfg<BN, PAIR, X3>::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<BN, PAIR, X3>::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear: treated as "no cluster plan"
+    return 0;
+  }
+  return n;
 }
 
 template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>

@@ -66,4 +66,20 @@ cudaError_t set_attributes_kk() {
   return e;
 }
 
+int max_clusters_kk(int bn, bool x3, int cluster, int grid) {
+  switch (bn) {
+    case 64:
+      return x3 ? max_active_clusters_t<64, false, false, false, true>(cluster, grid)
+                : max_active_clusters_t<64, false, false, false>(cluster, grid);
+    case 128:
+      return x3 ? max_active_clusters_t<128, false, false, false, true>(cluster, grid)
+                : max_active_clusters_t<128, false, false, false>(cluster, grid);
+    case 256:
+      return x3 ? max_active_clusters_t<256, false, false, false, true>(cluster, grid)
+                : max_active_clusters_t<256, false, false, false>(cluster, grid);
+    default:
+      return 0;
+  }
+}
+
 }  // namespace dp

@@ -39,4 +39,17 @@ cudaError_t set_attributes_km() {
   return e;
 }
 
+int max_clusters_km(int bn, int cluster, int grid) {
+  switch (bn) {
+    case 64:
+      return max_active_clusters_t<64, false, true, false>(cluster, grid);
+    case 128:
+      return max_active_clusters_t<128, false, true, false>(cluster, grid);
+    case 256:
+      return max_active_clusters_t<256, false, true, false>(cluster, grid);
+    default:
+      return 0;
+  }
+}
+
 }  // namespace dp

@@ -66,4 +66,20 @@ cudaError_t set_attributes_mm() {
   return e;
 }
 
+int max_clusters_mm(int bn, bool x3, int cluster, int grid) {
+  switch (bn) {
+    case 64:
+      return x3 ? max_active_clusters_t<64, true, true, false, true>(cluster, grid)
+                : max_active_clusters_t<64, true, true, false>(cluster, grid);
+    case 128:
+      return x3 ? max_active_clusters_t<128, true, true, false, true>(cluster, grid)
+                : max_active_clusters_t<128, true, true, false>(cluster, grid);
+    case 256:
+      return x3 ? max_active_clusters_t<256, true, true, false, true>(cluster, grid)
+                : max_active_clusters_t<256, true, true, false>(cluster, grid);
+    default:
+      return 0;
+  }
+}
+
 }  // namespace dp

@@ -26,6 +26,8 @@ constexpr double kL2BytesPerNsPerSm = 160.0;  // operand bytes an SM pulls when 
 constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 45.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceNs = 2000.0;          // the split reduction kernel's launch and one L2 round trip
+constexpr double kClusterSumNs = 700.0;       // in-cluster sum (one unit per CTA, clusters of <= 4 run at once)
+constexpr int kClusterSumMax = 4;             // largest cluster the device is assumed to co-schedule for it
 constexpr double kReduceBytesPerNs = 4000.0;  // partial bytes it sums per ns (whole GPU, L2-resident)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
@@ -127,10 +129,14 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
             unit_ns(v, t, ceil_div(nkb, splits), splits > 1, active_sms, reuse, out_bytes);
   const double t_dram = (unique + static_cast<double>(v.gm) * v.gn * out_bytes) / kHbmBytesPerNs;
   time = std::max(time, t_dram);
-  if (splits > 1 && split_units > 0)  // every split tile's partials, summed by the reduction kernel
-    time += kReduceNs + static_cast<double>(tiles - full) * (t.pair ? 2 : 1) * splits *
-                            std::min<double>(kBlockM, a_rows) * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) *
-                            4.0 / kReduceBytesPerNs;
+  if (splits > 1 && split_units > 0) {  // every split tile's partials, summed in split order
+    // by the GEMM's own clusters (single-CTA tiles, every tile split, one unit per
+    // CTA) or else by the reduction kernel
+    const bool in_cluster = !t.pair && full == 0 && splits <= kClusterSumMax && units <= slots;
+    time += (in_cluster ? kClusterSumNs : kReduceNs) +
+            static_cast<double>(tiles - full) * (t.pair ? 2 : 1) * splits * std::min<double>(kBlockM, a_rows) *
+                static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0 / kReduceBytesPerNs;
+  }
   return time;
 }
 

@@ -201,3 +201,25 @@ def test_one_workspace_serves_every_op_in_turn():
         want = gpu(op, a, b, workspace=fresh, **kw)
         assert torch.equal(got.view(torch.int32), want.view(torch.int32)), (i, op)
     no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K", [("wgrad", 16173, 64, 4096), ("wgrad", 16173, 48, 5120), ("fwd", 64, 1024, 4096),
+                                      ("router_fwd", 1024, 256, 4096), ("wgrad", 4100, 64, 1024)])
+def test_cluster_sum_matches_reduction_kernel(monkeypatch, op, T, N, K):
+    # plans with one split unit per CTA sum their partials inside the GEMM's clusters;
+    # the reduction kernel adds the same partials in the same order: same bits
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K).items()}
+    a, b = operands(op, c)
+    kw = {} if op.startswith("router") else {"out_dtype": torch.bfloat16}
+    p = dp.plan(op, T, N, K, out_f32=op.startswith("router"))
+    if not (p["splits"] > 1 and p["full_units"] == 0 and not p["cta_pair"]):
+        pytest.skip(f"not a split-everything single-CTA plan: {p}")
+    in_cluster = gpu(op, a, b, **kw)
+    monkeypatch.setenv("DP_FORCE_CLUSTER_SUM", "0")
+    by_kernel = gpu(op, a, b, **kw)
+    bits = torch.int16 if in_cluster.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(in_cluster.view(bits), by_kernel.view(bits))
+    ref = full_ref(op, *operands(op, case_tensors(op, T, N, K)))
+    assert_budget(as_f64(in_cluster), ref, "bf16" if bits == torch.int16 else "f32", f"{op} T={T} in-cluster sum")
+    no_device_fault()
+

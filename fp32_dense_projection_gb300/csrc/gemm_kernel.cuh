@@ -366,8 +366,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // X3: the B loads' arrival and one per converter warp (of both CTAs of a pair)
-      mbar_init(full_bar(s), X3 ? 1 + (PAIR ? 2 : 1) * C::CONV_WARPS : 1);
+      // X3: the B loads' arrival and one per converter warp; for a pair, the leader's
+      // also takes one forwarded arrival from the peer, whose own full barriers only
+      // collect its converters
+      mbar_init(full_bar(s), !X3 ? 1 : (PAIR && rank != 0) ? C::CONV_WARPS : 1 + C::CONV_WARPS + (PAIR ? 1 : 0));
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < SSTAGES; ++s) {
@@ -427,16 +429,23 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         auto next = [&](Cursor& c) {
           if (++c.kb == c.kb1) seek(c, c.u + unit_step);
         };
-        Cursor xc, bc;
+        Cursor xc, bc, fc;
         seek(xc, unit0);
         seek(bc, unit0);
+        seek(fc, unit0);
+        // (a pair's peer: one arrival on the leader's full barrier per stage, once this
+        // CTA's converters have filled it)
+        const bool forward = PAIR && rank != 0;
+        int fstage = 0;
+        uint32_t fphase = 0;
+        if (!forward) fc.u = args.units;
         uint32_t idle = 0;
         uint64_t t_idle = 0;
         // The staging ring is filled first: A (FP32, the caller's) does not depend on
         // the split kernel, so its loads overlap that kernel's tail.
         bool b_ready = false;
         int issued_x = 0;
-        while (xc.u < args.units || bc.u < args.units) {
+        while (xc.u < args.units || bc.u < args.units || fc.u < args.units) {
           if (xc.u >= args.units) issued_x = SSTAGES;  // (fewer blocks than staging slots)
           bool progressed = false;
           if (xc.u < args.units && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
@@ -508,6 +517,15 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
               phase ^= 1u;
             }
             next(bc);
+            progressed = true;
+          }
+          if (fc.u < args.units && mbar_peek(full_bar(fstage), fphase)) {
+            mbar_arrive_cluster(map_shared_rank(full_bar(fstage), 0));
+            if (++fstage == STAGES) {
+              fstage = 0;
+              fphase ^= 1u;
+            }
+            next(fc);
             progressed = true;
           }
           // bounded: give up once neither ring has moved for kWaitLimitNs
@@ -748,11 +766,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(sempty_bar(sstage));  // staging tile may be reloaded
-          // A half of the bf16 stage ready for the MMAs (the leader's, for a pair)
-          if (PAIR)
-            mbar_arrive_cluster(map_shared_rank(full_bar(stage), 0));
-          else
-            mbar_arrive(full_bar(stage));
+          // A half of the bf16 stage ready (a pair's peer forwards it to the leader)
+          mbar_arrive(full_bar(stage));
         }
         if (++sstage == SSTAGES) {
           sstage = 0;

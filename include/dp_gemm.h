@@ -166,7 +166,11 @@ dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int6
  * pages) and K the hidden size.  Each FP32 operand value x is split into bf16
  * hi = RNE(x) and lo = RNE(x - hi); every product a*b is formed as
  * hi_a*hi_b + hi_a*lo_b + lo_a*hi_b on the BF16 tensor cores with FP32
- * accumulation (lo_a*lo_b is dropped). */
+ * accumulation (lo_a*lo_b is dropped).  The operand the whole output reuses (W,
+ * or dY for the weight gradient; both for the input gradient) is split once per
+ * call into bf16 copies in the workspace (so router calls always need one);
+ * the streamed FP32 operand is split inside the GEMM.  The weight gradient is
+ * always computed as dW^T = X^T dY and stored transposed. */
 
 /* Router forward: Y[t][n] = sum_k X[t][k] * W[n][k];  X: T x K, W: N x K, Y: T x N. */
 dp_status router_fwd(const float* X, const float* W, float* Y,
@@ -193,6 +197,14 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
                           void* workspace, size_t workspace_bytes, dp_stream stream);
 
 /* ------------------------------------------------------------ planning, misc */
+/* Tuning and test overrides, read from the environment on every call (unset in
+ * normal use): DP_FORCE_BN (64 / 128 / 256), DP_FORCE_SPLITS (uniform split
+ * count), DP_FORCE_TAIL_SPLITS (split only the last partial wave, this many
+ * ways), DP_FORCE_SWAP (0 / 1: BF16 weight-gradient orientation), DP_FORCE_PAIR
+ * (0 / 1: single-CTA or CTA-pair tiles), DP_FORCE_CLUSTER_SUM=0 (sum split
+ * partials in the reduction kernel instead of inside the GEMM's clusters; the
+ * two give the same bits).  A forced plan is still deterministic and keeps the
+ * accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of
  * (op, T, N, K, out, sm_count), so a workspace sized here fits the call. */

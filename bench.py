@@ -637,7 +637,32 @@ def run_suite(args, local):
             nb = 4 * (2 * (T * K + N * K + T * N) + 2 * (T * N + N * K + T * K))
             report("cfg5", f"router 2fwd+bwd T={T} {K}->{N} f32", 4 * 2 * T * N * K, 3 * 4 * 2 * T * N * K, nb, rstep)
             del X, W, dY, Y, dX, dW
+    if "batched" in which:  # per-head projections, 128 heads, T = 4096: one batched launch vs 128 calls
+        H, T = 128, 4096
+        for N, K in ((512, 128), (128, 512)):
+            for op in ("fwd", "dgrad", "wgrad"):
+                X = bf(T, H, K).permute(1, 0, 2)              # [H, T, K] per-head views of [T, H, K]
+                dY = bf(T, H, N).permute(1, 0, 2)
+                W = bf(H, N, K, scale=1 / 16)
+                fb = {"fwd": lambda: dp.dp_gemm_fwd_batched(X, W, workspace=ws),
+                      "dgrad": lambda: dp.dp_gemm_dgrad_batched(dY, W, workspace=ws),
+                      "wgrad": lambda: dp.dp_gemm_wgrad_batched(dY, X, workspace=ws)}[op]
+                single = {"fwd": lambda: [dp.dp_gemm_fwd(X[h], W[h], workspace=ws) for h in range(H)],
+                          "dgrad": lambda: [dp.dp_gemm_dgrad(dY[h], W[h], workspace=ws) for h in range(H)],
+                          "wgrad": lambda: [dp.dp_gemm_wgrad(dY[h], X[h], workspace=ws) for h in range(H)]}[op]
+                nb = H * (2 * T * K + 2 * N * K + 2 * T * N)
+                report("batched", f"{op} {H} heads T={T} {K}->{N} batched", H * 2 * T * N * K, H * 2 * T * N * K,
+                       nb, fb, plan_brief_b(op, H, T, N, K))
+                report("batched", f"{op} {H} heads T={T} {K}->{N} {H} single calls", H * 2 * T * N * K,
+                       H * 2 * T * N * K, nb, single)
+                del X, dY, W
     assert dp.device_error() == 0
+
+
+def plan_brief_b(op, B, T, N, K):
+    import fp32_dense_projection_gb300 as dp
+    p = dp.plan_batched(op, B, T, N, K)
+    return {k: p[k] for k in ("cta_pair", "block_n", "splits", "full_units", "swap_ab", "tiles")}
 
 
 def main():
@@ -655,7 +680,7 @@ def main():
     ap.add_argument("--profile-K", type=int, default=0)
     ap.add_argument("--profile-f32", action="store_true")
     ap.add_argument("--suite", default=None,
-                    help="comma list of cfg1..cfg5: per-op eager/graph measurements of those configurations")
+                    help="comma list of cfg1..cfg5 (and 'batched'): per-op eager/graph/kernel-span measurements")
     ap.add_argument("--suite-reps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:

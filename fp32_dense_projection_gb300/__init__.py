@@ -46,7 +46,9 @@ class PlanInfo(ctypes.Structure):
         "block_m", "block_n", "block_k", "stages", "splits", "raster_group", "grid",
         "a_mn_major", "b_mn_major", "swap_ab", "cta_pair", "raster_rows", "reserved")] + [(n, ctypes.c_int64) for n in (
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
-        ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double)]
+        ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double),
+        ("batch", ctypes.c_int64), ("tiles", ctypes.c_int64), ("weight_kn", ctypes.c_int32),
+        ("reserved2", ctypes.c_int32)]
 
 
 def lib():
@@ -71,6 +73,12 @@ def lib():
             getattr(L, name).argtypes = [P, P, P] + rtail
             getattr(L, name + "_ex").argtypes = [P, I, P, I, P, I] + rtail
         L.dp_plan_query.argtypes = [S, I, I, I, S, S, ctypes.POINTER(PlanInfo)]
+        L.dp_plan_query_batched.argtypes = [S, I, I, I, I, S, S, S, ctypes.POINTER(PlanInfo)]
+        L.dp_workspace_size_batched.argtypes = [S, I, I, I, I, S, S, S, ctypes.POINTER(ctypes.c_size_t)]
+        btail = [I, I, I, I, S, S, P, Z, P]      # B T N K out deterministic ws ws_bytes stream
+        L.dp_gemm_fwd_batched.argtypes = [P, I, I, P, I, I, S, P, I, I] + btail
+        L.dp_gemm_dgrad_batched.argtypes = [P, I, I, P, I, I, S, P, I, I] + btail
+        L.dp_gemm_wgrad_batched.argtypes = [P, I, I, P, I, I, P, I, I, S] + btail
         L.dp_workspace_size.argtypes = [S, I, I, I, S, S, ctypes.POINTER(ctypes.c_size_t)]
         L.dp_init.argtypes = [S]
         L.dp_device_error.argtypes = [S]
@@ -99,7 +107,26 @@ def plan(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0) -
     info = PlanInfo()
     _check(lib().dp_plan_query(int(op), T, N, K, int(bool(out_f32)), int(sm_count), ctypes.byref(info)),
            "dp_plan_query")
-    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if not name.startswith("reserved")}
+
+
+def plan_batched(op, B: int, T: int, N: int, K: int, out_f32: bool = False, weight_kn: bool = False,
+                 sm_count: int = 0) -> dict:
+    """The plan of a batched BF16 call (op "fwd" / "dgrad" / "wgrad")."""
+    op = OP_NAMES.get(op, op)
+    info = PlanInfo()
+    _check(lib().dp_plan_query_batched(int(op), B, T, N, K, int(bool(out_f32)), int(bool(weight_kn)),
+                                       int(sm_count), ctypes.byref(info)), "dp_plan_query_batched")
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if not name.startswith("reserved")}
+
+
+def workspace_size_batched(op, B: int, T: int, N: int, K: int, out_f32: bool = False, weight_kn: bool = False,
+                           sm_count: int = 0) -> int:
+    op = OP_NAMES.get(op, op)
+    n = ctypes.c_size_t(0)
+    _check(lib().dp_workspace_size_batched(int(op), B, T, N, K, int(bool(out_f32)), int(bool(weight_kn)),
+                                           int(sm_count), ctypes.byref(n)), "dp_workspace_size_batched")
+    return int(n.value)
 
 
 def workspace_size(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0) -> int:
@@ -270,6 +297,92 @@ def router_wgrad(dY, X, out=None, deterministic=True, workspace=None, stream=Non
         raise ValueError("router_wgrad: X must be T x H")
     return _gemm(OP_ROUTER_WGRAD, "router_wgrad", dY, X, (N, K), out, torch.float32, deterministic, workspace,
                  stream, T, N, K)
+
+
+def _bview(t: torch.Tensor, name: str):
+    """(leading dimension, batch stride) of a [B, rows, cols] view with unit column stride."""
+    if t.dim() != 3 or (t.size(2) > 1 and t.stride(2) != 1):
+        raise ValueError(f"{name}: operands must be [B, rows, cols] views with unit column stride")
+    ld = t.stride(1) if t.size(1) > 1 else t.size(2)
+    bs = t.stride(0) if t.size(0) > 1 else t.size(1) * ld
+    return ld, bs
+
+
+def _batched(op: int, name: str, a, b, out, out_shape, out_dtype, weight_kn, deterministic, workspace, stream,
+             B, T, N, K):
+    for t, nm in ((a, "first operand"), (b, "second operand")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name}: {nm} must be a CUDA bfloat16 tensor")
+    device = a.device
+    if out is None:
+        out = torch.empty(out_shape, dtype=out_dtype, device=device)
+    elif tuple(out.shape) != tuple(out_shape) or out.dtype != out_dtype:
+        raise ValueError(f"{name}: out must be {tuple(out_shape)} {out_dtype}")
+    out_f32 = out.dtype == torch.float32
+    if workspace is None:
+        workspace = _default_workspace(device).get(workspace_size_batched(op, B, T, N, K, out_f32, weight_kn))
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    (lda, bsa), (ldb, bsb), (ldo, bso) = _bview(a, name), _bview(b, name), _bview(out, name)
+    fn = getattr(lib(), name)
+    code = DP_OUT_F32 if out_f32 else DP_OUT_BF16
+
+    def call():
+        st = _stream(device, stream)
+        if op == OP_WGRAD:
+            return fn(_ptr(a), lda, bsa, _ptr(b), ldb, bsb, _ptr(out), ldo, bso, int(bool(weight_kn)), B, T, N, K,
+                      code, int(bool(deterministic)), _ptr(workspace), nbytes, st)
+        return fn(_ptr(a), lda, bsa, _ptr(b), ldb, bsb, int(bool(weight_kn)), _ptr(out), ldo, bso, B, T, N, K,
+                  code, int(bool(deterministic)), _ptr(workspace), nbytes, st)
+
+    if device.index == torch.cuda.current_device():
+        status = call()
+    else:
+        with torch.cuda.device(device):
+            status = call()
+    _check(status, name)
+    return out
+
+
+def dp_gemm_fwd_batched(X, W, out=None, out_dtype=torch.bfloat16, weight_layout="nk", deterministic=True,
+                        workspace=None, stream=None):
+    """Y[b] = X[b] W[b]^T for each b: X [B,T,K]; W [B,N,K] ("nk") or [B,K,N] ("kn"); Y [B,T,N]."""
+    kn = _layout(weight_layout)
+    B, T, K = X.shape
+    N = W.shape[2] if kn else W.shape[1]
+    if W.shape[0] != B or (W.shape[1] if kn else W.shape[2]) != K:
+        raise ValueError("dp_gemm_fwd_batched: W does not match X")
+    return _batched(OP_FWD, "dp_gemm_fwd_batched", X, W, out, (B, T, N), out_dtype, kn, deterministic,
+                    workspace, stream, B, T, N, K)
+
+
+def dp_gemm_dgrad_batched(dY, W, out=None, out_dtype=torch.bfloat16, weight_layout="nk", deterministic=True,
+                          workspace=None, stream=None):
+    """dX[b] = dY[b] W[b]: dY [B,T,N]; W [B,N,K] ("nk") or [B,K,N] ("kn"); dX [B,T,K]."""
+    kn = _layout(weight_layout)
+    B, T, N = dY.shape
+    K = W.shape[1] if kn else W.shape[2]
+    if W.shape[0] != B or (W.shape[2] if kn else W.shape[1]) != N:
+        raise ValueError("dp_gemm_dgrad_batched: W does not match dY")
+    return _batched(OP_DGRAD, "dp_gemm_dgrad_batched", dY, W, out, (B, T, K), out_dtype, kn, deterministic,
+                    workspace, stream, B, T, N, K)
+
+
+def dp_gemm_wgrad_batched(dY, X, out=None, out_dtype=torch.bfloat16, weight_layout="nk", deterministic=True,
+                          workspace=None, stream=None):
+    """dW[b] = dY[b]^T X[b]: dY [B,T,N]; X [B,T,K]; dW [B,N,K] ("nk") or [B,K,N] ("kn")."""
+    kn = _layout(weight_layout)
+    B, T, N = dY.shape
+    K = X.shape[2]
+    if X.shape[0] != B or X.shape[1] != T:
+        raise ValueError("dp_gemm_wgrad_batched: X does not match dY")
+    return _batched(OP_WGRAD, "dp_gemm_wgrad_batched", dY, X, out, (B, K, N) if kn else (B, N, K), out_dtype, kn,
+                    deterministic, workspace, stream, B, T, N, K)
+
+
+def _layout(weight_layout) -> bool:
+    if weight_layout not in ("nk", "kn"):
+        raise ValueError('weight_layout must be "nk" ([N, K] weights) or "kn" ([K, N])')
+    return weight_layout == "kn"
 
 
 OPS = {"fwd": dp_gemm_fwd, "dgrad": dp_gemm_dgrad, "wgrad": dp_gemm_wgrad,

@@ -101,17 +101,20 @@ EncodeTiledFn encode_fn() {
 // Map over a row-major [rows][cols] matrix (leading dimension ld elements) of bf16
 // (box = box_rows x 64 columns) or FP32 (box = box_rows x 32 columns): 128-byte
 // box rows, 128-byte swizzle, zero fill outside the matrix.
+// batch > 1: a third dimension of `batch` matrices `bstride` elements apart (box 1).
 bool encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
-                bool f32, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
+                bool f32, uint32_t box_cols, CUtensorMapSwizzle swizzle, int64_t batch = 1, int64_t bstride = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (f32 ? 4 : 2)};
-  const cuuint32_t box[2] = {box_cols ? box_cols : (f32 ? 32u : 64u), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const int es = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * es, static_cast<cuuint64_t>(bstride) * es};
+  const cuuint32_t box[3] = {box_cols ? box_cols : (f32 ? 32u : 64u), box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, batch > 1 ? 3 : 2,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D map over the same matrix for MN-major tiles: dimensions (inner, rows,
@@ -142,13 +145,14 @@ bool encode_map3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, 
 // per call signature for the same reason.)
 struct MapKey {
   const void* ptr;
-  int64_t rows, cols, ld;
+  int64_t rows, cols, ld, batch, bstride;
   uint32_t box_rows, box_cols;
   int f32, swizzle;
   uint32_t groups;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows &&
-           box_cols == o.box_cols && f32 == o.f32 && swizzle == o.swizzle && groups == o.groups;
+           box_cols == o.box_cols && f32 == o.f32 && swizzle == o.swizzle && groups == o.groups &&
+           batch == o.batch && bstride == o.bstride;
   }
 };
 
@@ -170,12 +174,14 @@ thread_local MapEntry t_maps[kMapCacheSize];
 // groups > 0: the 3-D map of encode_map3 with inner = box_cols (or 64 / 32 columns).
 bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows,
               bool f32 = false, uint32_t box_cols = 0, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
-              uint32_t groups = 0) {
-  const MapKey k = {ptr, rows, cols, ld, box_rows, box_cols, f32 ? 1 : 0, static_cast<int>(swizzle), groups};
+              uint32_t groups = 0, int64_t batch = 1, int64_t bstride = 0) {
+  const MapKey k = {ptr, rows, cols, ld, batch, bstride, box_rows, box_cols, f32 ? 1 : 0, static_cast<int>(swizzle),
+                    groups};
   uint64_t h = mix(mix(mix(reinterpret_cast<uintptr_t>(ptr), static_cast<uint64_t>(rows)), static_cast<uint64_t>(cols)),
                    static_cast<uint64_t>(ld));
   h = mix(mix(h, box_rows | (static_cast<uint64_t>(box_cols) << 32)),
           static_cast<uint64_t>(k.f32 * 16 + k.swizzle) | (static_cast<uint64_t>(groups) << 8));
+  h = mix(mix(h, static_cast<uint64_t>(batch)), static_cast<uint64_t>(bstride));
   MapEntry& e = t_maps[h & (kMapCacheSize - 1)];
   if (e.valid && e.key == k) {
     *map = e.map;
@@ -183,7 +189,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
   }
   const bool ok = groups > 0 ? encode_map3(map, ptr, rows, cols, ld, box_cols ? box_cols : (f32 ? 32u : 64u), box_rows,
                                             groups, f32)
-                             : encode_map(map, ptr, rows, cols, ld, box_rows, f32, box_cols, swizzle);
+                             : encode_map(map, ptr, rows, cols, ld, box_rows, f32, box_cols, swizzle, batch, bstride);
   if (!ok) return false;
   e.valid = true;
   e.key = k;
@@ -218,14 +224,15 @@ int env_int(const char* name) {
 // tiles).  Unset in normal use.
 struct PlanEntry {
   bool valid = false;
-  int op, out_f32, sm;
-  int64_t T, N, K;
+  int op, out_f32, sm, w_kn;
+  int64_t T, N, K, batch;
   Overrides o;
   Plan plan;
 };
 thread_local PlanEntry t_plans[kPlanCacheSize];
 
-bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan) {
+bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan, int64_t batch = 1,
+              int w_kn = 0) {
   const char* sw = std::getenv("DP_FORCE_SWAP");
   const char* pr = std::getenv("DP_FORCE_PAIR");
   Overrides o;
@@ -239,14 +246,17 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
   h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
               (o.swap + 1) * 3 + (o.pair + 1));
+  h = mix(h, static_cast<uint64_t>(batch) * 2 + static_cast<uint64_t>(w_kn));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
-      e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
-      e.o.pair == o.pair) {
+      e.batch == batch && e.w_kn == w_kn && e.o.bn == o.bn && e.o.splits == o.splits &&
+      e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair) {
     *plan = e.plan;
     return true;
   }
-  if (!make_plan(op, T, N, K, out_f32, sm, plan, o)) return false;
+  if (!make_plan(op, T, N, K, out_f32, sm, plan, o, batch, w_kn != 0)) return false;
+  e.batch = batch;
+  e.w_kn = w_kn;
   e.valid = true;
   e.op = op;
   e.T = T;
@@ -310,9 +320,12 @@ int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
 // A: operand (m, k) -- K-major: [gm][gk] matrix; MN-major: [gk][gm] matrix.
 // B: operand (n, k) -- K-major: [gn][gk] matrix; MN-major: [gk][gn] matrix.
 // Router BF16x3 plans (x3): A is FP32, B and B_lo are B's bf16 hi and lo planes.
+// Batched plans: bsa / bsb / bso are the elements between consecutive batches of
+// A, B and the output.
 dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
-                      int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, cudaStream_t stream) {
-  if (p.units > 0x7FFFFFFF || p.tiles_m > 0x7FFFFFFF || p.tiles_n > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF)
+                      int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, cudaStream_t stream,
+                      int64_t bsa = 0, int64_t bsb = 0, int64_t bso = 0) {
+  if (p.units > 0x7FFFFFFF || p.tiles > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF || p.batch > 0xFFFFFF)
     return DP_ERR_UNSUPPORTED;
   GemmLaunch l;
   std::memset(&l, 0, sizeof(l));
@@ -323,15 +336,17 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   const uint32_t b_rows = static_cast<uint32_t>(p.pair ? p.bn / 2 : p.bn);
   // MN-major tiles load as one 3-D box when the matrix's columns are whole groups
   const uint32_t a_inner = x3 ? 32u : 64u;
-  const bool a3d = p.a_mn && p.gm % a_inner == 0;
-  const bool b3d = p.b_mn && p.gn % 64 == 0;
+  const int64_t nb = p.batch;
+  const bool a3d = p.a_mn && p.gm % a_inner == 0 && nb == 1;
+  const bool b3d = p.b_mn && p.gn % 64 == 0 && nb == 1;
   const uint32_t a_groups = a3d ? kBlockM / a_inner : 0u, b_groups = b3d ? b_rows / 64 : 0u;
-  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, x3, 0, CU_TENSOR_MAP_SWIZZLE_128B, a_groups)
-                           : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, x3);
+  const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const bool ok_a = p.a_mn ? make_map(&l.tmA, A, p.gk, p.gm, lda, kb_rows, x3, 0, sw128, a_groups, nb, bsa)
+                           : make_map(&l.tmA, A, p.gm, p.gk, lda, kBlockM, x3, 0, sw128, 0, nb, bsa);
   bool ok_b;
   if (!x3) {
-    ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, false, 0, CU_TENSOR_MAP_SWIZZLE_128B, b_groups)
-                  : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows);
+    ok_b = p.b_mn ? make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, false, 0, sw128, b_groups, nb, bsb)
+                  : make_map(&l.tmB, B, p.gn, p.gk, ldb, b_rows, false, 0, sw128, 0, nb, bsb);
     l.tmB2 = l.tmB;
   } else if (p.b_mn) {  // 64-column groups of 32 rows, 128-byte swizzle
     ok_b = make_map(&l.tmB, B, p.gk, p.gn, ldb, kb_rows, false, 0, CU_TENSOR_MAP_SWIZZLE_128B, b_groups) &&
@@ -352,10 +367,13 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.group = p.group;
   a.raster_m = p.raster_m ? 1 : 0;
   a.units = static_cast<int32_t>(p.units);
+  a.batch = static_cast<int32_t>(nb);
+  a.tiles_per_batch = static_cast<int32_t>(p.tiles_m * p.tiles_n);
+  a.out_bstride = bso;
   a.out = out;
   a.ldo = ldo;
   a.out_f32 = p.out_f32;
-  a.out_trans = p.swap ? 1 : 0;
+  a.out_trans = p.out_trans ? 1 : 0;
   a.a3d = a3d ? 1 : 0;
   a.b3d = b3d ? 1 : 0;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
@@ -375,7 +393,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
     e = launch_gemm_mm(p.bn, l, stream);
   // split tiles: the ordered sum of their partials, queued behind the GEMM (unless
   // the GEMM's clusters sum them themselves)
-  const int64_t split_tiles = p.tiles_m * p.tiles_n - p.full_units;
+  const int64_t split_tiles = p.tiles - p.full_units;
   if (e == cudaSuccess && p.splits > 1 && split_tiles > 0 && a.cluster_fixup <= 1)
     e = launch_split_reduce(l, p.bn, p.pair, split_tiles, stream);
   return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
@@ -458,6 +476,83 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
   if (op == kOpRouterWgrad)  // dW^T = X^T dY: A = X (FP32), B = dY planes; stored transposed
     return launch_view(p, *dev, b, ldb, sb, p.ld_split_b, sb + T * p.ld_split_b, out, ldo, ws, stream);
   return launch_view(p, *dev, sa, p.ld_split_a, sb, p.ld_split_b, nullptr, out, ldo, ws, stream);
+}
+
+void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->block_m = p.bm;
+  info->block_n = p.bn;
+  info->block_k = p.bk;
+  info->stages = p.stages;
+  info->splits = p.splits;
+  info->raster_group = p.group;
+  info->grid = p.grid;
+  info->a_mn_major = p.a_mn ? 1 : 0;
+  info->b_mn_major = p.b_mn ? 1 : 0;
+  info->swap_ab = p.swap ? 1 : 0;
+  info->cta_pair = p.pair ? 1 : 0;
+  info->raster_rows = p.raster_m ? 1 : 0;
+  info->gemm_m = p.gm;
+  info->gemm_n = p.gn;
+  info->gemm_k = p.gk;
+  info->tiles_m = p.tiles_m;
+  info->tiles_n = p.tiles_n;
+  info->k_blocks = p.nkb;
+  info->units = p.units;
+  info->full_units = p.full_units;
+  info->workspace_bytes = T == 0 ? 0 : p.ws_bytes;
+  info->batch = p.batch;
+  info->weight_kn = p.w_kn ? 1 : 0;
+  info->tiles = p.tiles;
+  info->model_us = p.model_ns * 1e-3;
+}
+
+// Batched BF16 ops: B independent problems in one launch.  Operand / output matrix
+// b starts b * bs elements after matrix 0 (bs = 0: rows * ld, packed).  w_kn: W and
+// dW are [K][N] matrices instead of [N][K].
+dp_status run_batched(int op, const void* a, int64_t lda, int64_t bsa, const void* b, int64_t ldb, int64_t bsb,
+                      void* out, int64_t ldo, int64_t bso, int w_kn, int64_t B, int64_t T, int64_t N, int64_t K,
+                      int out_f32, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (op < kOpFwd || op > kOpWgrad) return DP_ERR_INVALID_ARG;
+  if (out_f32 != DP_OUT_BF16 && out_f32 != DP_OUT_F32) return DP_ERR_INVALID_ARG;
+  if ((w_kn != 0 && w_kn != 1) || B < 0 || bsa < 0 || bsb < 0 || bso < 0) return DP_ERR_INVALID_ARG;
+  dp_status st = check_sizes(T, N, K, op);
+  if (st != DP_OK) return st;
+  if (B > 0xFFFFFF) return DP_ERR_UNSUPPORTED;
+  if (B == 0) return DP_OK;
+  int64_t ra, ca, rb, cb, ro, co;
+  op_shapes(op, T, N, K, &ra, &ca, &rb, &cb, &ro, &co);
+  if (w_kn) {  // W (fwd, dgrad) or dW (wgrad) stored [K][N]
+    if (op == kOpWgrad)
+      std::swap(ro, co);
+    else
+      std::swap(rb, cb);
+  }
+  const int out_size = out_f32 ? 4 : 2;
+  if ((st = check_matrix(a, ra, ca, &lda, 2)) != DP_OK) return st;
+  if ((st = check_matrix(b, rb, cb, &ldb, 2)) != DP_OK) return st;
+  if ((st = check_matrix(out, ro, co, &ldo, out_size)) != DP_OK) return st;
+  if (out == nullptr && ro > 0) return DP_ERR_INVALID_ARG;
+  if (bsa == 0) bsa = ra * lda;
+  if (bsb == 0) bsb = rb * ldb;
+  if (bso == 0) bso = ro * ldo;
+  if ((bsa * 2) % 16 != 0 || (bsb * 2) % 16 != 0 || (bso * out_size) % 16 != 0) return DP_ERR_ALIGNMENT;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != DP_OK) return st;
+  if (T == 0) {
+    if (op != kOpWgrad) return DP_OK;
+    for (int64_t i = 0; i < B; ++i)
+      if ((st = zero_output(static_cast<char*>(out) + i * bso * out_size, ro, co, ldo, out_size, stream)) != DP_OK)
+        return st;
+    return DP_OK;
+  }
+  Plan p;
+  if (!plan_for(op, T, N, K, out_f32, dev->sm_count, &p, B, w_kn)) return DP_ERR_INVALID_ARG;
+  if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes)) return DP_ERR_WORKSPACE;
+  if (p.ws_bytes > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
+  if (op == kOpWgrad && p.swap)  // A = X, B = dY
+    return launch_view(p, *dev, b, ldb, a, lda, nullptr, out, ldo, ws, stream, bsb, bsa, bso);
+  return launch_view(p, *dev, a, lda, b, ldb, nullptr, out, ldo, ws, stream, bsa, bsb, bso);
 }
 
 }  // namespace
@@ -559,29 +654,64 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
   Plan p;
   if (!plan_for(static_cast<int>(op), T, N, K, (router || out == DP_OUT_F32) ? 1 : 0, sm_count, &p))
     return DP_ERR_INVALID_ARG;
-  std::memset(info, 0, sizeof(*info));
-  info->block_m = p.bm;
-  info->block_n = p.bn;
-  info->block_k = p.bk;
-  info->stages = p.stages;
-  info->splits = p.splits;
-  info->raster_group = p.group;
-  info->grid = p.grid;
-  info->a_mn_major = p.a_mn ? 1 : 0;
-  info->b_mn_major = p.b_mn ? 1 : 0;
-  info->swap_ab = p.swap ? 1 : 0;
-  info->cta_pair = p.pair ? 1 : 0;
-  info->raster_rows = p.raster_m ? 1 : 0;
-  info->gemm_m = p.gm;
-  info->gemm_n = p.gn;
-  info->gemm_k = p.gk;
-  info->tiles_m = p.tiles_m;
-  info->tiles_n = p.tiles_n;
-  info->k_blocks = p.nkb;
-  info->units = p.units;
-  info->full_units = p.full_units;
-  info->workspace_bytes = T == 0 ? 0 : p.ws_bytes;
-  info->model_us = p.model_ns * 1e-3;
+  fill_info(p, T, info);
+  return DP_OK;
+}
+
+dp_status dp_gemm_fwd_batched(const void* X, int64_t ldx, int64_t bsx, const void* W, int64_t ldw, int64_t bsw,
+                              int weight_kn, void* Y, int64_t ldy, int64_t bsy, int64_t B, int64_t T, int64_t N,
+                              int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                              size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_batched(kOpFwd, X, ldx, bsx, W, ldw, bsw, Y, ldy, bsy, weight_kn, B, T, N, K, static_cast<int>(out),
+                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_gemm_dgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const void* W, int64_t ldw, int64_t bsw,
+                                int weight_kn, void* dX, int64_t ldx, int64_t bsx, int64_t B, int64_t T, int64_t N,
+                                int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                                size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_batched(kOpDgrad, dY, ldg, bsg, W, ldw, bsw, dX, ldx, bsx, weight_kn, B, T, N, K,
+                     static_cast<int>(out), workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_gemm_wgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const void* X, int64_t ldx, int64_t bsx,
+                                void* dW, int64_t ldw, int64_t bsw, int weight_kn, int64_t B, int64_t T, int64_t N,
+                                int64_t K, dp_out_dtype out, int deterministic, void* workspace,
+                                size_t workspace_bytes, dp_stream stream) {
+  (void)deterministic;
+  return run_batched(kOpWgrad, dY, ldg, bsg, X, ldx, bsx, dW, ldw, bsw, weight_kn, B, T, N, K,
+                     static_cast<int>(out), workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                                int weight_kn, int sm_count, dp_plan_info* info) {
+  if (!info || static_cast<int>(op) < 0 || static_cast<int>(op) > kOpWgrad) return DP_ERR_INVALID_ARG;
+  if (B < 1 || (weight_kn != 0 && weight_kn != 1)) return DP_ERR_INVALID_ARG;
+  if (B > 0xFFFFFF) return DP_ERR_UNSUPPORTED;
+  const dp_status st = check_sizes(T, N, K, static_cast<int>(op));
+  if (st != DP_OK) return st;
+  if (sm_count <= 0) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DP_ERR_LAUNCH;
+  }
+  Plan p;
+  if (!plan_for(static_cast<int>(op), T, N, K, out == DP_OUT_F32 ? 1 : 0, sm_count, &p, B, weight_kn))
+    return DP_ERR_INVALID_ARG;
+  fill_info(p, T, info);
+  return DP_OK;
+}
+
+dp_status dp_workspace_size_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                                    int weight_kn, int sm_count, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  dp_plan_info info;
+  const dp_status st = dp_plan_query_batched(op, B, T, N, K, out, weight_kn, sm_count, &info);
+  if (st != DP_OK) return st;
+  *bytes = static_cast<size_t>(info.workspace_bytes);
   return DP_OK;
 }
 

@@ -50,6 +50,9 @@ struct GemmArgs {
   int32_t group;       // raster group width, in tiles of the grouped raster dimension
   int32_t raster_m;    // 1: row tiles fastest inside a group (B column blocks shared)
   int32_t units;       // full_units + (tiles - full_units) * splits
+  int32_t batch;       // independent GEMMs sharing the plan (tiles of batch b follow those of b - 1)
+  int32_t tiles_per_batch;  // tiles_m * tiles_n
+  int64_t out_bstride; // output elements between consecutive batches
   void* out;
   int64_t ldo;         // output leading dimension (elements)
   int32_t out_f32;     // 1: FP32 output, 0: BF16 output
@@ -112,6 +115,7 @@ struct TileCfg {
 // columns (A row-blocks shared); with raster_m, groups of output rows (B
 // column-blocks shared), which the planner picks when B is the larger operand.
 struct Unit {
+  int b;         // batch
   int tm, tn;    // output tile coordinates
   int s;         // split index (0 for whole-K units)
   int ptile;     // index of a split tile among the split tiles (its partials' slot)
@@ -119,8 +123,11 @@ struct Unit {
   bool split;    // partial result: summed by the ordered reduction kernel
 };
 
-// Output tile index -> (row tile, column tile) under the grouped raster.
-__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int* tm, int* tn) {
+// Output tile index -> (batch, row tile, column tile); within a batch the tiles
+// follow the grouped raster.
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int* b, int* tm, int* tn) {
+  *b = tile / a.tiles_per_batch;
+  tile -= *b * a.tiles_per_batch;
   const int fast_tiles = a.raster_m ? a.tiles_m : a.tiles_n;  // dimension grouped, fastest
   const int slow_tiles = a.raster_m ? a.tiles_n : a.tiles_m;
   const int per_group = a.group * slow_tiles;
@@ -154,12 +161,17 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
     r.kb1 = static_cast<int>(static_cast<int64_t>(r.s + 1) * a.nkb / a.splits);
     r.split = a.splits > 1;
   }
-  tile_coords(a, tile, &r.tm, &r.tn);
+  tile_coords(a, tile, &r.b, &r.tm, &r.tn);
   return r;
 }
 
+// Output of batch b.
+__device__ __forceinline__ void* out_at(const GemmArgs& a, int b) {
+  return static_cast<char*>(a.out) + static_cast<int64_t>(b) * a.out_bstride * (a.out_f32 ? 4 : 2);
+}
+
 // Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
-__device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_t col0,
+__device__ __forceinline__ void store_row32(const GemmArgs& a, void* out, int64_t m, int64_t col0,
                                             const float (&v)[32]) {
   if (m >= a.gm) return;
   if (a.out_trans) {
@@ -170,21 +182,21 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, int64_t m, int64_
       if (col0 + j >= a.gn) break;
       const int64_t o = (col0 + j) * a.ldo + m;
       if (a.out_f32)
-        static_cast<float*>(a.out)[o] = v[j];
+        static_cast<float*>(out)[o] = v[j];
       else
-        static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
+        static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
     }
     return;
   }
   if (a.out_f32) {
-    float* dst = static_cast<float*>(a.out) + m * a.ldo + col0;
+    float* dst = static_cast<float*>(out) + m * a.ldo + col0;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (col0 + 4 * j < a.gn)
         *reinterpret_cast<float4*>(dst + 4 * j) =
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   } else {
-    uint16_t* dst = static_cast<uint16_t*>(a.out) + m * a.ldo + col0;
+    uint16_t* dst = static_cast<uint16_t*>(out) + m * a.ldo + col0;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       if (col0 + 8 * j < a.gn) {
@@ -224,12 +236,13 @@ __device__ __forceinline__ void stage_block32(const GemmArgs& a, uint32_t buf, i
   __syncwarp();
 }
 
-__device__ __forceinline__ void flush_block32(const GemmArgs& a, uint32_t buf, int lane, int64_t m0, int64_t col0) {
+__device__ __forceinline__ void flush_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
+                                              int64_t col0) {
   const int64_t rows_left = a.gm - m0;
   if (a.out_f32) {
     const int ch = lane & 7, r0 = lane >> 3;
     const bool col_ok = col0 + 4 * ch < a.gn;
-    float* p = static_cast<float*>(a.out) + (m0 + r0) * a.ldo + col0 + 4 * ch;
+    float* p = static_cast<float*>(out) + (m0 + r0) * a.ldo + col0 + 4 * ch;
     const int64_t step = 4 * a.ldo;
 #pragma unroll
     for (int i = 0; i < 8; ++i, p += step) {
@@ -240,7 +253,7 @@ __device__ __forceinline__ void flush_block32(const GemmArgs& a, uint32_t buf, i
   } else {
     const int ch = lane & 3, r0 = lane >> 2;
     const bool col_ok = col0 + 8 * ch < a.gn;
-    uint16_t* p = static_cast<uint16_t*>(a.out) + (m0 + r0) * a.ldo + col0 + 8 * ch;
+    uint16_t* p = static_cast<uint16_t*>(out) + (m0 + r0) * a.ldo + col0 + 8 * ch;
     const int64_t step = 8 * a.ldo;
 #pragma unroll
     for (int i = 0; i < 4; ++i, p += step) {
@@ -251,14 +264,14 @@ __device__ __forceinline__ void flush_block32(const GemmArgs& a, uint32_t buf, i
   }
 }
 
-__device__ __forceinline__ void store_block32(const GemmArgs& a, uint32_t buf, int lane, int64_t m0, int64_t col0,
-                                              const float (&v)[32]) {
+__device__ __forceinline__ void store_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
+                                              int64_t col0, const float (&v)[32]) {
   if (a.out_trans) {
-    store_row32(a, m0 + lane, col0, v);
+    store_row32(a, out, m0 + lane, col0, v);
     return;
   }
   stage_block32(a, buf, lane, v);
-  flush_block32(a, buf, lane, m0, col0);
+  flush_block32(a, out, buf, lane, m0, col0);
 }
 
 // In-kernel ordered sum for cluster plans: the S CTAs of a cluster computed the S
@@ -279,6 +292,7 @@ __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthread
   const int64_t m_tile = static_cast<int64_t>(w.tm) * kBlockM, n0 = static_cast<int64_t>(w.tn) * BN;
   const size_t pstride = static_cast<size_t>(kBlockM) * BN / 4;
   const float4* p0 = a.partials + static_cast<size_t>(w.ptile) * S * pstride;
+  void* out = out_at(a, w.b);
   const int total = rows * (BN / 4);
   for (int e = static_cast<int>(threadIdx.x); e < total; e += nthreads) {
     const int j4 = e / rows, row = r0 + (e - j4 * rows);
@@ -308,14 +322,14 @@ __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthread
       for (int t = 0; t < 4; ++t) {
         const int64_t o = (col + t) * a.ldo + m;
         if (a.out_f32)
-          static_cast<float*>(a.out)[o] = v[t];
+          static_cast<float*>(out)[o] = v[t];
         else
-          static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(v[t], 0.0f) & 0xFFFFu);
+          static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(v[t], 0.0f) & 0xFFFFu);
       }
     } else if (a.out_f32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + m * a.ldo + col) = acc;
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + m * a.ldo + col) = acc;
     } else {
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + m * a.ldo + col) =
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * a.ldo + col) =
           make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     }
   }
@@ -559,11 +573,18 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           // a pair's loads all complete on the leader's full barrier
           const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
           if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES);
+          // (batched plans: every map has a trailing batch dimension)
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            if (PAIR)
+            if (args.batch > 1) {
+              if (PAIR)
+                tma_load_3d_pair(dst, map, fb, x, y, w.b);
+              else
+                tma_load_3d(dst, map, fb, x, y, w.b);
+            } else if (PAIR) {
               tma_load_2d_pair(dst, map, fb, x, y);
-            else
+            } else {
               tma_load_2d(dst, map, fb, x, y);
+            }
           };
           auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z) {
             if (PAIR)
@@ -817,6 +838,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(tm) * C::TM + static_cast<int64_t>(rank) * C::BM + row;
       const int64_t m0 = m - lane;  // row of lane 0
+      void* outb = out_at(args, w.b);
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
       if (!w.split) {
@@ -829,7 +851,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_block32(args, ebuf, lane, m0, n0 + c * 32, v);
+          store_block32(args, outb, ebuf, lane, m0, n0 + c * 32, v);
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's

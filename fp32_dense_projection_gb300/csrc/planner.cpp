@@ -43,15 +43,18 @@ struct View {
   int a_elem, b_elem;  // bytes per element as streamed by the GEMM (bf16 = 2, fp32 = 4)
   int terms = 1;       // MMAs per contraction element (3 for the router's BF16x3)
   int bk = kBlockK;    // contraction block (32 for the router's fused split)
+  int64_t batch = 1;   // independent GEMMs of this view
 };
 
-bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v) {
+// w_kn: the weight (and the weight gradient) stored [K][N] instead of [N][K] (the
+// batched entry points' weight layout); it flips the majorness of W's view.
+bool make_view(int op, int64_t T, int64_t N, int64_t K, View* v, bool w_kn = false) {
   switch (op) {
-    case kOpFwd:  // Y[T,N] = X[T,K] W[N,K]^T : A = X (K-major), B = W (K-major)
-      *v = {T, N, K, false, false, 2, 2};
+    case kOpFwd:  // Y[T,N] = X[T,K] W[N,K]^T : A = X (K-major), B = W (K-major; MN-major if W is [K][N])
+      *v = {T, N, K, false, w_kn, 2, 2};
       return true;
-    case kOpDgrad:  // dX[T,K] = dY[T,N] W[N,K] : A = dY (K-major), B = W (MN-major)
-      *v = {T, K, N, false, true, 2, 2};
+    case kOpDgrad:  // dX[T,K] = dY[T,N] W[N,K] : A = dY (K-major), B = W (MN-major; K-major if W is [K][N])
+      *v = {T, K, N, false, !w_kn, 2, 2};
       return true;
     case kOpWgrad:  // dW[N,K] = dY[T,N]^T X[T,K] : A = dY (MN-major), B = X (MN-major)
       *v = {N, K, T, true, true, 2, 2};
@@ -111,7 +114,7 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
 // reduction kernel that sums the partials.
 double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes) {
   const int64_t slots = t.pair ? sm / 2 : sm;
-  const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
+  const int64_t tiles = v.batch * ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
   const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, v.bk));
   const int64_t split_units = (tiles - full) * splits;
   const int64_t units = full + split_units;
@@ -119,7 +122,7 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
   const double a_rows = static_cast<double>(std::min<int64_t>(t.rows(), v.gm));
   const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn));
   const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
-  const double unique = static_cast<double>(v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
+  const double unique = static_cast<double>(v.batch) * (v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
   const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
   double time = 0.0;
   if (full > 0)
@@ -127,7 +130,7 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
   if (split_units > 0)  // full is 0 or a whole number of waves when any tile is split
     time += static_cast<double>(ceil_div(split_units, slots)) *
             unit_ns(v, t, ceil_div(nkb, splits), splits > 1, active_sms, reuse, out_bytes);
-  const double t_dram = (unique + static_cast<double>(v.gm) * v.gn * out_bytes) / kHbmBytesPerNs;
+  const double t_dram = (unique + static_cast<double>(v.batch) * v.gm * v.gn * out_bytes) / kHbmBytesPerNs;
   time = std::max(time, t_dram);
   if (splits > 1 && split_units > 0) {  // every split tile's partials, summed in split order
     // by the GEMM's own clusters (single-CTA tiles, every tile split, one unit per
@@ -170,7 +173,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       if (o.bn > 0 && bn != o.bn) continue;
       if (o.bn <= 0 && bn > 64 && v.gn <= bn / 2) continue;  // tile would be mostly empty
       const Tiling t = {bn, pair != 0};
-      const int64_t tiles = ceil_div(v.gm, t.rows()) * ceil_div(v.gn, bn);
+      const int64_t tiles = v.batch * ceil_div(v.gm, t.rows()) * ceil_div(v.gn, bn);
       const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // partial slots: one per CTA tile
       // bounded accumulation length, unless the tiles are too many to split at all
       // (then whole K per tile: a longer running sum, the only case without the bound)
@@ -200,11 +203,16 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
 
 }  // namespace
 
-bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, const Overrides& o) {
-  if (!p || sm < 1 || T < 0 || N < 1 || K < 1) return false;
+bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, const Overrides& o,
+               int64_t batch, bool w_kn) {
+  if (!p || sm < 1 || T < 0 || N < 1 || K < 1 || batch < 1) return false;
+  if ((batch > 1 || w_kn) && op >= kOpRouterFwd) return false;  // batched forms: BF16 ops only
   View v;
-  if (!make_view(op, T, N, K, &v)) return false;
+  if (!make_view(op, T, N, K, &v, w_kn)) return false;
+  v.batch = batch;
   Plan plan;
+  plan.batch = batch;
+  plan.w_kn = w_kn;
   plan.op = op;
   plan.T = T;
   plan.N = N;
@@ -225,7 +233,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
     if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, o, &c);
     if (op == kOpWgrad && o.swap != 0) {
       // thin outputs: let K fill the 128-row tile side and N be the MMA's N
-      const View sv = {K, N, T, true, true, 2, 2};
+      View sv = {K, N, T, true, true, 2, 2};
+      sv.batch = batch;
       Choice cs;
       search(sv, plan.nkb, sm, out_bytes, o, &cs);
       if (cs.have && (!c.have || cs.t < c.t * 0.97 || o.swap == 1)) {
@@ -247,7 +256,8 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.stages = v.terms > 1 ? stages_x3(plan.bn, plan.pair) : stages_for(plan.bn, plan.pair);
   plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
-  const int64_t tiles = plan.tiles_m * plan.tiles_n;
+  plan.tiles = batch * plan.tiles_m * plan.tiles_n;
+  const int64_t tiles = plan.tiles;
   plan.full_units = (v.gm > 0 && plan.nkb > 0) ? c.full : tiles;
   plan.units = plan.full_units + (tiles - plan.full_units) * plan.splits;
   // Group along the dimension whose operand is larger, so the tiles that share
@@ -290,6 +300,9 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
     }
   }
   plan.ws_bytes = (plan.splits > 1 || (router && T > 0)) ? round_up(off, 256) : 0;
+  // D[m][n] goes out transposed for the swapped weight gradient, unless the weight
+  // gradient is itself stored [K][N] (then the unswapped one is transposed instead)
+  plan.out_trans = (op == kOpWgrad || op == kOpRouterWgrad) && (plan.swap != w_kn);
   *p = plan;
   return true;
 }

@@ -47,9 +47,13 @@ struct Plan {
   bool swap = false;
   bool raster_m = false;  // raster groups of row tiles, rows fastest (B is the larger operand)
   bool pair = false;      // tiles of 256 rows computed by a cluster of two CTAs (bm = 256)
+  bool out_trans = false; // D[m][n] stored at out[n][m]
+  int64_t batch = 1;      // independent GEMMs; tiles of batch b follow those of batch b - 1
+  bool w_kn = false;      // W / dW stored [K][N]
   // tiling
   int bm = kBlockM, bn = 256, bk = kBlockK, stages = 4, splits = 1, group = 16, grid = 0;
   int64_t tiles_m = 0, tiles_n = 0, nkb = 0, units = 0;
+  int64_t tiles = 0;      // batch * tiles_m * tiles_n
   // units [0, full_units) are whole-K tiles; the remaining tiles are split
   // `splits` ways (all tiles when full_units = 0, the last partial wave otherwise)
   int64_t full_units = 0;
@@ -106,7 +110,9 @@ struct Overrides {
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,
 // sm_count < 1, unknown op, or overrides that admit no plan).
+// batch > 1: `batch` independent GEMMs of this shape in one launch (BF16 ops);
+// w_kn: W (and dW) stored [K][N] rather than [N][K].
 bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm_count, Plan* plan,
-               const Overrides& overrides = Overrides());
+               const Overrides& overrides = Overrides(), int64_t batch = 1, bool w_kn = false);
 
 }  // namespace dp

@@ -46,8 +46,9 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
   const int chunk = slice % ra.chunks;
   const int slot = slice / ra.chunks;
   const int ptile = slot / ra.slots_per_tile, rank = slot - ptile * ra.slots_per_tile;
-  int tm, tn;
-  tile_coords(a, a.full_units + ptile, &tm, &tn);
+  int bt, tm, tn;
+  tile_coords(a, a.full_units + ptile, &bt, &tm, &tn);
+  void* out = out_at(a, bt);
   const int row = t & (kBlockM - 1), j = t >> 7;  // row of the slot, float4 column in the chunk
   const int64_t m = static_cast<int64_t>(tm) * ra.tile_rows + rank * kBlockM + row;
   const int64_t col = static_cast<int64_t>(tn) * ra.bn + chunk * 32 + 4 * j;
@@ -81,14 +82,14 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
     for (int q = 0; q < 4; ++q) {
       const int64_t o = (col + q) * a.ldo + m;
       if (a.out_f32)
-        static_cast<float*>(a.out)[o] = e[q];
+        static_cast<float*>(out)[o] = e[q];
       else
-        static_cast<uint16_t*>(a.out)[o] = static_cast<uint16_t>(pack_bf16x2(e[q], 0.0f) & 0xFFFFu);
+        static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(e[q], 0.0f) & 0xFFFFu);
     }
   } else if (a.out_f32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + m * a.ldo + col) = acc;
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + m * a.ldo + col) = acc;
   } else {
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + m * a.ldo + col) =
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * a.ldo + col) =
         make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
 }

@@ -161,6 +161,32 @@ dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int6
                                 int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
                                 dp_stream stream);
 
+/* ------------------------------------------------------------ batched BF16 ops */
+/* Batched projection GEMMs: B independent problems of one shape in one launch,
+ * as the pages' integration runs its per-head projections ("one batched BF16 GEMM
+ * over strided views, forward and both gradients", with a weight layout option).
+ * Problem b reads X_b = X + b*bsx (and so on for every operand and output, in
+ * elements; a batch stride of 0 means packed, rows * ld).  Batch strides may be
+ * smaller than a row (per-head slices of a [T][H][D] tensor: ld = H*D, bs = D);
+ * they must keep 16-byte alignment.  weight_kn = 0: W_b and dW_b are [N][K]
+ * matrices as in the single-problem calls; 1: they are [K][N].  One plan covers
+ * the B * tiles_m * tiles_n tiles in one persistent launch (its tile shape and
+ * splits are chosen for the whole batch, so they can differ from a single
+ * problem's); every problem's tiles use the same fixed contraction partition and
+ * summation order, so the outputs are deterministic. */
+dp_status dp_gemm_fwd_batched(const void* X, int64_t ldx, int64_t bsx, const void* W, int64_t ldw, int64_t bsw,
+                              int weight_kn, void* Y, int64_t ldy, int64_t bsy,
+                              int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                              void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status dp_gemm_dgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const void* W, int64_t ldw, int64_t bsw,
+                                int weight_kn, void* dX, int64_t ldx, int64_t bsx,
+                                int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                                void* workspace, size_t workspace_bytes, dp_stream stream);
+dp_status dp_gemm_wgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const void* X, int64_t ldx, int64_t bsx,
+                                void* dW, int64_t ldw, int64_t bsw, int weight_kn,
+                                int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                                void* workspace, size_t workspace_bytes, dp_stream stream);
+
 /* ----------------------------------------------------------------- router ops */
 /* [router]: FP32 operands and FP32 output; N is the expert count (256 on the
  * pages) and K the hidden size.  Each FP32 operand value x is split into bf16
@@ -235,16 +261,25 @@ typedef struct dp_plan_info {
     int64_t full_units;       /* leading whole-K units; the remaining tiles are split */
     uint64_t workspace_bytes; /* == dp_workspace_size() */
     double model_us;          /* the planner's modelled duration of the call (diagnostic) */
+    int64_t batch;            /* independent problems in the launch (1 except batched calls) */
+    int64_t tiles;            /* batch * tiles_m * tiles_n */
+    int32_t weight_kn;        /* batched calls: W / dW stored [K][N] */
+    int32_t reserved2;
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs
  * (sm_count <= 0: query the current device).  Pure host function. */
 dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                         int sm_count, dp_plan_info* info);
+/* The same for a batched BF16 call (op DP_OP_FWD / DGRAD / WGRAD, B >= 1). */
+dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                                int weight_kn, int sm_count, dp_plan_info* info);
 
 /* Workspace bytes a call needs (see dp_plan_query for sm_count). */
 dp_status dp_workspace_size(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                             int sm_count, size_t* bytes);
+dp_status dp_workspace_size_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
+                                    int weight_kn, int sm_count, size_t* bytes);
 
 /* Check the device's architecture and set kernel attributes on `device`
  * (the current device if < 0).  Optional: the first call on a device does it. */

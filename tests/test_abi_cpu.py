@@ -230,3 +230,40 @@ def test_accumulation_length_is_bounded(op, T):
         per_split = -(-p["k_blocks"] // p["splits"]) * p["block_k"]
         if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else whole K (bounded workspace)
             assert per_split * terms <= 16384 + p["block_k"] * terms, (op, T, N, K, p)
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("kn", [False, True])
+@pytest.mark.parametrize("B,T,N,K", [(1, 1000, 128, 512), (16, 2048, 128, 512), (128, 64, 512, 128), (4, 65537, 64, 256)])
+def test_batched_plan_is_valid(op, kn, B, T, N, K):
+    p = dp.plan_batched(op, B, T, N, K, weight_kn=kn, sm_count=SM)
+    tiles = B * p["tiles_m"] * p["tiles_n"]
+    assert p["batch"] == B and p["tiles"] == tiles and p["weight_kn"] == int(kn)
+    assert p["units"] == p["full_units"] + (tiles - p["full_units"]) * p["splits"]
+    assert 1 <= p["grid"] <= SM
+    # [K][N] weights flip the majorness of W's view; the weight gradient's view does not change
+    if op == "fwd":
+        assert (p["a_mn_major"], p["b_mn_major"]) == (0, int(kn))
+    elif op == "dgrad":
+        assert (p["a_mn_major"], p["b_mn_major"]) == (0, int(not kn))
+    else:
+        assert (p["a_mn_major"], p["b_mn_major"]) == (1, 1)
+    if B == 1:  # one problem: the plan of the single-problem call (for the [N][K] layout)
+        single = dp.plan(op, T, N, K, sm_count=SM)
+        if not kn:
+            assert p == single
+    assert dp.workspace_size_batched(op, B, T, N, K, weight_kn=kn, sm_count=SM) == p["workspace_bytes"]
+
+
+def test_batched_argument_checks(L):
+    P = ctypes.c_void_p
+    good = P(1 << 20)
+    # bad weight layout flag
+    assert L.dp_gemm_fwd_batched(good, 0, 0, good, 0, 0, 2, good, 0, 0, 4, 64, 64, 64, 0, 1, None, 0, None) == 1
+    # batch stride breaking the 16-byte alignment (bf16: a multiple of 8 elements)
+    assert L.dp_gemm_fwd_batched(good, 0, 12, good, 0, 0, 0, good, 0, 0, 4, 64, 64, 64, 0, 1, None, 0, None) == 2
+    # negative batch count
+    assert L.dp_gemm_wgrad_batched(good, 0, 0, good, 0, 0, good, 0, 0, 0, -1, 64, 64, 64, 0, 1, None, 0, None) == 1
+    # router ops have no batched form
+    info = dp.PlanInfo()
+    assert L.dp_plan_query_batched(3, 2, 64, 64, 64, 0, 0, SM, ctypes.byref(info)) == 1

@@ -383,7 +383,13 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   l.grid = p.grid;
   l.pair = p.pair;
   l.x3 = x3;
-  l.pdl = p.op >= kOpRouterFwd;  // right behind the kernel that split the router's operands
+  // Every GEMM launches as a programmatic dependent of the kernel before it on the
+  // stream: its setup (barriers, TMEM, descriptor prefetch) overlaps that kernel's
+  // tail, and its producer waits (griddepcontrol.wait) before its first load, so
+  // every global access of the GEMM follows the predecessor's completion.  (The
+  // router's FP32 staging loads start before that wait: their predecessor is the
+  // same call's split kernel, which writes only the workspace.)
+  l.pdl = true;
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);

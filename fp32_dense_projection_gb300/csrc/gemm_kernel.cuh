@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           }
         }
       }
-      if (!X3) pdl_wait();  // (the router's input gradient reads the split kernel's operands)
+      if (!X3) pdl_wait();  // the previous kernel on the stream (launched as its dependent) is done
       for (int u = unit0; !X3 && ok && u < args.units; u += unit_step) {
         const Unit w = decode_unit(args, u);
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
@@ -899,7 +899,7 @@ struct GemmLaunch {
   int grid;   // CTAs (twice the number of pairs for a paired plan)
   bool pair;  // clusters of two CTAs share each tile
   bool x3;    // router BF16x3 mode: FP32 A split in the kernel, B from pre-split planes
-  bool pdl;   // launched as a programmatic dependent of the operand-split kernel
+  bool pdl;   // launched as a programmatic dependent of the previous kernel on the stream
 };
 
 // Clusters of `cluster` single-CTA tiles of width bn that run at once (0 if none).

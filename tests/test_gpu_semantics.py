@@ -223,3 +223,31 @@ def test_cluster_sum_matches_reduction_kernel(monkeypatch, op, T, N, K):
     assert_budget(as_f64(in_cluster), ref, "bf16" if bits == torch.int16 else "f32", f"{op} T={T} in-cluster sum")
     no_device_fault()
 
+
+
+def test_dependent_calls_keep_their_order():
+    # Consecutive GEMMs overlap only their setup with the previous kernel: a call that
+    # reads the previous call's output, and a call that overwrites a buffer the
+    # previous call reads, give the same bits as the same calls with a full
+    # device synchronisation between them.
+    T, N, K = 4100, 1024, 2048
+    c = {k: v.to(DEV) for k, v in case_tensors("fwd", T, N, K, seed=4).items()}
+    X, W, dY = c["X"], c["W"], c["dY"]
+
+    def chain(sync):
+        x = X.clone()
+        y = dp.dp_gemm_fwd(x, W)                        # reads x
+        if sync:
+            torch.cuda.synchronize()
+        dx = dp.dp_gemm_dgrad(y, W, out=x)              # reads y (written just before), overwrites x
+        if sync:
+            torch.cuda.synchronize()
+        dw = dp.dp_gemm_wgrad(y, dx, out_dtype=torch.float32)  # reads both
+        torch.cuda.synchronize()
+        return y, dx, dw
+
+    a, b = chain(False), chain(True)
+    for u, v in zip(a, b):
+        bits = torch.int16 if u.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(u.view(bits), v.view(bits))
+    no_device_fault()

@@ -26,10 +26,12 @@ constexpr double kL2BytesPerNsPerSm = 160.0;  // operand bytes an SM pulls when 
 constexpr double kHbmBytesPerNs = 5500.0;     // whole-GPU DRAM streaming rate
 constexpr double kSmDramBytesPerNs = 45.0;    // most DRAM bandwidth one SM's TMA stream sustains
 constexpr double kReduceNs = 2000.0;          // the split reduction kernel's launch and one L2 round trip
-constexpr double kClusterSumNs = 700.0;       // in-cluster sum (one unit per CTA, clusters of <= 4 run at once)
+constexpr double kClusterSumNs = 1500.0;      // in-cluster sum (one unit per CTA, clusters of <= 4 run at once)
 constexpr int kClusterSumMax = 4;             // largest cluster the device is assumed to co-schedule for it
 constexpr double kReduceBytesPerNs = 4000.0;  // partial bytes it sums per ns (whole GPU, L2-resident)
 constexpr double kPairGain = 0.93;            // a CTA pair reads half of B per SM: less shared-memory traffic
+constexpr double kNarrowB = 1.35;             // tiles whose B slice per CTA is 64 columns (128 x 64, or a pair's
+                                              // 256 x 128) run their main loop this much slower than the rates say
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
@@ -97,12 +99,13 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn)) / (t.pair ? 2.0 : 1.0);
   const double bytes_per_kb = (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
   const double flop_per_kb = 2.0 * kBlockM * t.bn * v.bk * v.terms;  // per SM, tensor-pipe work
-  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0);
+  const double narrow = (t.pair ? t.bn / 2 : t.bn) == 64 ? kNarrowB : 1.0;
+  const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0) * narrow;
   // BF16x3: the converter warps split every A element of the block
   const double t_split = v.terms > 1 ? kb * std::max(kBlockM * v.bk / kX3SplitPerNs, kX3BlockNs) : 0.0;
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
-  const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
+  const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) * narrow / kL2BytesPerNsPerSm);
   const double t_load = kb * bytes_per_kb / bw;
   const double out_tile = a_rows * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * (split ? 4.0 : out_bytes);
   return std::max(std::max(t_mma, t_load), t_split) + out_tile / dram;

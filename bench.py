@@ -617,17 +617,35 @@ def run_suite(args, local):
                 dX = torch.empty(T, K, dtype=torch.bfloat16, device=device)
                 dW = torch.empty(N, K, dtype=torch.bfloat16, device=device)
 
+                def bwd(X=X, W=W, dY=dY, dX=dX, dW=dW):
+                    # input and weight gradient: one co-scheduled launch or two calls, as planned
+                    dp.dp_gemm_bwd(dY, X, W, dX=dX, dW=dW, workspace=ws)
+
+                def bwd_two_calls(X=X, W=W, dY=dY, dX=dX, dW=dW):
+                    dp.dp_gemm_dgrad(dY, W, out=dX, workspace=ws)
+                    dp.dp_gemm_wgrad(dY, X, out=dW, workspace=ws)
+
                 def step(X=X, W=W, dY=dY, Y=Y, dX=dX, dW=dW):
                     dp.dp_gemm_fwd(X, W, out=Y, workspace=ws)
                     dp.dp_gemm_fwd(X, W, out=Y, workspace=ws)
-                    dp.dp_gemm_dgrad(dY, W, out=dX, workspace=ws)
-                    dp.dp_gemm_wgrad(dY, X, out=dW, workspace=ws)
-                nb = 2 * (2 * T * K + 2 * N * K + 2 * T * N) + (2 * T * N + 2 * N * K + 2 * T * K) * 2
-                report("cfg5", f"2fwd+bwd T={T} {K}->{N} bf16", 4 * 2 * T * N * K, 4 * 2 * T * N * K, nb, step)
+                    dp.dp_gemm_bwd(dY, X, W, dX=dX, dW=dW, workspace=ws)
+                nb_b = (2 * T * N + 2 * N * K + 2 * T * K) * 2
+                nb = 2 * (2 * T * K + 2 * N * K + 2 * T * N) + nb_b
+                pb = dp.plan_bwd(T, N, K)
+                form = {"co_scheduled": pb["fused"], "wgrad_first": pb["wgrad_first"],
+                        "tile": [pb["dgrad"]["block_m"], pb["dgrad"]["block_n"]]}
+                report("cfg5", f"bwd T={T} {K}->{N} bf16", 2 * 2 * T * N * K, 2 * 2 * T * N * K, nb_b, bwd, form)
+                report("cfg5", f"bwd T={T} {K}->{N} bf16 two calls", 2 * 2 * T * N * K, 2 * 2 * T * N * K, nb_b,
+                       bwd_two_calls)
+                report("cfg5", f"2fwd+bwd T={T} {K}->{N} bf16", 4 * 2 * T * N * K, 4 * 2 * T * N * K, nb, step, form)
                 del X, W, dY, Y, dX, dW
             K, N = 4096, 256
             X, W, dY = f32(T, K), f32(N, K, scale=0.02), f32(T, N)
             Y, dX, dW = torch.empty(T, N, device=device), torch.empty(T, K, device=device), torch.empty(N, K, device=device)
+
+            def rbwd(X=X, W=W, dY=dY, dX=dX, dW=dW):
+                dp.router_dgrad(dY, W, out=dX, workspace=ws)
+                dp.router_wgrad(dY, X, out=dW, workspace=ws)
 
             def rstep(X=X, W=W, dY=dY, Y=Y, dX=dX, dW=dW):
                 dp.router_fwd(X, W, out=Y, workspace=ws)
@@ -635,6 +653,8 @@ def run_suite(args, local):
                 dp.router_dgrad(dY, W, out=dX, workspace=ws)
                 dp.router_wgrad(dY, X, out=dW, workspace=ws)
             nb = 4 * (2 * (T * K + N * K + T * N) + 2 * (T * N + N * K + T * K))
+            report("cfg5", f"router bwd T={T} {K}->{N} f32", 2 * 2 * T * N * K, 3 * 2 * 2 * T * N * K,
+                   4 * 2 * (T * N + N * K + T * K), rbwd)
             report("cfg5", f"router 2fwd+bwd T={T} {K}->{N} f32", 4 * 2 * T * N * K, 3 * 4 * 2 * T * N * K, nb, rstep)
             del X, W, dY, Y, dX, dW
     if "batched" in which:  # per-head projections, 128 heads, T = 4096: one batched launch vs 128 calls

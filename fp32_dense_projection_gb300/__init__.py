@@ -9,6 +9,8 @@ first call raises.
   dp_gemm_fwd(X, W)        Y  = X W^T       X[T,K], W[N,K]  (bf16)  -> Y[T,N]
   dp_gemm_dgrad(dY, W)     dX = dY W        dY[T,N], W[N,K] (bf16)  -> dX[T,K]
   dp_gemm_wgrad(dY, X)     dW = dY^T X      dY[T,N], X[T,K] (bf16)  -> dW[N,K]
+  dp_gemm_bwd(dY, X, W)    (dX, dW) of one layer: two single-op calls, or one
+                           co-scheduled launch over both problems' tiles
   router_fwd / router_dgrad / router_wgrad: the same on FP32 operands through
   BF16x3 emulation, FP32 output.
 
@@ -51,6 +53,12 @@ class PlanInfo(ctypes.Structure):
         ("reserved2", ctypes.c_int32)]
 
 
+class BwdPlanInfo(ctypes.Structure):
+    _fields_ = [("fused", ctypes.c_int32), ("wgrad_first", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("model_us", ctypes.c_double), ("separate_us", ctypes.c_double),
+                ("workspace_bytes", ctypes.c_uint64), ("dgrad", PlanInfo), ("wgrad", PlanInfo)]
+
+
 def lib():
     """Load libdp_gb300.so (raises if it has not been built)."""
     global _lib
@@ -80,6 +88,9 @@ def lib():
         L.dp_gemm_dgrad_batched.argtypes = [P, I, I, P, I, I, S, P, I, I] + btail
         L.dp_gemm_wgrad_batched.argtypes = [P, I, I, P, I, I, P, I, I, S] + btail
         L.dp_workspace_size.argtypes = [S, I, I, I, S, S, ctypes.POINTER(ctypes.c_size_t)]
+        L.dp_gemm_bwd.argtypes = [P, I, P, I, P, I, P, I, S, P, I, S, I, I, I, S, P, Z, P]
+        L.dp_plan_query_bwd.argtypes = [I, I, I, S, S, S, ctypes.POINTER(BwdPlanInfo)]
+        L.dp_workspace_size_bwd.argtypes = [I, I, I, S, S, S, ctypes.POINTER(ctypes.c_size_t)]
         L.dp_init.argtypes = [S]
         L.dp_device_error.argtypes = [S]
         L.dp_status_string.argtypes = [S]
@@ -134,6 +145,29 @@ def workspace_size(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: 
     n = ctypes.c_size_t(0)
     _check(lib().dp_workspace_size(int(op), T, N, K, int(bool(out_f32)), int(sm_count), ctypes.byref(n)),
            "dp_workspace_size")
+    return int(n.value)
+
+
+def _info_dict(info: PlanInfo) -> dict:
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if not name.startswith("reserved")}
+
+
+def plan_bwd(T: int, N: int, K: int, dx_f32: bool = False, dw_f32: bool = False, sm_count: int = 0) -> dict:
+    """The backward pass's plan: {"fused", "wgrad_first", "grid", "model_us", "separate_us",
+    "workspace_bytes", "dgrad": {...}, "wgrad": {...}}."""
+    info = BwdPlanInfo()
+    _check(lib().dp_plan_query_bwd(T, N, K, int(bool(dx_f32)), int(bool(dw_f32)), int(sm_count),
+                                   ctypes.byref(info)), "dp_plan_query_bwd")
+    out = {name: getattr(info, name) for name, _ in BwdPlanInfo._fields_[:7] if name != "reserved"}
+    out["dgrad"], out["wgrad"] = _info_dict(info.dgrad), _info_dict(info.wgrad)
+    return out
+
+
+def workspace_size_bwd(T: int, N: int, K: int, dx_f32: bool = False, dw_f32: bool = False,
+                       sm_count: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().dp_workspace_size_bwd(T, N, K, int(bool(dx_f32)), int(bool(dw_f32)), int(sm_count),
+                                       ctypes.byref(n)), "dp_workspace_size_bwd")
     return int(n.value)
 
 
@@ -267,6 +301,46 @@ def dp_gemm_wgrad(dY, X, out=None, out_dtype=torch.bfloat16, deterministic=True,
         raise ValueError("dp_gemm_wgrad: X must be T x K")
     return _gemm(OP_WGRAD, "dp_gemm_wgrad", dY, X, (N, K), out, out_dtype, deterministic, workspace, stream,
                  T, N, K)
+
+
+def dp_gemm_bwd(dY, X, W, dX=None, dW=None, dx_dtype=torch.bfloat16, dw_dtype=torch.bfloat16,
+                deterministic=True, workspace=None, stream=None):
+    """(dX[T,K] = dY W, dW[N,K] = dY^T X) of one layer in one call: the two single-op
+    calls, or one co-scheduled launch over both problems' whole-K tiles."""
+    T, N = dY.shape
+    K = X.shape[1]
+    if X.shape[0] != T or tuple(W.shape) != (N, K):
+        raise ValueError("dp_gemm_bwd: dY must be T x N, X T x K and W N x K")
+    for t, nm in ((dY, "dY"), (X, "X"), (W, "W")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"dp_gemm_bwd: {nm} must be a CUDA bfloat16 tensor")
+    device = dY.device
+    if dX is None:
+        dX = torch.empty((T, K), dtype=dx_dtype, device=device)
+    elif tuple(dX.shape) != (T, K) or dX.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dp_gemm_bwd: dX must be T x K, bf16 or fp32")
+    if dW is None:
+        dW = torch.empty((N, K), dtype=dw_dtype, device=device)
+    elif tuple(dW.shape) != (N, K) or dW.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("dp_gemm_bwd: dW must be N x K, bf16 or fp32")
+    dx32, dw32 = dX.dtype == torch.float32, dW.dtype == torch.float32
+    if workspace is None:
+        workspace = _default_workspace(device).get(workspace_size_bwd(T, N, K, dx32, dw32))
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+
+    def call():
+        return lib().dp_gemm_bwd(_ptr(dY), _ld(dY), _ptr(X), _ld(X), _ptr(W), _ld(W), _ptr(dX), _ld(dX),
+                                 DP_OUT_F32 if dx32 else DP_OUT_BF16, _ptr(dW), _ld(dW),
+                                 DP_OUT_F32 if dw32 else DP_OUT_BF16, T, N, K, int(bool(deterministic)),
+                                 _ptr(workspace), nbytes, _stream(device, stream))
+
+    if device.index == torch.cuda.current_device():
+        status = call()
+    else:
+        with torch.cuda.device(device):
+            status = call()
+    _check(status, "dp_gemm_bwd")
+    return dX, dW
 
 
 def router_fwd(X, W, out=None, deterministic=True, workspace=None, stream=None):

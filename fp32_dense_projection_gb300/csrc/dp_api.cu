@@ -57,6 +57,7 @@ dp_status init_device(int dev, DeviceState** out) {
       cudaError_t e = set_attributes_kk();
       if (e == cudaSuccess) e = set_attributes_km();
       if (e == cudaSuccess) e = set_attributes_mm();
+      if (e == cudaSuccess) e = set_attributes_bwd();
       if (e == cudaSuccess) e = set_attributes_split();
       if (e == cudaSuccess) e = set_attributes_reduce();
       if (e == cudaSuccess) e = cudaGetSymbolAddress(&fault, g_fault_word);
@@ -322,12 +323,13 @@ int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
 // Router BF16x3 plans (x3): A is FP32, B and B_lo are B's bf16 hi and lo planes.
 // Batched plans: bsa / bsb / bso are the elements between consecutive batches of
 // A, B and the output.
-dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
-                      int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, cudaStream_t stream,
-                      int64_t bsa = 0, int64_t bsb = 0, int64_t bso = 0) {
+// prepare_view fills a launch (tensor maps and kernel arguments) without enqueueing it.
+dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, int64_t bsa, int64_t bsb,
+                       int64_t bso, GemmLaunch* launch) {
   if (p.units > 0x7FFFFFFF || p.tiles > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF || p.batch > 0xFFFFFF)
     return DP_ERR_UNSUPPORTED;
-  GemmLaunch l;
+  GemmLaunch& l = *launch;
   std::memset(&l, 0, sizeof(l));
   const bool x3 = p.op == kOpRouterFwd || p.op == kOpRouterWgrad;
   // Boxes: K-major operands one box of bk contraction columns x tile rows; MN-major
@@ -376,6 +378,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   a.out_trans = p.out_trans ? 1 : 0;
   a.a3d = a3d ? 1 : 0;
   a.b3d = b3d ? 1 : 0;
+  a.a_mn = p.a_mn ? 1 : 0;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
@@ -390,6 +393,16 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   // router's FP32 staging loads start before that wait: their predecessor is the
   // same call's split kernel, which writes only the workspace.)
   l.pdl = true;
+  return DP_OK;
+}
+
+dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int64_t lda, const void* B,
+                      int64_t ldb, const void* B_lo, void* out, int64_t ldo, void* ws, cudaStream_t stream,
+                      int64_t bsa = 0, int64_t bsb = 0, int64_t bso = 0) {
+  GemmLaunch l;
+  const dp_status st = prepare_view(p, dev, A, lda, B, ldb, B_lo, out, ldo, ws, bsa, bsb, bso, &l);
+  if (st != DP_OK) return st;
+  const GemmArgs& a = l.args;
   cudaError_t e = cudaErrorInvalidValue;
   if (!p.a_mn && !p.b_mn)
     e = launch_gemm_kk(p.bn, l, stream);
@@ -559,6 +572,110 @@ dp_status run_batched(int op, const void* a, int64_t lda, int64_t bsa, const voi
   if (op == kOpWgrad && p.swap)  // A = X, B = dY
     return launch_view(p, *dev, b, ldb, a, lda, nullptr, out, ldo, ws, stream, bsb, bsa, bso);
   return launch_view(p, *dev, a, lda, b, ldb, nullptr, out, ldo, ws, stream, bsa, bsb, bso);
+}
+
+// ------------------------------------------------------------ backward pass
+
+Overrides env_overrides() {
+  const char* sw = std::getenv("DP_FORCE_SWAP");
+  const char* pr = std::getenv("DP_FORCE_PAIR");
+  const char* fu = std::getenv("DP_FORCE_FUSE");
+  Overrides o;
+  o.bn = env_int("DP_FORCE_BN");
+  o.splits = env_int("DP_FORCE_SPLITS");
+  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
+  o.swap = sw ? std::atoi(sw) : -1;
+  o.pair = pr ? std::atoi(pr) : -1;
+  o.fuse = fu ? std::atoi(fu) : -1;
+  return o;
+}
+
+struct BwdEntry {
+  bool valid = false;
+  int64_t T, N, K;
+  int dx_f32, dw_f32, sm;
+  Overrides o;
+  BwdPlan plan;
+};
+thread_local BwdEntry t_bwd_plans[16];
+
+bool bwd_plan_for(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int sm, BwdPlan* plan) {
+  const Overrides o = env_overrides();
+  uint64_t h = mix(mix(mix(static_cast<uint64_t>(T), static_cast<uint64_t>(N)), static_cast<uint64_t>(K)),
+                   static_cast<uint64_t>(dx_f32 * 2 + dw_f32) * 4096 + static_cast<uint64_t>(sm));
+  h = mix(h, static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
+                 (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.fuse + 1) * 1000003);
+  BwdEntry& e = t_bwd_plans[h & 15];
+  if (e.valid && e.T == T && e.N == N && e.K == K && e.dx_f32 == dx_f32 && e.dw_f32 == dw_f32 && e.sm == sm &&
+      e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
+      e.o.pair == o.pair && e.o.fuse == o.fuse) {
+    *plan = e.plan;
+    return true;
+  }
+  if (!make_plan_bwd(T, N, K, dx_f32, dw_f32, sm, plan, o)) return false;
+  e.valid = true;
+  e.T = T;
+  e.N = N;
+  e.K = K;
+  e.dx_f32 = dx_f32;
+  e.dw_f32 = dw_f32;
+  e.sm = sm;
+  e.o = o;
+  e.plan = *plan;
+  return true;
+}
+
+// dX = dY W and dW = dY^T X: either the two single-op calls one after the other, or
+// one co-scheduled launch over both problems' whole-K tiles.
+dp_status run_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const void* W, int64_t ldw, void* dX,
+                  int64_t ld_dx, int dx_f32, void* dW, int64_t ld_dw, int dw_f32, int64_t T, int64_t N, int64_t K,
+                  void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if ((dx_f32 != DP_OUT_BF16 && dx_f32 != DP_OUT_F32) || (dw_f32 != DP_OUT_BF16 && dw_f32 != DP_OUT_F32))
+    return DP_ERR_INVALID_ARG;
+  dp_status st = check_sizes(T, N, K, kOpDgrad);
+  if (st != DP_OK) return st;
+  if ((st = check_matrix(dY, T, N, &ldg, 2)) != DP_OK) return st;
+  if ((st = check_matrix(X, T, K, &ldx, 2)) != DP_OK) return st;
+  if ((st = check_matrix(W, N, K, &ldw, 2)) != DP_OK) return st;
+  if ((st = check_matrix(dX, T, K, &ld_dx, dx_f32 ? 4 : 2)) != DP_OK) return st;
+  if ((st = check_matrix(dW, N, K, &ld_dw, dw_f32 ? 4 : 2)) != DP_OK) return st;
+  if (dW == nullptr || (dX == nullptr && T > 0) || W == nullptr) return DP_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != DP_OK) return st;
+  BwdPlan bp;
+  if (!bwd_plan_for(T, N, K, dx_f32, dw_f32, dev->sm_count, &bp)) return DP_ERR_INVALID_ARG;
+  if (bp.ws_bytes > 0 && T > 0 && (ws == nullptr || ws_bytes < bp.ws_bytes)) return DP_ERR_WORKSPACE;
+  if (bp.ws_bytes > 0 && T > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
+  if (!bp.fused) {
+    st = run_op(kOpDgrad, dY, ldg, W, ldw, dX, ld_dx, T, N, K, dx_f32, ws, ws_bytes, stream);
+    if (st != DP_OK) return st;
+    return run_op(kOpWgrad, dY, ldg, X, ldx, dW, ld_dw, T, N, K, dw_f32, ws, ws_bytes, stream);
+  }
+  GemmLaunch ld, lw;
+  st = prepare_view(bp.dgrad, *dev, dY, ldg, W, ldw, nullptr, dX, ld_dx, nullptr, 0, 0, 0, &ld);
+  if (st != DP_OK) return st;
+  st = bp.wgrad.swap ? prepare_view(bp.wgrad, *dev, X, ldx, dY, ldg, nullptr, dW, ld_dw, nullptr, 0, 0, 0, &lw)
+                     : prepare_view(bp.wgrad, *dev, dY, ldg, X, ldx, nullptr, dW, ld_dw, nullptr, 0, 0, 0, &lw);
+  if (st != DP_OK) return st;
+  GemmLaunch& first = bp.wgrad_first ? lw : ld;
+  const GemmLaunch& second = bp.wgrad_first ? ld : lw;
+  first.second.tmA = second.tmA;
+  first.second.tmB = second.tmB;
+  first.second.args = second.args;
+  first.grid = bp.grid;
+  return launch_gemm_bwd(bp.dgrad.bn, bp.dgrad.pair, first, stream) == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
+}
+
+void fill_bwd_info(const BwdPlan& bp, int64_t T, dp_bwd_plan_info* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->fused = bp.fused ? 1 : 0;
+  info->wgrad_first = bp.wgrad_first ? 1 : 0;
+  info->grid = bp.fused ? bp.grid : 0;
+  info->model_us = bp.model_ns * 1e-3;
+  info->separate_us = bp.separate_ns * 1e-3;
+  info->workspace_bytes = T == 0 ? 0 : bp.ws_bytes;
+  fill_info(bp.dgrad, T, &info->dgrad);
+  fill_info(bp.wgrad, T, &info->wgrad);
 }
 
 }  // namespace
@@ -731,6 +848,44 @@ dp_status dp_workspace_size(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dt
   return DP_OK;
 }
 
+dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const void* W, int64_t ldw, void* dX,
+                      int64_t ld_dx, dp_out_dtype out_dx, void* dW, int64_t ld_dw, dp_out_dtype out_dw, int64_t T,
+                      int64_t N, int64_t K, int deterministic, void* workspace, size_t workspace_bytes,
+                      dp_stream stream) {
+  (void)deterministic;
+  return run_bwd(dY, ldg, X, ldx, W, ldw, dX, ld_dx, static_cast<int>(out_dx), dW, ld_dw, static_cast<int>(out_dw),
+                 T, N, K, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+dp_status dp_plan_query_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx, dp_out_dtype out_dw, int sm_count,
+                            dp_bwd_plan_info* info) {
+  if (!info || (out_dx != DP_OUT_BF16 && out_dx != DP_OUT_F32) || (out_dw != DP_OUT_BF16 && out_dw != DP_OUT_F32))
+    return DP_ERR_INVALID_ARG;
+  const dp_status st = check_sizes(T, N, K, kOpDgrad);
+  if (st != DP_OK) return st;
+  if (sm_count <= 0) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DP_ERR_LAUNCH;
+  }
+  BwdPlan bp;
+  if (!bwd_plan_for(T, N, K, out_dx == DP_OUT_F32 ? 1 : 0, out_dw == DP_OUT_F32 ? 1 : 0, sm_count, &bp))
+    return DP_ERR_INVALID_ARG;
+  fill_bwd_info(bp, T, info);
+  return DP_OK;
+}
+
+dp_status dp_workspace_size_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx, dp_out_dtype out_dw,
+                                int sm_count, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  dp_bwd_plan_info info;
+  const dp_status st = dp_plan_query_bwd(T, N, K, out_dx, out_dw, sm_count, &info);
+  if (st != DP_OK) return st;
+  *bytes = static_cast<size_t>(info.workspace_bytes);
+  return DP_OK;
+}
+
 dp_status dp_init(int device) {
   if (device < 0 && cudaGetDevice(&device) != cudaSuccess) return DP_ERR_LAUNCH;
   DeviceState* d = nullptr;
@@ -774,6 +929,6 @@ const char* dp_status_string(dp_status status) {
   }
 }
 
-int dp_version(void) { return 110; }
+int dp_version(void) { return 120; }
 
 }  // extern "C"

@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "planner.h"
 #include "ptx.cuh"
@@ -60,6 +61,9 @@ struct GemmArgs {
   // MN-major operands whose tensor map is 3-D, [column group][contraction row][128 B]:
   // the groups of a tile arrive in one load instead of one load per group
   int32_t a3d, b3d;
+  // A read MN-major (the template's A_MN, except in a co-scheduled launch, whose two
+  // problems may differ)
+  int32_t a_mn;
   // > 1: launched as clusters of `splits` CTAs, one split tile per cluster and one
   // unit per CTA; the cluster sums its partials itself after the main loop
   int32_t cluster_fixup;
@@ -168,6 +172,46 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
 // Output of batch b.
 __device__ __forceinline__ void* out_at(const GemmArgs& a, int b) {
   return static_cast<char*>(a.out) + static_cast<int64_t>(b) * a.out_bstride * (a.out_f32 ? 4 : 2);
+}
+
+// The second problem of a co-scheduled launch (DUAL): its tensor maps and
+// arguments.  Its units follow the first problem's in the launch's unit list, so
+// the persistent CTAs that finish the first problem's tiles go on with the second's
+// (the input and weight gradients of one layer in one launch: B is MN-major in
+// both, A is K-major in the input gradient and MN-major in the weight gradient).
+template <bool DUAL>
+struct SecondProblem {
+  int32_t none;
+};
+template <>
+struct SecondProblem<true> {
+  CUtensorMap tmA, tmB;
+  GemmArgs args;
+};
+
+// One unit of the launch: its problem's arguments and maps, and its index there.
+struct UnitRef {
+  const GemmArgs* a;
+  const CUtensorMap* mA;
+  const CUtensorMap* mB;
+  int u;
+};
+
+__device__ __forceinline__ int second_units(const SecondProblem<false>&) { return 0; }
+__device__ __forceinline__ int second_units(const SecondProblem<true>& s) { return s.args.units; }
+__device__ __forceinline__ void prefetch_second(const SecondProblem<false>&) {}
+__device__ __forceinline__ void prefetch_second(const SecondProblem<true>& s) {
+  tma_prefetch_map(&s.tmA);
+  tma_prefetch_map(&s.tmB);
+}
+__device__ __forceinline__ UnitRef unit_ref(int u, const GemmArgs& a0, const CUtensorMap& mA, const CUtensorMap& mB,
+                                            const SecondProblem<false>&) {
+  return {&a0, &mA, &mB, u};
+}
+__device__ __forceinline__ UnitRef unit_ref(int u, const GemmArgs& a0, const CUtensorMap& mA, const CUtensorMap& mB,
+                                            const SecondProblem<true>& s) {
+  if (u < a0.units) return {&a0, &mA, &mB, u};
+  return {&s.args, &s.tmA, &s.tmB, u - a0.units};
 }
 
 // Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
@@ -335,14 +379,20 @@ __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthread
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3>
+// DUAL: a co-scheduled launch of two problems with MN-major B (see SecondProblem);
+// each unit's A majorness comes from its problem's arguments.
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3, bool DUAL>
 __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ GemmArgs args,
+                     const __grid_constant__ SecondProblem<DUAL> second) {
   using C = TileCfg<BN, PAIR, X3>;
+  static_assert(!DUAL || (B_MN && !X3), "co-scheduled problems: BF16, MN-major B");
   constexpr int STAGES = C::STAGES;
   constexpr int SSTAGES = C::SSTAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(C::TM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC_AMN = idesc_bf16_f32(C::TM, BN, true, B_MN);  // (DUAL: MN-major A)
+  const int total_units = args.units + second_units(second);
   // With PAIR, a cluster of two CTAs computes one TM x BN tile: rank r loads A rows
   // [r*128, r*128+128) and B rows [r*BN/2, (r+1)*BN/2) of the tile into the same
   // shared-memory offsets, the leader (rank 0) issues the 2-CTA MMAs, and rank r's
@@ -376,6 +426,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     tma_prefetch_map(&tmA);
     tma_prefetch_map(&tmB);
     if (X3) tma_prefetch_map(&tmB2);
+    prefetch_second(second);
   }
 
   if (threadIdx.x == 0) {
@@ -558,8 +609,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
       if (!X3) pdl_wait();  // the previous kernel on the stream (launched as its dependent) is done
-      for (int u = unit0; !X3 && ok && u < args.units; u += unit_step) {
-        const Unit w = decode_unit(args, u);
+      for (int u = unit0; !X3 && ok && u < total_units; u += unit_step) {
+        const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
+        const GemmArgs& ga = *ur.a;
+        const bool a_mn = DUAL ? ga.a_mn != 0 : A_MN;
+        const Unit w = decode_unit(ga, ur.u);
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -575,7 +629,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES);
           // (batched plans: every map has a trailing batch dimension)
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-            if (args.batch > 1) {
+            if (ga.batch > 1) {
               if (PAIR)
                 tma_load_3d_pair(dst, map, fb, x, y, w.b);
               else
@@ -593,21 +647,21 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
               tma_load_3d(dst, map, fb, 0, y, z);
           };
           // MN-major: 64-column groups of 64 contraction rows (8 KB each)
-          if (A_MN && args.a3d) {
-            load3(sa, &tmA, kb * C::BK, a_row0 / 64);
-          } else if (A_MN) {
-            load(sa, &tmA, a_row0, kb * C::BK);
-            load(sa + 8192, &tmA, a_row0 + 64, kb * C::BK);
+          if (a_mn && ga.a3d) {
+            load3(sa, ur.mA, kb * C::BK, a_row0 / 64);
+          } else if (a_mn) {
+            load(sa, ur.mA, a_row0, kb * C::BK);
+            load(sa + 8192, ur.mA, a_row0 + 64, kb * C::BK);
           } else {
-            load(sa, &tmA, kb * C::BK, a_row0);
+            load(sa, ur.mA, kb * C::BK, a_row0);
           }
-          if (B_MN && args.b3d) {
-            load3(sb, &tmB, kb * C::BK, b_row0 / 64);
+          if (B_MN && ga.b3d) {
+            load3(sb, ur.mB, kb * C::BK, b_row0 / 64);
           } else if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, &tmB, b_row0 + 64 * j, kb * C::BK);
+            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, ur.mB, b_row0 + 64 * j, kb * C::BK);
           } else {
-            load(sb, &tmB, kb * C::BK, b_row0);
+            load(sb, ur.mB, kb * C::BK, b_row0);
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -639,8 +693,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int u = unit0; ok && u < args.units; u += unit_step, ++local) {
-        const Unit w = decode_unit(args, u);
+      for (int u = unit0; ok && u < total_units; u += unit_step, ++local) {
+        const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
+        const Unit w = decode_unit(*ur.a, ur.u);
+        const bool a_mn = DUAL ? ur.a->a_mn != 0 : A_MN;
+        const uint32_t idesc = (DUAL && a_mn) ? IDESC_AMN : IDESC;
         const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
@@ -687,12 +744,12 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             }
             // K-major: step 16 elements (32 bytes) along the swizzled row;
             // MN-major: step 16 contraction rows (16 x 128 bytes).
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t ad = a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             if (PAIR)
-              mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+              mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             else
-              mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+              mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           // frees the stage (in both CTAs of a pair) once these MMAs have read it
           if (PAIR)
@@ -820,8 +877,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           mbar_arrive(tempty_bar(a));
       }
     };
-    for (int u = unit0; u < args.units; u += unit_step, ++local) {
-      const Unit w = decode_unit(args, u);
+    for (int u = unit0; u < total_units; u += unit_step, ++local) {
+      const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
+      const GemmArgs& ga = *ur.a;
+      const Unit w = decode_unit(ga, ur.u);
       const int tm = w.tm, tn = w.tn;
       const int slot = w.ptile * (PAIR ? 2 : 1) + static_cast<int>(rank);  // this CTA's partial slot
       const int acc = local & 1;
@@ -838,7 +897,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       tc_fence_after();
       const int64_t m = static_cast<int64_t>(tm) * C::TM + static_cast<int64_t>(rank) * C::BM + row;
       const int64_t m0 = m - lane;  // row of lane 0
-      void* outb = out_at(args, w.b);
+      void* outb = out_at(ga, w.b);
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
       if (!w.split) {
@@ -851,19 +910,19 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_block32(args, outb, ebuf, lane, m0, n0 + c * 32, v);
+          store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
         // 32 rows write 512 contiguous bytes.
-        float4* part = args.partials + (static_cast<size_t>(slot) * args.splits + w.s) * (C::BM * BN / 4);
+        float4* part = ga.partials + (static_cast<size_t>(slot) * ga.splits + w.s) * (C::BM * BN / 4);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tcol + c * 32, r);
           tmem_wait_ld();
           if (c == BN / 32 - 1) release_acc(acc);
-          if (m < args.gm) {  // padding rows of a thin tile are never read back
+          if (m < ga.gm) {  // padding rows of a thin tile are never read back
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               __stcg(&part[(c * 8 + j) * C::BM + row],
@@ -888,7 +947,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     else
       tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (!PAIR && args.cluster_fixup > 1) cluster_fixup_sum<BN>(args, C::THREADS);
+  if (!PAIR && !DUAL && args.cluster_fixup > 1) cluster_fixup_sum<BN>(args, C::THREADS);
 }
 
 // Host-side launch of one instantiation (defined in the per-view .cu files).
@@ -896,6 +955,7 @@ struct GemmLaunch {
   CUtensorMap tmA, tmB;
   CUtensorMap tmB2;  // X3: B's bf16 lo plane (tmB is the hi plane); otherwise unused
   GemmArgs args;
+  SecondProblem<true> second;  // co-scheduled launches: the second problem
   int grid;   // CTAs (twice the number of pairs for a paired plan)
   bool pair;  // clusters of two CTAs share each tile
   bool x3;    // router BF16x3 mode: FP32 A split in the kernel, B from pre-split planes
@@ -909,6 +969,10 @@ int max_clusters_mm(int bn, bool x3, int cluster, int grid);
 cudaError_t launch_gemm_kk(int bn, const GemmLaunch& l, cudaStream_t stream);  // forward
 cudaError_t launch_gemm_km(int bn, const GemmLaunch& l, cudaStream_t stream);  // input gradient
 cudaError_t launch_gemm_mm(int bn, const GemmLaunch& l, cudaStream_t stream);  // weight gradient
+// Input gradient and weight gradient co-scheduled in one launch (gemm_bwd.cu):
+// l.args / l.tmA / l.tmB the problem whose units come first, l.second the other.
+cudaError_t launch_gemm_bwd(int bn, bool pair, const GemmLaunch& l, cudaStream_t stream);
+cudaError_t set_attributes_bwd();
 // Router operand split: the bf16 hi/lo copies the BF16x3 GEMMs read (split_x3.cu).
 struct SplitJob {
   const float* x;       // FP32 [rows][cols], leading dimension ldx (multiple of 4)
@@ -929,7 +993,10 @@ cudaError_t set_attributes_kk();
 cudaError_t set_attributes_km();
 cudaError_t set_attributes_mm();
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
+inline SecondProblem<false> second_of(const GemmLaunch&, std::false_type) { return SecondProblem<false>{0}; }
+inline const SecondProblem<true>& second_of(const GemmLaunch& l, std::true_type) { return l.second; }
+
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false, bool DUAL = false>
 cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(l.grid), 1, 1);
@@ -953,7 +1020,8 @@ cudaError_t launch_gemm_t(const GemmLaunch& l, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, l.tmA, l.tmB, l.tmB2, l.args);
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3, DUAL>, l.tmA, l.tmB, l.tmB2, l.args,
+                            second_of(l, std::integral_constant<bool, DUAL>()));
 }
 
 // How many clusters of `cluster` CTAs of this instantiation the device runs at once
@@ -972,19 +1040,19 @@ int max_active_clusters_t(int cluster, int grid) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();  // clear: treated as "no cluster plan"
     return 0;
   }
   return n;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false>
+template <int BN, bool A_MN, bool B_MN, bool PAIR, bool X3 = false, bool DUAL = false>
 cudaError_t set_attr_t() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3, DUAL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, PAIR, X3>::SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3>,
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<BN, A_MN, B_MN, PAIR, X3, DUAL>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   return e;
 }

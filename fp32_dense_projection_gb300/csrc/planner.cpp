@@ -15,6 +15,7 @@
 #include "planner.h"
 
 #include <algorithm>
+#include <vector>
 
 namespace dp {
 
@@ -35,6 +36,8 @@ constexpr double kNarrowB = 1.35;             // tiles whose B slice per CTA is 
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
+constexpr double kLaunchNs = 3000.0;          // a launch's fixed cost: setup, first loads, last tile's epilogue
+constexpr double kFuseGain = 0.97;            // co-schedule the backward pass only for >= 3% modelled gain
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -111,6 +114,17 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   return std::max(std::max(t_mma, t_load), t_split) + out_tile / dram;
 }
 
+// How many times the tiles load each unique operand byte (at least 1).
+double reuse_of(const View& v, const Tiling& t) {
+  const int64_t tiles = v.batch * ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
+  const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, v.bk));
+  const double a_rows = static_cast<double>(std::min<int64_t>(t.rows(), v.gm));
+  const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn));
+  const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
+  const double unique = static_cast<double>(v.batch) * (v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
+  return std::max(1.0, loaded / std::max(1.0, unique));
+}
+
 // Modelled time of a plan: `full` whole-K units followed by (tiles - full) tiles
 // split `splits` ways, run by min(units, slots) persistent CTAs (or pairs); never
 // faster than the unique operand bytes cross from DRAM; split plans add the
@@ -123,10 +137,8 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
   const int64_t units = full + split_units;
   const int64_t active_sms = std::min<int64_t>(units, slots) * (t.pair ? 2 : 1);
   const double a_rows = static_cast<double>(std::min<int64_t>(t.rows(), v.gm));
-  const double b_rows = static_cast<double>(std::min<int64_t>(t.bn, v.gn));
-  const double loaded = static_cast<double>(tiles) * nkb * (a_rows * v.a_elem + b_rows * v.b_elem) * v.bk;
+  const double reuse = reuse_of(v, t);
   const double unique = static_cast<double>(v.batch) * (v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
-  const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
   double time = 0.0;
   if (full > 0)
     time += static_cast<double>(ceil_div(full, slots)) * unit_ns(v, t, nkb, false, active_sms, reuse, out_bytes);
@@ -202,6 +214,30 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       }
     }
   }
+}
+
+// Modelled time of one co-scheduled launch: the whole-K units of `first`, then
+// those of `second` (same tiling), dealt round-robin to the persistent CTAs (unit
+// u to CTA slot u mod slots, as the kernel walks them); the busiest slot sets the
+// time, never below the DRAM time of both problems' unique bytes.
+double fused_model_ns(const Plan& first, const Plan& second, int sm) {
+  const Tiling t = {first.bn, first.pair};
+  const int64_t slots = t.pair ? sm / 2 : sm;
+  const int64_t units = first.units + second.units;
+  const int64_t active_sms = std::min<int64_t>(units, slots) * (t.pair ? 2 : 1);
+  double dram_bytes = 0.0;
+  auto unit_time = [&](const Plan& p) {
+    const View v = {p.gm, p.gn, p.gk, p.a_mn, p.b_mn, 2, 2};
+    const int out_bytes = p.out_f32 ? 4 : 2;
+    dram_bytes += (v.gm * v.a_elem + v.gn * v.b_elem) * static_cast<double>(v.gk) +
+                  static_cast<double>(v.gm) * v.gn * out_bytes;
+    return unit_ns(v, t, std::max<int64_t>(1, p.nkb), false, active_sms, reuse_of(v, t), out_bytes);
+  };
+  const double t1 = unit_time(first), t2 = unit_time(second);
+  std::vector<double> slot(static_cast<size_t>(slots), 0.0);
+  for (int64_t u = 0; u < units; ++u) slot[static_cast<size_t>(u % slots)] += u < first.units ? t1 : t2;
+  const double busiest = *std::max_element(slot.begin(), slot.end());
+  return std::max(busiest, dram_bytes / kHbmBytesPerNs);
 }
 
 }  // namespace
@@ -307,6 +343,60 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   // gradient is itself stored [K][N] (then the unswapped one is transposed instead)
   plan.out_trans = (op == kOpWgrad || op == kOpRouterWgrad) && (plan.swap != w_kn);
   *p = plan;
+  return true;
+}
+
+bool make_plan_bwd(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int sm, BwdPlan* out,
+                   const Overrides& o) {
+  if (!out || sm < 1) return false;
+  BwdPlan r;
+  if (!make_plan(kOpDgrad, T, N, K, dx_f32, sm, &r.dgrad, o) || !make_plan(kOpWgrad, T, N, K, dw_f32, sm, &r.wgrad, o))
+    return false;
+  r.separate_ns = r.dgrad.model_ns + r.wgrad.model_ns + 2 * kLaunchNs;
+  r.model_ns = r.separate_ns;
+  r.ws_bytes = std::max(r.dgrad.ws_bytes, r.wgrad.ws_bytes);
+  // Co-scheduled candidates: one tiling for both problems, whole K per tile (no
+  // workspace, and the same per-tile sums as whole-K single-op plans), either
+  // problem's units first.
+  if (T > 0 && o.fuse != 0 && o.splits <= 1 && o.tail_splits <= 0) {
+    bool have = false;
+    BwdPlan best;
+    for (int pair = 0; pair < 2; ++pair) {
+      if (o.pair >= 0 && pair != o.pair) continue;
+      for (int bn : {256, 128}) {
+        if (o.bn > 0 && bn != o.bn) continue;
+        Overrides f = o;
+        f.pair = pair;
+        f.bn = bn;
+        f.splits = 1;
+        f.tail_splits = 0;
+        Plan d, w;
+        if (!make_plan(kOpDgrad, T, N, K, dx_f32, sm, &d, f) || !make_plan(kOpWgrad, T, N, K, dw_f32, sm, &w, f))
+          continue;
+        if (d.splits != 1 || w.splits != 1 || d.units < 1 || w.units < 1) continue;
+        for (int wf = 0; wf < 2; ++wf) {
+          if (o.fuse >= 2 && wf != (o.fuse == 2 ? 1 : 0)) continue;
+          const double t = fused_model_ns(wf ? w : d, wf ? d : w, sm) + kLaunchNs;
+          if (!have || t < best.model_ns) {
+            have = true;
+            best.fused = true;
+            best.wgrad_first = wf != 0;
+            best.dgrad = d;
+            best.wgrad = w;
+            best.model_ns = t;
+            const int64_t slots = pair ? sm / 2 : sm;
+            best.grid = static_cast<int>(std::min<int64_t>(d.units + w.units, slots) * (pair ? 2 : 1));
+          }
+        }
+      }
+    }
+    if (have && (o.fuse >= 1 || best.model_ns < kFuseGain * r.separate_ns)) {
+      best.separate_ns = r.separate_ns;
+      best.ws_bytes = 0;
+      r = best;
+    }
+  }
+  *out = r;
   return true;
 }
 

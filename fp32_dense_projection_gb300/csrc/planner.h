@@ -106,6 +106,9 @@ struct Overrides {
   int tail_splits = 0;
   int swap = -1;
   int pair = -1;
+  // backward pass: 0 two launches; 1 one co-scheduled launch (if any tiling admits it),
+  // 2 / 3 the same with the weight / input gradient's units first
+  int fuse = -1;
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,
@@ -114,5 +117,22 @@ struct Overrides {
 // w_kn: W (and dW) stored [K][N] rather than [N][K].
 bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm_count, Plan* plan,
                const Overrides& overrides = Overrides(), int64_t batch = 1, bool w_kn = false);
+
+// The backward pass of one layer: the input gradient and the weight gradient of
+// the same dY.  Either the two single-op plans, run one after the other, or one
+// co-scheduled launch: both problems tiled alike with whole K per tile, their units
+// in one list dealt to the same persistent CTAs, so the CTAs that run out of one
+// problem's tiles go on with the other's instead of waiting for a second launch.
+struct BwdPlan {
+  bool fused = false;        // one co-scheduled launch
+  bool wgrad_first = false;  // fused: the weight gradient's units come first in the list
+  Plan dgrad, wgrad;         // fused: whole-K plans of one tiling; else the single-op plans
+  int grid = 0;              // fused: CTAs of the launch
+  double model_ns = 0.0;     // the chosen form's modelled duration
+  double separate_ns = 0.0;  // the two single-op launches' modelled duration
+  size_t ws_bytes = 0;       // workspace (the two single-op calls share one)
+};
+bool make_plan_bwd(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int sm_count, BwdPlan* plan,
+                   const Overrides& overrides = Overrides());
 
 }  // namespace dp

@@ -44,9 +44,13 @@
  *   needs no initial value.  One workspace must not be used by two calls that may
  *   run concurrently.
  * Launches.  Each call enqueues one GEMM kernel; a plan that splits contractions
- *   adds the kernel that sums the partials (launched as a programmatic dependent
- *   of the GEMM), and a router call adds the kernel that splits its reused FP32
- *   operand into bf16 hi/lo before the GEMM.
+ *   adds the kernel that sums the partials, and a router call adds the kernel
+ *   that splits its reused FP32 operand into bf16 hi/lo before the GEMM.  The GEMM
+ *   and the reduction launch as programmatic dependents of the kernel before them
+ *   on the stream: their setup overlaps that kernel's tail, and they wait for its
+ *   completion before touching global memory, so stream order between calls (one
+ *   call reading what the previous one wrote, or overwriting what it read) holds
+ *   as for ordinary launches.
  * Stream.  `stream` is a cudaStream_t (NULL = legacy default stream).  All work
  *   is enqueued on it; calls return before the GPU finishes.  Calls are legal
  *   inside CUDA stream capture after the first call on the device (which sets
@@ -187,6 +191,31 @@ dp_status dp_gemm_wgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const 
                                 int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
                                 void* workspace, size_t workspace_bytes, dp_stream stream);
 
+/* -------------------------------------------------------- backward pass (BF16) */
+/* Input gradient and weight gradient of one layer from the same dY (the pages'
+ * "bwd" op is dgrad + wgrad, [router] benchmark rows):
+ *   dX[t][k] = sum_n dY[t][n] * W[n][k]      (as dp_gemm_dgrad_ex)
+ *   dW[n][k] = sum_t dY[t][n] * X[t][k]      (as dp_gemm_wgrad_ex)
+ * with their own output precisions and leading dimensions.  The planner picks one
+ * of two forms (dp_plan_query_bwd reports which):
+ *   - the two single-op calls, one after the other on `stream`, sharing the
+ *     workspace (bitwise the same as calling dp_gemm_dgrad_ex, dp_gemm_wgrad_ex);
+ *   - one co-scheduled launch: both problems tiled alike (one tile shape) with
+ *     whole K per tile, their tiles in one list dealt to one persistent grid, so
+ *     the SMs left idle by one problem's last wave run the other's tiles.  Needs
+ *     no workspace.  Every output element is the same whole-K sum a whole-K
+ *     single-op plan computes.
+ * Chosen when the cost model expects the co-scheduled launch to be at least 3%
+ * faster (small and mid-size T, where each single-op launch leaves SMs idle);
+ * DP_FORCE_FUSE overrides (0: two calls; 1: co-scheduled; 2 / 3: co-scheduled
+ * with the weight / input gradient's tiles first).  dX and dW must not overlap
+ * dY, X or W.
+ * Arguments and errors as the single-op calls; workspace: dp_workspace_size_bwd. */
+dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const void* W, int64_t ldw,
+                      void* dX, int64_t ld_dx, dp_out_dtype out_dx, void* dW, int64_t ld_dw, dp_out_dtype out_dw,
+                      int64_t T, int64_t N, int64_t K, int deterministic,
+                      void* workspace, size_t workspace_bytes, dp_stream stream);
+
 /* ----------------------------------------------------------------- router ops */
 /* [router]: FP32 operands and FP32 output; N is the expert count (256 on the
  * pages) and K the hidden size.  Each FP32 operand value x is split into bf16
@@ -229,7 +258,8 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * ways), DP_FORCE_SWAP (0 / 1: BF16 weight-gradient orientation), DP_FORCE_PAIR
  * (0 / 1: single-CTA or CTA-pair tiles), DP_FORCE_CLUSTER_SUM=0 (sum split
  * partials in the reduction kernel instead of inside the GEMM's clusters; the
- * two give the same bits).  A forced plan is still deterministic and keeps the
+ * two give the same bits), DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls
+ * or as one co-scheduled launch, see dp_gemm_bwd).  A forced plan is still deterministic and keeps the
  * accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of
@@ -275,11 +305,29 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
 dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                                 int weight_kn, int sm_count, dp_plan_info* info);
 
+/* The backward pass's plan: the form chosen and the plan of each problem (for the
+ * co-scheduled launch, whole-K plans of one tile shape; grid is the launch's). */
+typedef struct dp_bwd_plan_info {
+    int32_t fused;            /* 1: one co-scheduled launch; 0: two single-op calls */
+    int32_t wgrad_first;      /* co-scheduled: the weight gradient's tiles are dealt first */
+    int32_t grid;             /* co-scheduled: persistent CTAs of the launch (else 0) */
+    int32_t reserved;
+    double model_us;          /* modelled duration of the chosen form */
+    double separate_us;       /* modelled duration of the two single-op calls */
+    uint64_t workspace_bytes; /* == dp_workspace_size_bwd() */
+    dp_plan_info dgrad;       /* input-gradient problem */
+    dp_plan_info wgrad;       /* weight-gradient problem */
+} dp_bwd_plan_info;
+dp_status dp_plan_query_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx, dp_out_dtype out_dw,
+                            int sm_count, dp_bwd_plan_info* info);
+
 /* Workspace bytes a call needs (see dp_plan_query for sm_count). */
 dp_status dp_workspace_size(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                             int sm_count, size_t* bytes);
 dp_status dp_workspace_size_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                                     int weight_kn, int sm_count, size_t* bytes);
+dp_status dp_workspace_size_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx, dp_out_dtype out_dw,
+                                int sm_count, size_t* bytes);
 
 /* Check the device's architecture and set kernel attributes on `device`
  * (the current device if < 0).  Optional: the first call on a device does it. */

@@ -267,3 +267,70 @@ def test_batched_argument_checks(L):
     # router ops have no batched form
     info = dp.PlanInfo()
     assert L.dp_plan_query_batched(3, 2, 64, 64, 64, 0, 0, SM, ctypes.byref(info)) == 1
+
+
+# ------------------------------------------------------------------ backward pass
+
+@pytest.mark.parametrize("T,N,K", [(1024, 1024, 4096), (4031, 1024, 4096), (1024, 12288, 4096),
+                                   (16384, 12288, 4096), (64, 1024, 4096), (1000, 384, 640), (65537, 64, 4096),
+                                   (0, 64, 128)])
+@pytest.mark.parametrize("dx32,dw32", [(False, False), (True, False), (False, True)])
+def test_bwd_plan_is_consistent(T, N, K, dx32, dw32):
+    b = dp.plan_bwd(T, N, K, dx32, dw32, sm_count=SM)
+    d, w = b["dgrad"], b["wgrad"]
+    if b["fused"]:
+        # one tile shape, whole K in every tile of both problems, no workspace, one CTA
+        # (or pair) per unit up to one per SM
+        per = 2 if d["cta_pair"] else 1
+        assert (d["cta_pair"], d["block_n"]) == (w["cta_pair"], w["block_n"])
+        for p in (d, w):
+            assert p["splits"] == 1 and p["full_units"] == p["units"] == p["tiles"]
+        assert b["workspace_bytes"] == 0
+        assert b["grid"] == min(d["units"] + w["units"], SM // per) * per
+        assert b["model_us"] < b["separate_us"]
+    else:
+        # the single-op plans, run one after the other with one workspace
+        assert d == dp.plan("dgrad", T, N, K, dx32, sm_count=SM)
+        assert w == dp.plan("wgrad", T, N, K, dw32, sm_count=SM)
+        assert b["workspace_bytes"] == (0 if T == 0 else max(d["workspace_bytes"], w["workspace_bytes"]))
+        assert b["grid"] == 0 and b["model_us"] == b["separate_us"]
+    assert dp.workspace_size_bwd(T, N, K, dx32, dw32, sm_count=SM) == b["workspace_bytes"]
+
+
+def test_bwd_co_schedules_small_and_mid_sizes_only():
+    assert dp.plan_bwd(1024, 1024, 4096, sm_count=SM)["fused"]
+    assert dp.plan_bwd(4031, 1024, 4096, sm_count=SM)["fused"]
+    assert not dp.plan_bwd(16384, 12288, 4096, sm_count=SM)["fused"]
+    assert not dp.plan_bwd(0, 1024, 4096, sm_count=SM)["fused"]
+
+
+def test_bwd_overrides(monkeypatch):
+    monkeypatch.setenv("DP_FORCE_FUSE", "1")
+    assert dp.plan_bwd(16384, 12288, 4096, sm_count=SM)["fused"]
+    # beyond the accumulation bound the weight gradient must split: two launches
+    assert not dp.plan_bwd(40000, 1024, 1024, sm_count=SM)["fused"]
+    for order, first in (("2", 1), ("3", 0)):
+        monkeypatch.setenv("DP_FORCE_FUSE", order)
+        assert dp.plan_bwd(1000, 384, 640, sm_count=SM)["wgrad_first"] == first
+    monkeypatch.setenv("DP_FORCE_FUSE", "1")
+    monkeypatch.setenv("DP_FORCE_PAIR", "0")
+    monkeypatch.setenv("DP_FORCE_BN", "128")
+    b = dp.plan_bwd(1000, 384, 640, sm_count=SM)
+    assert b["fused"] and (b["dgrad"]["cta_pair"], b["dgrad"]["block_n"]) == (0, 128)
+    monkeypatch.setenv("DP_FORCE_FUSE", "0")
+    assert not dp.plan_bwd(1024, 1024, 4096, sm_count=SM)["fused"]
+
+
+def test_bwd_argument_checks(L):
+    P = ctypes.c_void_p
+    good = P(1 << 20)   # never dereferenced: every call below fails its checks first
+    odd = P((1 << 20) + 8)
+    args = lambda dY=good, X=good, W=good, dX=good, dW=good, odx=0, odw=0, N=64: (
+        dY, 0, X, 0, W, 0, dX, 0, odx, dW, 0, odw, 64, N, 64, 1, None, 0, None)
+    assert L.dp_gemm_bwd(*args(W=None)) == 1
+    assert L.dp_gemm_bwd(*args(dW=None)) == 1
+    assert L.dp_gemm_bwd(*args(X=odd)) == 2
+    assert L.dp_gemm_bwd(*args(odw=5)) == 1
+    assert L.dp_gemm_bwd(*args(N=60)) == 3
+    info = dp.BwdPlanInfo()
+    assert L.dp_plan_query_bwd(64, 64, 64, 2, 0, SM, ctypes.byref(info)) == 1

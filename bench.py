@@ -516,7 +516,7 @@ def run_suite(args, local):
                 flush.zero_()
                 fn()
             torch.cuda.synchronize()
-        mine = ("gemm_bf16_kernel", "split_reduce_kernel", "split_x3_kernel")
+        mine = ("gemm_bf16_kernel", "split_reduce_kernel", "split_x3_kernel", "router_ffma_kernel")
         calls, cur = [], None
         for e in sorted((e for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA),
                         key=lambda e: e.time_range.start):

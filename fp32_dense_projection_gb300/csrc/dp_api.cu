@@ -58,6 +58,7 @@ dp_status init_device(int dev, DeviceState** out) {
       if (e == cudaSuccess) e = set_attributes_km();
       if (e == cudaSuccess) e = set_attributes_mm();
       if (e == cudaSuccess) e = set_attributes_bwd();
+      if (e == cudaSuccess) e = set_attributes_ffma();
       if (e == cudaSuccess) e = set_attributes_split();
       if (e == cudaSuccess) e = set_attributes_reduce();
       if (e == cudaSuccess) e = cudaGetSymbolAddress(&fault, g_fault_word);
@@ -242,16 +243,18 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
   o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
   o.swap = sw ? std::atoi(sw) : -1;
   o.pair = pr ? std::atoi(pr) : -1;
+  const char* ff = std::getenv("DP_FORCE_FFMA");
+  o.ffma = ff ? std::atoi(ff) : -1;
   uint64_t h = mix(mix(mix(static_cast<uint64_t>(op), static_cast<uint64_t>(T)), static_cast<uint64_t>(N)),
                    static_cast<uint64_t>(K));
   h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
-              (o.swap + 1) * 3 + (o.pair + 1));
+              (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919);
   h = mix(h, static_cast<uint64_t>(batch) * 2 + static_cast<uint64_t>(w_kn));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
       e.batch == batch && e.w_kn == w_kn && e.o.bn == o.bn && e.o.splits == o.splits &&
-      e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair) {
+      e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma) {
     *plan = e.plan;
     return true;
   }
@@ -472,6 +475,26 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
     return launch_view(p, *dev, a, lda, b, ldb, nullptr, out, ldo, ws, stream);
   }
 
+  // Router, small T: the SIMT FP32 program, one launch on the caller's operands.
+  if (p.ffma) {
+    FfmaArgs fa;
+    std::memset(&fa, 0, sizeof(fa));
+    fa.a = static_cast<const float*>(a);
+    fa.b = static_cast<const float*>(b);
+    fa.out = static_cast<float*>(out);
+    fa.lda = lda;
+    fa.ldb = ldb;
+    fa.ldo = ldo;
+    fa.gm = p.gm;
+    fa.gn = p.gn;
+    fa.gk = p.gk;
+    fa.tiles_n = static_cast<int32_t>(p.tiles_n);
+    fa.splits = p.splits;
+    fa.kchunks = static_cast<int32_t>(p.nkb);
+    if (p.units > 0x7FFFFFFF || p.nkb > 0x7FFFFFFF) return DP_ERR_UNSUPPORTED;
+    return launch_router_ffma(p.bn, p.a_mn, p.b_mn, fa, stream) == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
+  }
+
   // Router (BF16x3).  The operand that every row tile reuses is split into bf16
   // hi/lo once here; the streamed FP32 operand is split inside the GEMM.
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -523,6 +546,7 @@ void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
   info->batch = p.batch;
   info->weight_kn = p.w_kn ? 1 : 0;
   info->tiles = p.tiles;
+  info->program = p.ffma ? 1 : 0;
   info->model_us = p.model_ns * 1e-3;
 }
 
@@ -587,6 +611,8 @@ Overrides env_overrides() {
   o.swap = sw ? std::atoi(sw) : -1;
   o.pair = pr ? std::atoi(pr) : -1;
   o.fuse = fu ? std::atoi(fu) : -1;
+  const char* ff = std::getenv("DP_FORCE_FFMA");
+  o.ffma = ff ? std::atoi(ff) : -1;
   return o;
 }
 

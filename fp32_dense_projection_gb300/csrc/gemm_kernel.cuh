@@ -982,6 +982,24 @@ struct SplitJob {
   uint32_t lo_mask;     // bit s set: segment s holds lo = RNE(x - hi), else hi = RNE(x)
 };
 cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream);
+// Small-T FP32 router program (router_ffma.cu): D[m][n] = sum_k A(m, k) B(n, k) on
+// FP32 operands with FP32 FMAs; 64 x bn tiles (bn 16 / 32 / 64), each tile's
+// contraction split over a cluster of `splits` CTAs (<= 8) whose partials are
+// summed in rank order.  K-major operands are [rows][k] matrices, MN-major ones
+// [k][rows] (leading dimensions in elements, multiples of 4, 16-byte aligned).
+struct FfmaArgs {
+  const float* a;
+  const float* b;
+  float* out;          // [gm][gn], leading dimension ldo
+  int64_t lda, ldb, ldo;
+  int64_t gm, gn, gk;
+  int32_t tiles_n;     // ceil(gn / bn)
+  int32_t splits;      // CTAs per tile (cluster size)
+  int32_t kchunks;     // ceil(gk / (4096 / bn)): contraction chunks of one stage
+};
+constexpr int ffma_stage_k(int bn) { return 4096 / bn; }  // 16 elements x (256 / bn) contraction groups
+cudaError_t launch_router_ffma(int bn, bool a_mn, bool b_mn, const FfmaArgs& a, cudaStream_t stream);
+cudaError_t set_attributes_ffma();
 // Ordered sum of the split partials a GEMM launch wrote (split_reduce.cu): for each
 // split tile, partials s = 0..splits-1 added in that order in FP32, rounded once.
 cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t split_tiles, cudaStream_t stream);

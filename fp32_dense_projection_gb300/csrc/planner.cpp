@@ -37,9 +37,19 @@ constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter 
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 constexpr double kLaunchNs = 3000.0;          // a launch's fixed cost: setup, first loads, last tile's epilogue
+// SIMT FP32 router program, measured on GB300: FMAs one SM sustains (~51% of 4 x 32
+// lanes at ~1.9 GHz: its shared-memory reads match the FMA pipe's rate), the
+// launch's fixed cost, each wave's fixed cost (first loads from DRAM, the group and
+// cluster sums, the store), and CTAs per SM (its ~150 KB of shared memory: one)
+constexpr double kFfmaPerNsPerSm = 125.0;
+constexpr double kFfmaFixedNs = 1500.0;
+constexpr double kFfmaWaveNs = 3000.0;
+constexpr double kFfmaClusterNs = 1000.0;
+constexpr int kFfmaCtasPerSm = 1;
 constexpr double kFuseGain = 0.97;            // co-schedule the backward pass only for >= 3% modelled gain
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t ffma_stage_k_host(int bn) { return 4096 / bn; }  // contraction elements per stage of the SIMT program
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
 struct View {
@@ -216,6 +226,43 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
   }
 }
 
+// The router's plain FP32 contraction views for the SIMT program:
+//   forward      D = Y[T][N]:   A = X [T][K] (K-major),  B = W [N][K] (K-major)
+//   input grad.  D = dX[T][K]:  A = dY [T][N] (K-major), B = W [N][K] (MN-major), over N
+//   weight grad. D = dW[N][K]:  A = dY [T][N] (MN-major), B = X [T][K] (MN-major), over T
+View ffma_view(int op, int64_t T, int64_t N, int64_t K) {
+  if (op == kOpRouterFwd) return {T, N, K, false, false, 4, 4};
+  if (op == kOpRouterDgrad) return {T, K, N, false, true, 4, 4};
+  return {N, K, T, true, true, 4, 4};
+}
+
+// Modelled time of the SIMT program for tile width bn and `splits` CTAs per tile:
+// the CTAs run in waves of kFfmaCtasPerSm per SM sharing its FMA rate; each CTA's
+// FMAs, or its operand bytes at the L2 / DRAM mix of unit_ns, whichever is longer.
+double ffma_model_ns(const View& v, int bn, int splits, int sm) {
+  const int64_t bk = ffma_stage_k_host(bn);
+  const int64_t tiles = ceil_div(v.gm, 64) * ceil_div(v.gn, bn);
+  const int64_t chunks = std::max<int64_t>(1, ceil_div(v.gk, bk));
+  const int64_t ctas = tiles * splits;
+  const int64_t per_sm = std::min<int64_t>(kFfmaCtasPerSm, ceil_div(ctas, sm));
+  // clusters of 8 of these CTAs (~150 KB of shared memory each) run 8 at a time
+  const int64_t resident = splits > 4 ? std::min<int64_t>(sm, 64) : static_cast<int64_t>(sm) * per_sm;
+  const int64_t waves = ceil_div(ctas, resident);
+  const double k_slice = static_cast<double>(ceil_div(chunks, splits) * bk);
+  const double t_fma = 64.0 * bn * k_slice * per_sm / kFfmaPerNsPerSm;
+  const double loaded = static_cast<double>(ctas) * (64 + bn) * k_slice * 4;
+  const double unique = (static_cast<double>(v.gm) + v.gn) * v.gk * 4;
+  const double reuse = std::max(1.0, loaded / std::max(1.0, unique));
+  const double active = static_cast<double>(std::min<int64_t>(ctas, sm));
+  const double dram = std::min(kSmDramBytesPerNs, kHbmBytesPerNs / active);
+  const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) / kL2BytesPerNsPerSm);
+  const double t_load = (64 + bn) * k_slice * 4 * per_sm / bw;
+  const double out_bytes = static_cast<double>(v.gm) * v.gn * 4;
+  const double t_cluster = splits > 1 ? kFfmaClusterNs : 0.0;  // the partials' sum across the cluster
+  return kFfmaFixedNs + static_cast<double>(waves) * (kFfmaWaveNs + t_cluster + std::max(t_fma, t_load)) +
+         out_bytes / kHbmBytesPerNs;
+}
+
 // Modelled time of one co-scheduled launch: the whole-K units of `first`, then
 // those of `second` (same tiling), dealt round-robin to the persistent CTAs (unit
 // u to CTA slot u mod slots, as the kernel walks them); the busiest slot sets the
@@ -268,8 +315,11 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   c.have = true;  // empty problems: any tiling, no work units
   if (v.gm > 0 && plan.nkb > 0) {
     c.have = false;
-    // (the orientation override applies to the BF16 weight gradient only)
-    if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, o, &c);
+    // (the orientation override applies to the BF16 weight gradient only; a router
+    // plan forced onto the SIMT program takes its tile and split overrides there)
+    Overrides ot = o;
+    if (op >= kOpRouterFwd && o.ffma == 1) ot.bn = ot.splits = ot.tail_splits = 0;
+    if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, ot, &c);
     if (op == kOpWgrad && o.swap != 0) {
       // thin outputs: let K fill the 128-row tile side and N be the MMA's N
       View sv = {K, N, T, true, true, 2, 2};
@@ -342,6 +392,63 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   // D[m][n] goes out transposed for the swapped weight gradient, unless the weight
   // gradient is itself stored [K][N] (then the unswapped one is transposed instead)
   plan.out_trans = (op == kOpWgrad || op == kOpRouterWgrad) && (plan.swap != w_kn);
+
+  // Router: the SIMT FP32 program instead, when it models faster than the BF16x3
+  // program plus that program's operand-split kernel (one more launch and a pass
+  // over the reused operand).
+  if (router && T > 0 && o.ffma != 0) {
+    const View fv = ffma_view(op, T, N, K);
+    double best = 0.0;
+    int best_bn = 0, best_s = 0;
+    for (int bn : {64, 32}) {
+      if (o.bn > 0 && bn != o.bn) continue;
+      const int64_t chunks = std::max<int64_t>(1, ceil_div(fv.gk, ffma_stage_k_host(bn)));
+      for (int sp = 1; sp <= 8; ++sp) {
+        if (o.splits > 0 && sp != o.splits) continue;
+        if (sp > chunks) break;
+        const double t = ffma_model_ns(fv, bn, sp, sm);
+        if (best_bn == 0 || t < best * 0.99) {
+          best = t;
+          best_bn = bn;
+          best_s = sp;
+        }
+      }
+    }
+    // (the BF16x3 program: its GEMM's launch, plus the split kernel's pass over the
+    // reused operand, reading FP32 and writing bf16 hi / lo, and the half of that
+    // kernel's launch which the GEMM, its programmatic dependent, does not overlap)
+    const double split_pass = kLaunchNs / 2 + static_cast<double>(plan.bytes_split_a + plan.bytes_split_b) * 3.0 /
+                                                  kHbmBytesPerNs;
+    if (best_bn > 0 && (o.ffma == 1 || best < plan.model_ns + kLaunchNs + split_pass)) {
+      Plan f;
+      f.op = op;
+      f.T = T;
+      f.N = N;
+      f.K = K;
+      f.out_f32 = 1;
+      f.ffma = true;
+      f.gm = fv.gm;
+      f.gn = fv.gn;
+      f.gk = fv.gk;
+      f.a_mn = fv.a_mn;
+      f.b_mn = fv.b_mn;
+      f.bm = 64;
+      f.bn = best_bn;
+      f.bk = static_cast<int>(ffma_stage_k_host(best_bn));
+      f.stages = 2;
+      f.splits = best_s;
+      f.group = 1;
+      f.tiles_m = ceil_div(fv.gm, 64);
+      f.tiles_n = ceil_div(fv.gn, best_bn);
+      f.tiles = f.tiles_m * f.tiles_n;
+      f.nkb = std::max<int64_t>(1, ceil_div(fv.gk, f.bk));
+      f.units = f.tiles * best_s;
+      f.full_units = best_s == 1 ? f.tiles : 0;
+      f.grid = static_cast<int>(std::min<int64_t>(f.units, 0x7FFFFFFF));
+      f.model_ns = best;
+      plan = f;
+    }
+  }
   *p = plan;
   return true;
 }

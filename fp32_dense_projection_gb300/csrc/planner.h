@@ -67,6 +67,11 @@ struct Plan {
   int64_t ld_split_a = 0, ld_split_b = 0;  // their leading dimensions (elements)
   size_t ws_bytes = 0;
   double model_ns = 0.0;  // the cost model's estimate for the chosen plan
+  // Router only: the SIMT FP32 program (64 x bn tiles, each tile's contraction split
+  // over a cluster of `splits` CTAs) instead of the tensor-core BF16x3 program; its
+  // view is the plain contraction (input gradient over N, weight gradient unswapped),
+  // nkb counts its contraction chunks of bk = 4096 / bn elements.
+  bool ffma = false;
 };
 
 // Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows
@@ -109,6 +114,7 @@ struct Overrides {
   // backward pass: 0 two launches; 1 one co-scheduled launch (if any tiling admits it),
   // 2 / 3 the same with the weight / input gradient's units first
   int fuse = -1;
+  int ffma = -1;  // router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,

@@ -223,9 +223,17 @@ dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, c
  * hi_a*hi_b + hi_a*lo_b + lo_a*hi_b on the BF16 tensor cores with FP32
  * accumulation (lo_a*lo_b is dropped).  The operand the whole output reuses (W,
  * or dY for the weight gradient; both for the input gradient) is split once per
- * call into bf16 copies in the workspace (so router calls always need one);
- * the streamed FP32 operand is split inside the GEMM.  The weight gradient is
- * always computed as dW^T = X^T dY and stored transposed. */
+ * call into bf16 copies in the workspace; the streamed FP32 operand is split
+ * inside the GEMM.  The weight gradient is computed as dW^T = X^T dY and stored
+ * transposed.
+ * Small T (a few hundred tokens or fewer, as the planner's cost model decides;
+ * dp_plan_info.program reports it): a SIMT FP32 program instead -- the plain
+ * FP32 contraction with FP32 fused multiply-adds on the CUDA cores, in one launch
+ * and without workspace, each output tile's contraction split over the CTAs of a
+ * thread-block cluster whose partials are summed in a fixed order (so the output
+ * is bitwise repeatable; its error is the FP32 rounding of the sum, below the
+ * BF16x3 program's).  DP_FORCE_FFMA=0 / 1 forces either program (1: where the
+ * forced tile width and split count, if any, fit the shape). */
 
 /* Router forward: Y[t][n] = sum_k X[t][k] * W[n][k];  X: T x K, W: N x K, Y: T x N. */
 dp_status router_fwd(const float* X, const float* W, float* Y,
@@ -294,7 +302,9 @@ typedef struct dp_plan_info {
     int64_t batch;            /* independent problems in the launch (1 except batched calls) */
     int64_t tiles;            /* batch * tiles_m * tiles_n */
     int32_t weight_kn;        /* batched calls: W / dW stored [K][N] */
-    int32_t reserved2;
+    int32_t program;          /* router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
+                                 (64 x block_n tiles, `splits` CTAs per tile, block_k
+                                 contraction elements per stage); BF16 ops: 0 */
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs

@@ -51,11 +51,26 @@ def test_status_strings(L):
 SM = 152
 
 
+def check_simt_plan(op, T, N, K, p):
+    assert op.startswith("router")
+    assert p["block_m"] == 64 and p["block_n"] in (32, 64) and p["block_k"] == 4096 // p["block_n"]
+    assert 1 <= p["splits"] <= 8 and p["workspace_bytes"] == 0 and not p["cta_pair"] and not p["swap_ab"]
+    view = {"router_fwd": (T, N, K, 0, 0), "router_dgrad": (T, K, N, 0, 1), "router_wgrad": (N, K, T, 1, 1)}[op]
+    assert (p["gemm_m"], p["gemm_n"], p["gemm_k"], p["a_mn_major"], p["b_mn_major"]) == view
+    assert p["tiles_m"] == -(-p["gemm_m"] // 64) and p["tiles_n"] == -(-p["gemm_n"] // p["block_n"])
+    assert p["units"] == p["grid"] == p["tiles_m"] * p["tiles_n"] * p["splits"]
+    assert p["k_blocks"] == -(-p["gemm_k"] // p["block_k"]) and p["splits"] <= p["k_blocks"]
+    assert dp.plan(op, T, N, K, sm_count=SM) == p
+
+
 @pytest.mark.parametrize("op", list(dp.OP_NAMES))
 @pytest.mark.parametrize("T,N,K", [(64, 1024, 4096), (16384, 12288, 4096), (16231, 12288, 4096),
                                    (65537, 64, 4096), (1025, 48, 5120), (1024, 256, 4096), (1, 8, 8)])
 def test_plan_is_valid(op, T, N, K):
     p = dp.plan(op, T, N, K, out_f32=False, sm_count=SM)
+    if p["program"] == 1:  # the router's SIMT FP32 program
+        check_simt_plan(op, T, N, K, p)
+        return
     pair = bool(p["cta_pair"])
     x3 = op in ("router_fwd", "router_wgrad")  # FP32 A split in the kernel, 32-wide blocks
     assert p["block_m"] == (256 if pair else 128)
@@ -210,7 +225,9 @@ def test_workspace_only_when_needed():
             n = dp.workspace_size(op, T, N, K, sm_count=SM)
             tiles = p["tiles_m"] * p["tiles_n"]
             partials = (tiles - p["full_units"]) * (2 if p["cta_pair"] else 1) * p["splits"] * 128 * p["block_n"] * 4
-            if op.startswith("router"):
+            if p["program"] == 1:  # the router's SIMT program sums its splits in the cluster
+                assert n == 0
+            elif op.startswith("router"):
                 assert n > partials
             elif p["splits"] > 1:
                 assert n >= partials > 0
@@ -334,3 +351,35 @@ def test_bwd_argument_checks(L):
     assert L.dp_gemm_bwd(*args(N=60)) == 3
     info = dp.BwdPlanInfo()
     assert L.dp_plan_query_bwd(64, 64, 64, 2, 0, SM, ctypes.byref(info)) == 1
+
+
+# ------------------------------------------------------------ router SIMT program
+
+def test_router_program_choice():
+    # the SIMT FP32 program for the router's input gradient at a few dozen tokens (one
+    # launch, no workspace); the BF16x3 tensor-core program elsewhere
+    for T in (1, 64):
+        p = dp.plan("router_dgrad", T, 256, 4096, sm_count=SM)
+        assert p["program"] == 1 and p["workspace_bytes"] == 0 and p["block_m"] == 64
+        assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["splits"] and 1 <= p["splits"] <= 8
+    for op in ("router_fwd", "router_wgrad"):
+        assert dp.plan(op, 64, 256, 4096, sm_count=SM)["program"] == 0
+    for op in ("router_fwd", "router_dgrad", "router_wgrad"):
+        assert dp.plan(op, 1024, 256, 4096, sm_count=SM)["program"] == 0
+    for op in ("fwd", "dgrad", "wgrad"):
+        assert dp.plan(op, 64, 256, 4096, sm_count=SM)["program"] == 0
+
+
+def test_router_program_overrides(monkeypatch):
+    monkeypatch.setenv("DP_FORCE_FFMA", "1")
+    monkeypatch.setenv("DP_FORCE_BN", "32")
+    monkeypatch.setenv("DP_FORCE_SPLITS", "3")
+    p = dp.plan("router_wgrad", 1000, 256, 4096, sm_count=SM)
+    assert (p["program"], p["block_n"], p["splits"]) == (1, 32, 3)
+    # its view: the plain contraction (weight gradient over the tokens, unswapped)
+    assert (p["gemm_m"], p["gemm_n"], p["gemm_k"], p["swap_ab"]) == (256, 4096, 1000, 0)
+    assert p["k_blocks"] == -(-1000 // p["block_k"]) and p["block_k"] == 4096 // 32
+    monkeypatch.setenv("DP_FORCE_FFMA", "0")
+    monkeypatch.delenv("DP_FORCE_BN")
+    monkeypatch.delenv("DP_FORCE_SPLITS")
+    assert dp.plan("router_dgrad", 64, 256, 4096, sm_count=SM)["program"] == 0

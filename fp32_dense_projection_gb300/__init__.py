@@ -46,7 +46,7 @@ class DPError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "splits", "raster_group", "grid",
-        "a_mn_major", "b_mn_major", "swap_ab", "cta_pair", "raster_rows", "reserved")] + [(n, ctypes.c_int64) for n in (
+        "a_mn_major", "b_mn_major", "swap_ab", "cta_pair", "raster_rows", "stream_k")] + [(n, ctypes.c_int64) for n in (
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
         ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double),
         ("batch", ctypes.c_int64), ("tiles", ctypes.c_int64), ("weight_kn", ctypes.c_int32),

@@ -245,16 +245,20 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
   o.pair = pr ? std::atoi(pr) : -1;
   const char* ff = std::getenv("DP_FORCE_FFMA");
   o.ffma = ff ? std::atoi(ff) : -1;
+  const char* sk = std::getenv("DP_FORCE_STREAM_K");
+  o.stream_k = sk ? std::atoi(sk) : -1;
   uint64_t h = mix(mix(mix(static_cast<uint64_t>(op), static_cast<uint64_t>(T)), static_cast<uint64_t>(N)),
                    static_cast<uint64_t>(K));
   h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
-              (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919);
+              (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919 +
+              static_cast<uint64_t>(o.stream_k + 1) * 104729);
   h = mix(h, static_cast<uint64_t>(batch) * 2 + static_cast<uint64_t>(w_kn));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
       e.batch == batch && e.w_kn == w_kn && e.o.bn == o.bn && e.o.splits == o.splits &&
-      e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma) {
+      e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma &&
+      e.o.stream_k == o.stream_k) {
     *plan = e.plan;
     return true;
   }
@@ -296,7 +300,7 @@ std::mutex g_cluster_mutex;
 std::vector<std::pair<ClusterKey, int>> g_cluster_capacity;
 
 int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
-  if (p.pair || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid) return 0;
+  if (p.pair || p.stream_k || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid) return 0;
   const char* off = std::getenv("DP_FORCE_CLUSTER_SUM");  // "0": always the reduction kernel (tests)
   if (off && std::atoi(off) == 0) return 0;
   int cur = 0;
@@ -382,6 +386,8 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   a.a3d = a3d ? 1 : 0;
   a.b3d = b3d ? 1 : 0;
   a.a_mn = p.a_mn ? 1 : 0;
+  a.sk_slots = p.stream_k ? p.grid / (p.pair ? 2 : 1) : 0;
+  a.sk_work = p.tiles * p.nkb;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
@@ -547,6 +553,7 @@ void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
   info->weight_kn = p.w_kn ? 1 : 0;
   info->tiles = p.tiles;
   info->program = p.ffma ? 1 : 0;
+  info->stream_k = p.stream_k ? 1 : 0;
   info->model_us = p.model_ns * 1e-3;
 }
 
@@ -613,6 +620,8 @@ Overrides env_overrides() {
   o.fuse = fu ? std::atoi(fu) : -1;
   const char* ff = std::getenv("DP_FORCE_FFMA");
   o.ffma = ff ? std::atoi(ff) : -1;
+  const char* sk = std::getenv("DP_FORCE_STREAM_K");
+  o.stream_k = sk ? std::atoi(sk) : -1;
   return o;
 }
 
@@ -630,11 +639,12 @@ bool bwd_plan_for(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int s
   uint64_t h = mix(mix(mix(static_cast<uint64_t>(T), static_cast<uint64_t>(N)), static_cast<uint64_t>(K)),
                    static_cast<uint64_t>(dx_f32 * 2 + dw_f32) * 4096 + static_cast<uint64_t>(sm));
   h = mix(h, static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
-                 (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.fuse + 1) * 1000003);
+                 (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.fuse + 1) * 1000003 +
+                 static_cast<uint64_t>(o.stream_k + 1) * 104729);
   BwdEntry& e = t_bwd_plans[h & 15];
   if (e.valid && e.T == T && e.N == N && e.K == K && e.dx_f32 == dx_f32 && e.dw_f32 == dw_f32 && e.sm == sm &&
       e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
-      e.o.pair == o.pair && e.o.fuse == o.fuse) {
+      e.o.pair == o.pair && e.o.fuse == o.fuse && e.o.stream_k == o.stream_k && e.o.ffma == o.ffma) {
     *plan = e.plan;
     return true;
   }

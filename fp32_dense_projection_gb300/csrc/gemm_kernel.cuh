@@ -67,6 +67,14 @@ struct GemmArgs {
   // > 1: launched as clusters of `splits` CTAs, one split tile per cluster and one
   // unit per CTA; the cluster sums its partials itself after the main loop
   int32_t cluster_fixup;
+  // > 0: a stream-K plan.  The sk_slots persistent slots (CTAs, or pairs) share the
+  // sk_work = tiles * nkb contraction blocks evenly: slot c takes the blocks
+  // [c * sk_work / sk_slots, (c + 1) * sk_work / sk_slots) of the tile-major order.
+  // A tile cut by a slot boundary is summed in pieces, one per slot that touches it
+  // (piece s of the tile from the s-th such slot, in block order), each an FP32
+  // partial in slot s of the tile's `splits` partial slots; whole tiles are stored.
+  int32_t sk_slots;
+  int64_t sk_work;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
@@ -169,6 +177,28 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, int u) {
   return r;
 }
 
+// Stream-K plans: the first block of slot c's range, the slot whose range holds
+// block x, and the j-th piece of slot c's range (false past its end).
+__device__ __forceinline__ int64_t sk_begin(const GemmArgs& a, int64_t c) { return c * a.sk_work / a.sk_slots; }
+__device__ __forceinline__ int sk_slot_of(const GemmArgs& a, int64_t x) {
+  int64_t c = x * a.sk_slots / a.sk_work;
+  while (c + 1 < a.sk_slots && sk_begin(a, c + 1) <= x) ++c;
+  while (c > 0 && sk_begin(a, c) > x) --c;
+  return static_cast<int>(c);
+}
+__device__ __forceinline__ bool sk_piece(const GemmArgs& a, int c, int j, Unit* w) {
+  const int64_t b = sk_begin(a, c), e = sk_begin(a, c + 1);
+  const int64_t tile = b / a.nkb + j, t0 = tile * a.nkb;
+  if (b >= e || t0 >= e) return false;
+  w->kb0 = static_cast<int>((b > t0 ? b : t0) - t0);
+  w->kb1 = static_cast<int>((e < t0 + a.nkb ? e : t0 + a.nkb) - t0);
+  w->split = !(w->kb0 == 0 && w->kb1 == a.nkb);
+  w->s = c - sk_slot_of(a, t0);  // the tile's first piece comes from the slot holding its block 0
+  w->ptile = static_cast<int>(tile);
+  tile_coords(a, static_cast<int>(tile), &w->b, &w->tm, &w->tn);
+  return true;
+}
+
 // Output of batch b.
 __device__ __forceinline__ void* out_at(const GemmArgs& a, int b) {
   return static_cast<char*>(a.out) + static_cast<int64_t>(b) * a.out_bstride * (a.out_f32 ? 4 : 2);
@@ -212,6 +242,24 @@ __device__ __forceinline__ UnitRef unit_ref(int u, const GemmArgs& a0, const CUt
                                             const SecondProblem<true>& s) {
   if (u < a0.units) return {&a0, &mA, &mB, u};
   return {&s.args, &s.tmA, &s.tmB, u - a0.units};
+}
+
+// The k-th unit of the CTA (or pair) in slot `slot`: units slot, slot + step, ... of
+// the launch's list, or the pieces of the slot's block range in a stream-K plan.
+// False past the last one.
+template <bool DUAL>
+__device__ __forceinline__ bool slot_unit(int k, int slot, int step, int total, const GemmArgs& args,
+                                          const CUtensorMap& mA, const CUtensorMap& mB,
+                                          const SecondProblem<DUAL>& sec, UnitRef* ur, Unit* w) {
+  if (!DUAL && args.sk_slots > 0) {
+    *ur = {&args, &mA, &mB, 0};
+    return sk_piece(args, slot, k, w);
+  }
+  const int u = slot + k * step;
+  if (u >= total) return false;
+  *ur = unit_ref(u, args, mA, mB, sec);
+  *w = decode_unit(*ur->a, ur->u);
+  return true;
 }
 
 // Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
@@ -609,11 +657,12 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
       if (!X3) pdl_wait();  // the previous kernel on the stream (launched as its dependent) is done
-      for (int u = unit0; !X3 && ok && u < total_units; u += unit_step) {
-        const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
+      for (int k = 0; !X3 && ok; ++k) {
+        UnitRef ur;
+        Unit w;
+        if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
         const GemmArgs& ga = *ur.a;
         const bool a_mn = DUAL ? ga.a_mn != 0 : A_MN;
-        const Unit w = decode_unit(ga, ur.u);
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -693,9 +742,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int u = unit0; ok && u < total_units; u += unit_step, ++local) {
-        const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
-        const Unit w = decode_unit(*ur.a, ur.u);
+      for (int k = 0; ok; ++k, ++local) {
+        UnitRef ur;
+        Unit w;
+        if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
         const bool a_mn = DUAL ? ur.a->a_mn != 0 : A_MN;
         const uint32_t idesc = (DUAL && a_mn) ? IDESC_AMN : IDESC;
         const int kb0 = w.kb0, kb1 = w.kb1;
@@ -877,10 +927,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           mbar_arrive(tempty_bar(a));
       }
     };
-    for (int u = unit0; u < total_units; u += unit_step, ++local) {
-      const UnitRef ur = unit_ref(u, args, tmA, tmB, second);
+    for (int k = 0;; ++k, ++local) {
+      UnitRef ur;
+      Unit w;
+      if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
       const GemmArgs& ga = *ur.a;
-      const Unit w = decode_unit(ga, ur.u);
       const int tm = w.tm, tn = w.tn;
       const int slot = w.ptile * (PAIR ? 2 : 1) + static_cast<int>(rank);  // this CTA's partial slot
       const int acc = local & 1;

@@ -173,11 +173,49 @@ struct Choice {
   double t = 0.0;
   Tiling tiling = {256, false};
   int64_t splits = 1, full = 0;
+  bool stream_k = false;
 };
+
+// Stream-K pieces: the slots' block ranges [c W / G, (c + 1) W / G) over the tiles'
+// nkb blocks each; per tile, how many slots' ranges touch it.  Returns the most
+// pieces of one tile and the total (pieces[] optional).
+int64_t stream_k_pieces(int64_t tiles, int64_t nkb, int64_t slots, int64_t* total) {
+  const int64_t work = tiles * nkb;
+  std::vector<int64_t> pieces(static_cast<size_t>(tiles), 0);
+  for (int64_t c = 0; c < slots; ++c) {
+    const int64_t b = c * work / slots, e = (c + 1) * work / slots;
+    if (b >= e) continue;
+    for (int64_t t = b / nkb; t <= (e - 1) / nkb; ++t) ++pieces[static_cast<size_t>(t)];
+  }
+  int64_t most = 0, sum = 0;
+  for (int64_t p : pieces) {
+    most = std::max(most, p);
+    sum += p;
+  }
+  if (total) *total = sum;
+  return most;
+}
+
+// Modelled time of a stream-K plan: every slot sums ceil(W / G) blocks (the pieces of
+// one or two tiles) and writes up to two FP32 partial tiles; then the reduction
+// kernel adds the cut tiles' pieces.
+double stream_k_model_ns(const View& v, const Tiling& t, int64_t tiles, int64_t nkb, int sm, int out_bytes) {
+  const int64_t slots = t.pair ? sm / 2 : sm;
+  const int64_t per_slot = ceil_div(tiles * nkb, slots);
+  const int64_t active_sms = slots * (t.pair ? 2 : 1);
+  const double reuse = reuse_of(v, t);
+  const double a_rows = static_cast<double>(std::min<int64_t>(kBlockM, v.gm));
+  const double partial = a_rows * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0;
+  const double dram = std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(active_sms));
+  double time = unit_ns(v, t, per_slot, true, active_sms, reuse, out_bytes) + partial / dram;
+  const double unique = static_cast<double>(v.batch) * (v.gm * v.a_elem + v.gn * v.b_elem) * v.gk;
+  time = std::max(time, (unique + static_cast<double>(v.batch) * v.gm * v.gn * out_bytes) / kHbmBytesPerNs);
+  return time + kReduceNs + 2.0 * slots * (t.pair ? 2 : 1) * partial / kReduceBytesPerNs;
+}
 
 // Best (tiling, split count, whole-K prefix) for one contraction view.
 void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& o, Choice* best) {
-  auto consider = [&](const Tiling& t, int64_t full, int64_t s, double time) {
+  auto consider = [&](const Tiling& t, int64_t full, int64_t s, double time, bool sk = false) {
     // prefer earlier candidates (single CTA, wider tiles, fewer splits) on near-ties
     if (!best->have || time < best->t * 0.99) {
       best->have = true;
@@ -185,6 +223,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       best->tiling = t;
       best->splits = s;
       best->full = full;
+      best->stream_k = sk;
     }
   };
   for (int pair = 0; pair < 2; ++pair) {
@@ -207,14 +246,26 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       const int64_t min_s = cta_tiles > kMaxSplitTiles ? 1 : ceil_div(nkb, max_blocks);
       const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(nkb, 64));
       // every tile split the same way (s = 1: whole K per tile)
-      for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0; ++s) {
+      for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0 && o.stream_k != 1; ++s) {
         if (o.splits > 0 && s != std::min<int64_t>(o.splits, nkb)) continue;
         if (o.splits <= 0 && s > min_s && tiles * s > 4LL * slots) break;  // beyond 4 waves never pays
         if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // bounded partial workspace
         consider(t, s == 1 ? tiles : 0, s, model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes));
       }
+      // Stream-K, for tile counts that fit in one wave: every slot takes an even share
+      // of all tiles' blocks, so no SM idles while others finish a wider split.  (More
+      // tiles keep the raster-ordered waves, whose neighbouring tiles share operands in
+      // L2.)  Each piece stays within the accumulation bound; BF16 operands only.
+      const int64_t per_slot = ceil_div(tiles * nkb, slots);
+      if (o.stream_k != 0 && v.terms == 1 && o.splits <= 0 && o.tail_splits <= 0 && tiles <= slots &&
+          tiles * nkb >= 2 * slots && std::min(per_slot, nkb) <= max_blocks) {
+        const int64_t most = stream_k_pieces(tiles, nkb, slots, nullptr);
+        if (most >= 2 && cta_tiles * most <= kMaxSplitTiles) {
+          consider(t, 0, most, stream_k_model_ns(v, t, tiles, nkb, sm, out_bytes), true);
+        }
+      }
       // whole-K tiles for the full waves, the last partial wave's tiles split
-      if (min_s == 1 && o.splits <= 0 && tiles > slots && tiles % slots != 0) {
+      if (o.stream_k != 1 && min_s == 1 && o.splits <= 0 && tiles > slots && tiles % slots != 0) {
         const int64_t full = tiles / slots * slots;
         if ((tiles - full) * (pair ? 2 : 1) <= kMaxSplitTiles) {
           for (int64_t s = 2; s <= std::min<int64_t>(nkb, 16); ++s)
@@ -342,6 +393,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.bm = static_cast<int>(c.tiling.rows());
   plan.bn = c.tiling.bn;
   plan.splits = static_cast<int>(c.splits);
+  plan.stream_k = c.stream_k;
   plan.stages = v.terms > 1 ? stages_x3(plan.bn, plan.pair) : stages_for(plan.bn, plan.pair);
   plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
@@ -349,13 +401,19 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   const int64_t tiles = plan.tiles;
   plan.full_units = (v.gm > 0 && plan.nkb > 0) ? c.full : tiles;
   plan.units = plan.full_units + (tiles - plan.full_units) * plan.splits;
+  const int64_t slots_all = plan.pair ? sm / 2 : sm;
+  if (plan.stream_k) {  // units: every piece of every slot's block range
+    stream_k_pieces(tiles, plan.nkb, slots_all, &plan.units);
+    plan.full_units = 0;
+  }
   // Group along the dimension whose operand is larger, so the tiles that share
   // its blocks run in the same wave and it crosses from DRAM about once.
   plan.raster_m = v.gn > v.gm;
   plan.group = static_cast<int>(
       std::max<int64_t>(1, std::min<int64_t>(16, plan.raster_m ? plan.tiles_m : plan.tiles_n)));
-  const int64_t slots = plan.pair ? sm / 2 : sm;
-  plan.grid = static_cast<int>(std::min<int64_t>(plan.units, slots) * (plan.pair ? 2 : 1));
+  // (stream-K: every slot, each with its share of the blocks)
+  plan.grid = static_cast<int>((plan.stream_k ? slots_all : std::min<int64_t>(plan.units, slots_all)) *
+                               (plan.pair ? 2 : 1));
 
   // workspace layout: [split partials | router's pre-split operands]
   size_t off = 0;

@@ -72,6 +72,11 @@ struct Plan {
   // view is the plain contraction (input gradient over N, weight gradient unswapped),
   // nkb counts its contraction chunks of bk = 4096 / bn elements.
   bool ffma = false;
+  // Stream-K: the grid's slots share the tiles' blocks evenly (slot c takes blocks
+  // [c W / G, (c + 1) W / G) of the tile-major order, W = tiles * nkb); a tile cut by
+  // slot boundaries is summed in pieces, up to `splits` of them, whose FP32 partials
+  // the reduction adds in block order.  units = the pieces of all slots.
+  bool stream_k = false;
 };
 
 // Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows
@@ -115,6 +120,7 @@ struct Overrides {
   // 2 / 3 the same with the weight / input gradient's units first
   int fuse = -1;
   int ffma = -1;  // router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
+  int stream_k = -1;  // 0 never, 1 only stream-K candidates (where the shape admits one)
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,

@@ -1,7 +1,8 @@
 // Ordered reduction of split partial tiles.
 //
 // A plan that splits a tile's contraction into `splits` contiguous ranges has the
-// GEMM write one FP32 partial tile per range.  This kernel, launched right behind
+// GEMM write one FP32 partial tile per range (a stream-K plan: one per slot whose
+// block range cuts the tile, however many that is for each tile).  This kernel, launched right behind
 // the GEMM on the same stream, adds them for every output element in ascending
 // range order (p_0 + p_1 + ... + p_{S-1}, FP32) and rounds the sum once to the
 // output type.  The order depends on nothing but the plan, so the result is
@@ -46,6 +47,14 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
   const int chunk = slice % ra.chunks;
   const int slot = slice / ra.chunks;
   const int ptile = slot / ra.slots_per_tile, rank = slot - ptile * ra.slots_per_tile;
+  // partials to add: the plan's split count, or for a stream-K plan the number of
+  // slots whose block ranges touch this tile (one: the GEMM stored the tile whole)
+  int nparts = a.splits;
+  if (a.sk_slots > 0) {
+    const int64_t t0 = static_cast<int64_t>(ptile) * a.nkb;
+    nparts = sk_slot_of(a, t0 + a.nkb - 1) - sk_slot_of(a, t0) + 1;
+    if (nparts < 2) return;
+  }
   int bt, tm, tn;
   tile_coords(a, a.full_units + ptile, &bt, &tm, &tn);
   void* out = out_at(a, bt);
@@ -58,14 +67,14 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
                       static_cast<size_t>(chunk * 8 + j) * kBlockM + row;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // splits in ascending order: acc = p_0, then acc += p_s
-  for (int s0 = 0; s0 < a.splits; s0 += kReduceBatch) {
+  for (int s0 = 0; s0 < nparts; s0 += kReduceBatch) {
     float4 x[kReduceBatch];
 #pragma unroll
     for (int k = 0; k < kReduceBatch; ++k)
-      if (s0 + k < a.splits) x[k] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride);
+      if (s0 + k < nparts) x[k] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride);
 #pragma unroll
     for (int k = 0; k < kReduceBatch; ++k)
-      if (s0 + k < a.splits) {
+      if (s0 + k < nparts) {
         if (s0 + k == 0) {
           acc = x[k];
         } else {

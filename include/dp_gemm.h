@@ -267,7 +267,8 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * (0 / 1: single-CTA or CTA-pair tiles), DP_FORCE_CLUSTER_SUM=0 (sum split
  * partials in the reduction kernel instead of inside the GEMM's clusters; the
  * two give the same bits), DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls
- * or as one co-scheduled launch, see dp_gemm_bwd).  A forced plan is still deterministic and keeps the
+ * or as one co-scheduled launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never;
+ * 1: a stream-K plan where the shape admits one).  A forced plan is still deterministic and keeps the
  * accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of
@@ -287,7 +288,11 @@ typedef struct dp_plan_info {
                                  stored transposed into dW */
     int32_t cta_pair;         /* 1: tiles of 256 rows shared by a cluster of two CTAs */
     int32_t raster_rows;      /* 1: raster groups of row tiles, rows fastest */
-    int32_t reserved;
+    int32_t stream_k;         /* 1: the grid's slots share all tiles' contraction blocks evenly
+                                 (slot c takes blocks [c W / grid_slots, (c + 1) W / grid_slots)
+                                 of the tile-major order, W = tiles * k_blocks); a tile cut by
+                                 slot boundaries is summed from up to `splits` pieces in block
+                                 order; units counts the pieces */
     int64_t gemm_m;           /* output rows of the contraction */
     int64_t gemm_n;           /* output columns */
     int64_t gemm_k;           /* contraction length (3N for the router's input gradient,

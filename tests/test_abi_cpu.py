@@ -383,3 +383,28 @@ def test_router_program_overrides(monkeypatch):
     monkeypatch.delenv("DP_FORCE_BN")
     monkeypatch.delenv("DP_FORCE_SPLITS")
     assert dp.plan("router_dgrad", 64, 256, 4096, sm_count=SM)["program"] == 0
+
+
+# ------------------------------------------------------------------ stream-K plans
+
+@pytest.mark.parametrize("op,T,N,K", [("wgrad", 16173, 64, 4096), ("wgrad", 1025, 128, 4096), ("fwd", 1000, 136, 4096)])
+def test_stream_k_plan(monkeypatch, op, T, N, K):
+    # forced: every slot of the grid, splits = the most pieces one tile is cut into,
+    # units = all pieces, a partial slot per piece in the workspace
+    monkeypatch.setenv("DP_FORCE_STREAM_K", "1")
+    p = dp.plan(op, T, N, K, sm_count=SM)
+    per = 2 if p["cta_pair"] else 1
+    slots = SM // per
+    tiles = p["tiles_m"] * p["tiles_n"]
+    assert p["stream_k"] == 1 and p["grid"] == slots * per and p["full_units"] == 0 and tiles <= slots
+    W = tiles * p["k_blocks"]
+    counts = [0] * tiles
+    for c in range(slots):
+        b, e = c * W // slots, (c + 1) * W // slots
+        for t in range(b // p["k_blocks"], (e - 1) // p["k_blocks"] + 1):
+            counts[t] += 1
+    assert p["splits"] == max(counts) >= 2 and p["units"] == sum(counts)
+    assert p["workspace_bytes"] >= tiles * per * p["splits"] * 128 * p["block_n"] * 4
+    # the planner's own choice for these shapes is not stream-K (measured slower on GB300)
+    monkeypatch.delenv("DP_FORCE_STREAM_K")
+    assert dp.plan(op, T, N, K, sm_count=SM)["stream_k"] == 0

@@ -50,7 +50,7 @@ class PlanInfo(ctypes.Structure):
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
         ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double),
         ("batch", ctypes.c_int64), ("tiles", ctypes.c_int64), ("weight_kn", ctypes.c_int32),
-        ("program", ctypes.c_int32)]
+        ("program", ctypes.c_int32), ("atomic", ctypes.c_int32), ("reserved3", ctypes.c_int32)]
 
 
 class BwdPlanInfo(ctypes.Structure):
@@ -81,6 +81,7 @@ def lib():
             getattr(L, name).argtypes = [P, P, P] + rtail
             getattr(L, name + "_ex").argtypes = [P, I, P, I, P, I] + rtail
         L.dp_plan_query.argtypes = [S, I, I, I, S, S, ctypes.POINTER(PlanInfo)]
+        L.dp_plan_query_ex.argtypes = [S, I, I, I, S, S, S, ctypes.POINTER(PlanInfo)]
         L.dp_plan_query_batched.argtypes = [S, I, I, I, I, S, S, S, ctypes.POINTER(PlanInfo)]
         L.dp_workspace_size_batched.argtypes = [S, I, I, I, I, S, S, S, ctypes.POINTER(ctypes.c_size_t)]
         btail = [I, I, I, I, S, S, P, Z, P]      # B T N K out deterministic ws ws_bytes stream
@@ -112,12 +113,13 @@ def _check(status: int, what: str):
         raise DPError(status, what)
 
 
-def plan(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0) -> dict:
-    """The library's plan for a call (pure function of the shape and SM count)."""
+def plan(op, T: int, N: int, K: int, out_f32: bool = False, sm_count: int = 0, deterministic: bool = True) -> dict:
+    """The library's plan for a call (pure function of the shape, SM count and the
+    deterministic flag)."""
     op = OP_NAMES.get(op, op)
     info = PlanInfo()
-    _check(lib().dp_plan_query(int(op), T, N, K, int(bool(out_f32)), int(sm_count), ctypes.byref(info)),
-           "dp_plan_query")
+    _check(lib().dp_plan_query_ex(int(op), T, N, K, int(bool(out_f32)), int(bool(deterministic)), int(sm_count),
+                                  ctypes.byref(info)), "dp_plan_query_ex")
     return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if not name.startswith("reserved")}
 
 

@@ -226,7 +226,7 @@ int env_int(const char* name) {
 // tiles).  Unset in normal use.
 struct PlanEntry {
   bool valid = false;
-  int op, out_f32, sm, w_kn;
+  int op, out_f32, sm, w_kn, det;
   int64_t T, N, K, batch;
   Overrides o;
   Plan plan;
@@ -234,7 +234,8 @@ struct PlanEntry {
 thread_local PlanEntry t_plans[kPlanCacheSize];
 
 bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan, int64_t batch = 1,
-              int w_kn = 0) {
+              int w_kn = 0, int deterministic = 1) {
+  deterministic = deterministic ? 1 : 0;
   const char* sw = std::getenv("DP_FORCE_SWAP");
   const char* pr = std::getenv("DP_FORCE_PAIR");
   Overrides o;
@@ -247,22 +248,25 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
   o.ffma = ff ? std::atoi(ff) : -1;
   const char* sk = std::getenv("DP_FORCE_STREAM_K");
   o.stream_k = sk ? std::atoi(sk) : -1;
+  const char* at = std::getenv("DP_FORCE_ATOMIC");
+  o.atomic = at ? std::atoi(at) : -1;
   uint64_t h = mix(mix(mix(static_cast<uint64_t>(op), static_cast<uint64_t>(T)), static_cast<uint64_t>(N)),
                    static_cast<uint64_t>(K));
   h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
               (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919 +
-              static_cast<uint64_t>(o.stream_k + 1) * 104729);
-  h = mix(h, static_cast<uint64_t>(batch) * 2 + static_cast<uint64_t>(w_kn));
+              static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.atomic + 1) * 1299709);
+  h = mix(h, static_cast<uint64_t>(batch) * 4 + static_cast<uint64_t>(w_kn) * 2 + static_cast<uint64_t>(deterministic));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
-      e.batch == batch && e.w_kn == w_kn && e.o.bn == o.bn && e.o.splits == o.splits &&
+      e.batch == batch && e.w_kn == w_kn && e.det == deterministic && e.o.bn == o.bn && e.o.splits == o.splits &&
       e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma &&
-      e.o.stream_k == o.stream_k) {
+      e.o.stream_k == o.stream_k && e.o.atomic == o.atomic) {
     *plan = e.plan;
     return true;
   }
-  if (!make_plan(op, T, N, K, out_f32, sm, plan, o, batch, w_kn != 0)) return false;
+  if (!make_plan(op, T, N, K, out_f32, sm, plan, o, batch, w_kn != 0, deterministic != 0)) return false;
+  e.det = deterministic;
   e.batch = batch;
   e.w_kn = w_kn;
   e.valid = true;
@@ -300,7 +304,8 @@ std::mutex g_cluster_mutex;
 std::vector<std::pair<ClusterKey, int>> g_cluster_capacity;
 
 int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
-  if (p.pair || p.stream_k || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid) return 0;
+  if (p.pair || p.stream_k || p.atomic || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid)
+    return 0;
   const char* off = std::getenv("DP_FORCE_CLUSTER_SUM");  // "0": always the reduction kernel (tests)
   if (off && std::atoi(off) == 0) return 0;
   int cur = 0;
@@ -387,6 +392,7 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   a.b3d = b3d ? 1 : 0;
   a.a_mn = p.a_mn ? 1 : 0;
   a.sk_slots = p.stream_k ? p.grid / (p.pair ? 2 : 1) : 0;
+  a.atomic = p.atomic ? 1 : 0;
   a.sk_work = p.tiles * p.nkb;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -422,7 +428,7 @@ dp_status launch_view(const Plan& p, const DeviceState& dev, const void* A, int6
   // split tiles: the ordered sum of their partials, queued behind the GEMM (unless
   // the GEMM's clusters sum them themselves)
   const int64_t split_tiles = p.tiles - p.full_units;
-  if (e == cudaSuccess && p.splits > 1 && split_tiles > 0 && a.cluster_fixup <= 1)
+  if (e == cudaSuccess && p.splits > 1 && split_tiles > 0 && a.cluster_fixup <= 1 && !p.atomic)
     e = launch_split_reduce(l, p.bn, p.pair, split_tiles, stream);
   return e == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
 }
@@ -451,7 +457,8 @@ void op_shapes(int op, int64_t T, int64_t N, int64_t K, int64_t* ra, int64_t* ca
 }
 
 dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb, void* out, int64_t ldo, int64_t T,
-                 int64_t N, int64_t K, int out_f32, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                 int64_t N, int64_t K, int out_f32, void* ws, size_t ws_bytes, cudaStream_t stream,
+                 int deterministic = 1) {
   const bool router = op >= kOpRouterFwd;
   if (!router && out_f32 != DP_OUT_BF16 && out_f32 != DP_OUT_F32) return DP_ERR_INVALID_ARG;
   dp_status st = check_sizes(T, N, K, op);
@@ -472,11 +479,14 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
     return DP_OK;
   }
   Plan p;
-  if (!plan_for(op, T, N, K, out_size == 4 ? 1 : 0, dev->sm_count, &p)) return DP_ERR_INVALID_ARG;
+  if (!plan_for(op, T, N, K, out_size == 4 ? 1 : 0, dev->sm_count, &p, 1, 0, deterministic))
+    return DP_ERR_INVALID_ARG;
   if (p.ws_bytes > 0 && (ws == nullptr || ws_bytes < p.ws_bytes)) return DP_ERR_WORKSPACE;
   if (p.ws_bytes > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
 
   if (!router) {
+    // non-deterministic split sums add into the output: zero it first
+    if (p.atomic && (st = zero_output(out, ro, co, ldo, 4, stream)) != DP_OK) return st;
     if (p.swap) return launch_view(p, *dev, b, ldb, a, lda, nullptr, out, ldo, ws, stream);  // A = X, B = dY
     return launch_view(p, *dev, a, lda, b, ldb, nullptr, out, ldo, ws, stream);
   }
@@ -518,7 +528,10 @@ dp_status run_op(int op, const void* a, int64_t lda, const void* b, int64_t ldb,
     jobs[1] = {static_cast<const float*>(b), sb, N, K, ldb, p.ld_split_b, N * p.ld_split_b, 3, 0x2u};
     njobs = 2;
   }
-  if (launch_split_x3(jobs, njobs, dev->sm_count, stream) != cudaSuccess) return DP_ERR_LAUNCH;
+  // (non-deterministic split sums add into the output: the split kernel zeroes it too)
+  ZeroJob zero = {static_cast<float*>(out), ro, co, ldo};
+  if (launch_split_x3(jobs, njobs, dev->sm_count, stream, p.atomic ? &zero : nullptr) != cudaSuccess)
+    return DP_ERR_LAUNCH;
   if (op == kOpRouterFwd)  // A = X (FP32), B = W planes
     return launch_view(p, *dev, a, lda, sb, p.ld_split_b, sb + N * p.ld_split_b, out, ldo, ws, stream);
   if (op == kOpRouterWgrad)  // dW^T = X^T dY: A = X (FP32), B = dY planes; stored transposed
@@ -554,6 +567,7 @@ void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
   info->tiles = p.tiles;
   info->program = p.ffma ? 1 : 0;
   info->stream_k = p.stream_k ? 1 : 0;
+  info->atomic = p.atomic ? 1 : 0;
   info->model_us = p.model_ns * 1e-3;
 }
 
@@ -665,7 +679,7 @@ bool bwd_plan_for(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int s
 // one co-scheduled launch over both problems' whole-K tiles.
 dp_status run_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const void* W, int64_t ldw, void* dX,
                   int64_t ld_dx, int dx_f32, void* dW, int64_t ld_dw, int dw_f32, int64_t T, int64_t N, int64_t K,
-                  void* ws, size_t ws_bytes, cudaStream_t stream) {
+                  void* ws, size_t ws_bytes, cudaStream_t stream, int deterministic) {
   if ((dx_f32 != DP_OUT_BF16 && dx_f32 != DP_OUT_F32) || (dw_f32 != DP_OUT_BF16 && dw_f32 != DP_OUT_F32))
     return DP_ERR_INVALID_ARG;
   dp_status st = check_sizes(T, N, K, kOpDgrad);
@@ -683,9 +697,9 @@ dp_status run_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const
   if (bp.ws_bytes > 0 && T > 0 && (ws == nullptr || ws_bytes < bp.ws_bytes)) return DP_ERR_WORKSPACE;
   if (bp.ws_bytes > 0 && T > 0 && !aligned16(ws)) return DP_ERR_ALIGNMENT;
   if (!bp.fused) {
-    st = run_op(kOpDgrad, dY, ldg, W, ldw, dX, ld_dx, T, N, K, dx_f32, ws, ws_bytes, stream);
+    st = run_op(kOpDgrad, dY, ldg, W, ldw, dX, ld_dx, T, N, K, dx_f32, ws, ws_bytes, stream, deterministic);
     if (st != DP_OK) return st;
-    return run_op(kOpWgrad, dY, ldg, X, ldx, dW, ld_dw, T, N, K, dw_f32, ws, ws_bytes, stream);
+    return run_op(kOpWgrad, dY, ldg, X, ldx, dW, ld_dw, T, N, K, dw_f32, ws, ws_bytes, stream, deterministic);
   }
   GemmLaunch ld, lw;
   st = prepare_view(bp.dgrad, *dev, dY, ldg, W, ldw, nullptr, dX, ld_dx, nullptr, 0, 0, 0, &ld);
@@ -723,9 +737,8 @@ extern "C" {
 dp_status dp_gemm_fwd_ex(const void* X, int64_t ldx, const void* W, int64_t ldw, void* Y, int64_t ldy, int64_t T,
                          int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
                          size_t workspace_bytes, dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpFwd, X, ldx, W, ldw, Y, ldy, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status dp_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
@@ -736,9 +749,8 @@ dp_status dp_gemm_fwd(const void* X, const void* W, void* Y, int64_t T, int64_t 
 dp_status dp_gemm_dgrad_ex(const void* dY, int64_t ldg, const void* W, int64_t ldw, void* dX, int64_t ldx, int64_t T,
                            int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
                            size_t workspace_bytes, dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpDgrad, dY, ldg, W, ldw, dX, ldx, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status dp_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
@@ -749,9 +761,8 @@ dp_status dp_gemm_dgrad(const void* dY, const void* W, void* dX, int64_t T, int6
 dp_status dp_gemm_wgrad_ex(const void* dY, int64_t ldg, const void* X, int64_t ldx, void* dW, int64_t ldw, int64_t T,
                            int64_t N, int64_t K, dp_out_dtype out, int deterministic, void* workspace,
                            size_t workspace_bytes, dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpWgrad, dY, ldg, X, ldx, dW, ldw, T, N, K, static_cast<int>(out), workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status dp_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
@@ -762,9 +773,8 @@ dp_status dp_gemm_wgrad(const void* dY, const void* X, void* dW, int64_t T, int6
 dp_status router_fwd_ex(const float* X, int64_t ldx, const float* W, int64_t ldw, float* Y, int64_t ldy, int64_t T,
                         int64_t N, int64_t K, int deterministic, void* workspace, size_t workspace_bytes,
                         dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpRouterFwd, X, ldx, W, ldw, Y, ldy, T, N, K, 1, workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status router_fwd(const float* X, const float* W, float* Y, int64_t T, int64_t N, int64_t K, int deterministic,
@@ -775,9 +785,8 @@ dp_status router_fwd(const float* X, const float* W, float* Y, int64_t T, int64_
 dp_status router_dgrad_ex(const float* dY, int64_t ldg, const float* W, int64_t ldw, float* dX, int64_t ldx,
                           int64_t T, int64_t N, int64_t K, int deterministic, void* workspace,
                           size_t workspace_bytes, dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpRouterDgrad, dY, ldg, W, ldw, dX, ldx, T, N, K, 1, workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status router_dgrad(const float* dY, const float* W, float* dX, int64_t T, int64_t N, int64_t K,
@@ -788,9 +797,8 @@ dp_status router_dgrad(const float* dY, const float* W, float* dX, int64_t T, in
 dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t ldx, float* dW, int64_t ldw,
                           int64_t T, int64_t N, int64_t K, int deterministic, void* workspace,
                           size_t workspace_bytes, dp_stream stream) {
-  (void)deterministic;
   return run_op(kOpRouterWgrad, dY, ldg, X, ldx, dW, ldw, T, N, K, 1, workspace, workspace_bytes,
-                static_cast<cudaStream_t>(stream));
+                static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status router_wgrad(const float* dY, const float* X, float* dW, int64_t T, int64_t N, int64_t K,
@@ -800,6 +808,11 @@ dp_status router_wgrad(const float* dY, const float* X, float* dW, int64_t T, in
 
 dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int sm_count,
                         dp_plan_info* info) {
+  return dp_plan_query_ex(op, T, N, K, out, 1, sm_count, info);
+}
+
+dp_status dp_plan_query_ex(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                           int sm_count, dp_plan_info* info) {
   if (!info || static_cast<int>(op) < 0 || static_cast<int>(op) > kOpRouterWgrad) return DP_ERR_INVALID_ARG;
   const dp_status st = check_sizes(T, N, K, static_cast<int>(op));
   if (st != DP_OK) return st;
@@ -811,7 +824,8 @@ dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype 
   }
   const bool router = static_cast<int>(op) >= kOpRouterFwd;
   Plan p;
-  if (!plan_for(static_cast<int>(op), T, N, K, (router || out == DP_OUT_F32) ? 1 : 0, sm_count, &p))
+  if (!plan_for(static_cast<int>(op), T, N, K, (router || out == DP_OUT_F32) ? 1 : 0, sm_count, &p, 1, 0,
+                deterministic))
     return DP_ERR_INVALID_ARG;
   fill_info(p, T, info);
   return DP_OK;
@@ -888,9 +902,8 @@ dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, c
                       int64_t ld_dx, dp_out_dtype out_dx, void* dW, int64_t ld_dw, dp_out_dtype out_dw, int64_t T,
                       int64_t N, int64_t K, int deterministic, void* workspace, size_t workspace_bytes,
                       dp_stream stream) {
-  (void)deterministic;
   return run_bwd(dY, ldg, X, ldx, W, ldw, dX, ld_dx, static_cast<int>(out_dx), dW, ld_dw, static_cast<int>(out_dw),
-                 T, N, K, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+                 T, N, K, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), deterministic);
 }
 
 dp_status dp_plan_query_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx, dp_out_dtype out_dw, int sm_count,
@@ -965,6 +978,6 @@ const char* dp_status_string(dp_status status) {
   }
 }
 
-int dp_version(void) { return 120; }
+int dp_version(void) { return 130; }
 
 }  // extern "C"

@@ -75,6 +75,10 @@ struct GemmArgs {
   // partial in slot s of the tile's `splits` partial slots; whole tiles are stored.
   int32_t sk_slots;
   int64_t sk_work;
+  // 1 (non-deterministic plans, FP32 output): split units add their FP32 partial
+  // into the output, which the launch zero-filled, with atomic adds; no partials
+  // and no reduction.  The order of the adds, and so the last bits, vary by run.
+  int32_t atomic;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
@@ -364,6 +368,37 @@ __device__ __forceinline__ void store_block32(const GemmArgs& a, void* out, uint
   }
   stage_block32(a, buf, lane, v);
   flush_block32(a, out, buf, lane, m0, col0);
+}
+
+// Non-deterministic split units: add a 32 x 32 FP32 block (lane i: row m0 + i,
+// columns [col0, col0 + 32)) into the zero-filled FP32 output.  Row-major outputs go
+// through the warp's shared-memory block, so each instruction adds whole 128-byte
+// row segments (16-byte vector atomics); the transposed output adds straight from
+// the registers (the lanes' rows are consecutive elements).
+__device__ __forceinline__ void add_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
+                                            int64_t col0, const float (&v)[32]) {
+  float* o = static_cast<float*>(out);
+  if (a.out_trans) {
+    const int64_t m = m0 + lane;
+    if (m >= a.gm) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < a.gn) atomicAdd(o + (col0 + j) * a.ldo + m, v[j]);
+    return;
+  }
+  stage_block32(a, buf, lane, v);
+  const int64_t rows_left = a.gm - m0;
+  const int ch = lane & 7, r0 = lane >> 3;
+  const bool col_ok = col0 + 4 * ch < a.gn;
+  float* p = o + (m0 + r0) * a.ldo + col0 + 4 * ch;
+#pragma unroll
+  for (int i = 0; i < 8; ++i, p += 4 * a.ldo) {
+    const int r = 4 * i + r0;
+    const uint4 x = ld_shared_u4(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+    if (col_ok && r < rows_left)
+      atomicAdd(reinterpret_cast<float4*>(p),
+                make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)));
+  }
 }
 
 // In-kernel ordered sum for cluster plans: the S CTAs of a cluster computed the S
@@ -951,7 +986,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       void* outb = out_at(ga, w.b);
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
-      if (!w.split) {
+      if (!w.split || ga.atomic) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -961,7 +996,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
+          if (w.split)  // (non-deterministic plans: into the zero-filled output)
+            add_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
+          else
+            store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's
@@ -1032,7 +1070,14 @@ struct SplitJob {
   int32_t nseg;         // 2 or 3 segments
   uint32_t lo_mask;     // bit s set: segment s holds lo = RNE(x - hi), else hi = RNE(x)
 };
-cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream);
+// (zero, if not null: also zero-fill that FP32 [rows][cols] matrix, leading
+// dimension ld, in the same launch: the output of a non-deterministic router call)
+struct ZeroJob {
+  float* out;
+  int64_t rows, cols, ld;
+};
+cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream,
+                            const ZeroJob* zero = nullptr);
 // Small-T FP32 router program (router_ffma.cu): D[m][n] = sum_k A(m, k) B(n, k) on
 // FP32 operands with FP32 FMAs; 64 x bn tiles (bn 16 / 32 / 64), each tile's
 // contraction split over a cluster of `splits` CTAs (<= 8) whose partials are

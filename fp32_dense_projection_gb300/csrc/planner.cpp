@@ -37,6 +37,12 @@ constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter 
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 constexpr double kLaunchNs = 3000.0;          // a launch's fixed cost: setup, first loads, last tile's epilogue
+// Non-deterministic atomic split sums: the zero fill's fixed cost (a memset node
+// before the GEMM; for the router, a job of its operand-split kernel, nearly free),
+// and the rate of FP32 atomic adds into L2
+constexpr double kZeroMemsetNs = 2500.0;
+constexpr double kZeroInSplitNs = 300.0;
+constexpr double kAtomicBytesPerNs = 3000.0;
 // SIMT FP32 router program, measured on GB300: FMAs one SM sustains (~51% of 4 x 32
 // lanes at ~1.9 GHz: its shared-memory reads match the FMA pipe's rate), the
 // launch's fixed cost, each wave's fixed cost (first loads from DRAM, the group and
@@ -59,6 +65,7 @@ struct View {
   int terms = 1;       // MMAs per contraction element (3 for the router's BF16x3)
   int bk = kBlockK;    // contraction block (32 for the router's fused split)
   int64_t batch = 1;   // independent GEMMs of this view
+  bool zero_in_split = false;  // router: its operand-split kernel can zero-fill the output
 };
 
 // w_kn: the weight (and the weight gradient) stored [K][N] instead of [N][K] (the
@@ -139,7 +146,10 @@ double reuse_of(const View& v, const Tiling& t) {
 // split `splits` ways, run by min(units, slots) persistent CTAs (or pairs); never
 // faster than the unique operand bytes cross from DRAM; split plans add the
 // reduction kernel that sums the partials.
-double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes) {
+// atomic_ok: the split sums may be atomic adds (taken if modelled faster, or always
+// with force_atomic); *atomic reports the choice.
+double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, int sm, int out_bytes,
+                bool atomic_ok = false, bool* atomic = nullptr, bool force_atomic = false) {
   const int64_t slots = t.pair ? sm / 2 : sm;
   const int64_t tiles = v.batch * ceil_div(v.gm, t.rows()) * ceil_div(v.gn, t.bn);
   const int64_t nkb = std::max<int64_t>(1, ceil_div(v.gk, v.bk));
@@ -157,13 +167,24 @@ double model_ns(const View& v, const Tiling& t, int64_t full, int64_t splits, in
             unit_ns(v, t, ceil_div(nkb, splits), splits > 1, active_sms, reuse, out_bytes);
   const double t_dram = (unique + static_cast<double>(v.batch) * v.gm * v.gn * out_bytes) / kHbmBytesPerNs;
   time = std::max(time, t_dram);
+  if (atomic) *atomic = false;
   if (splits > 1 && split_units > 0) {  // every split tile's partials, summed in split order
     // by the GEMM's own clusters (single-CTA tiles, every tile split, one unit per
     // CTA) or else by the reduction kernel
     const bool in_cluster = !t.pair && full == 0 && splits <= kClusterSumMax && units <= slots;
-    time += (in_cluster ? kClusterSumNs : kReduceNs) +
-            static_cast<double>(tiles - full) * (t.pair ? 2 : 1) * splits * std::min<double>(kBlockM, a_rows) *
-                static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0 / kReduceBytesPerNs;
+    const double partial_bytes = static_cast<double>(tiles - full) * (t.pair ? 2 : 1) * splits *
+                                 std::min<double>(kBlockM, a_rows) *
+                                 static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * 4.0;
+    const double ordered = (in_cluster ? kClusterSumNs : kReduceNs) + partial_bytes / kReduceBytesPerNs;
+    // or, non-deterministic: atomic adds into the output after a zero fill of all of it
+    const double added = (v.zero_in_split ? kZeroInSplitNs : kZeroMemsetNs) + partial_bytes / kAtomicBytesPerNs +
+                         static_cast<double>(v.batch) * v.gm * v.gn * 4.0 / kHbmBytesPerNs;
+    if (atomic_ok && (force_atomic || added < ordered)) {
+      time += added;
+      if (atomic) *atomic = true;
+    } else {
+      time += ordered;
+    }
   }
   return time;
 }
@@ -174,6 +195,7 @@ struct Choice {
   Tiling tiling = {256, false};
   int64_t splits = 1, full = 0;
   bool stream_k = false;
+  bool atomic = false;
 };
 
 // Stream-K pieces: the slots' block ranges [c W / G, (c + 1) W / G) over the tiles'
@@ -214,7 +236,9 @@ double stream_k_model_ns(const View& v, const Tiling& t, int64_t tiles, int64_t 
 }
 
 // Best (tiling, split count, whole-K prefix) for one contraction view.
-void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& o, Choice* best) {
+void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& o, Choice* best,
+            bool atomic_ok = false) {
+  bool atomic = false;  // (set by the last model_ns call: its split sums are atomic)
   auto consider = [&](const Tiling& t, int64_t full, int64_t s, double time, bool sk = false) {
     // prefer earlier candidates (single CTA, wider tiles, fewer splits) on near-ties
     if (!best->have || time < best->t * 0.99) {
@@ -224,6 +248,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       best->splits = s;
       best->full = full;
       best->stream_k = sk;
+      best->atomic = !sk && atomic;
     }
   };
   for (int pair = 0; pair < 2; ++pair) {
@@ -250,7 +275,8 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
         if (o.splits > 0 && s != std::min<int64_t>(o.splits, nkb)) continue;
         if (o.splits <= 0 && s > min_s && tiles * s > 4LL * slots) break;  // beyond 4 waves never pays
         if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // bounded partial workspace
-        consider(t, s == 1 ? tiles : 0, s, model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes));
+        consider(t, s == 1 ? tiles : 0, s,
+                 model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes, atomic_ok, &atomic, o.atomic == 1));
       }
       // Stream-K, for tile counts that fit in one wave: every slot takes an even share
       // of all tiles' blocks, so no SM idles while others finish a wider split.  (More
@@ -270,7 +296,7 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
         if ((tiles - full) * (pair ? 2 : 1) <= kMaxSplitTiles) {
           for (int64_t s = 2; s <= std::min<int64_t>(nkb, 16); ++s)
             if (o.tail_splits <= 0 || s == o.tail_splits)
-              consider(t, full, s, model_ns(v, t, full, s, sm, out_bytes));
+              consider(t, full, s, model_ns(v, t, full, s, sm, out_bytes, atomic_ok, &atomic, o.atomic == 1));
         }
       }
     }
@@ -341,12 +367,13 @@ double fused_model_ns(const Plan& first, const Plan& second, int sm) {
 }  // namespace
 
 bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* p, const Overrides& o,
-               int64_t batch, bool w_kn) {
+               int64_t batch, bool w_kn, bool deterministic) {
   if (!p || sm < 1 || T < 0 || N < 1 || K < 1 || batch < 1) return false;
   if ((batch > 1 || w_kn) && op >= kOpRouterFwd) return false;  // batched forms: BF16 ops only
   View v;
   if (!make_view(op, T, N, K, &v, w_kn)) return false;
   v.batch = batch;
+  v.zero_in_split = op >= kOpRouterFwd;
   Plan plan;
   plan.batch = batch;
   plan.w_kn = w_kn;
@@ -370,13 +397,16 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
     // plan forced onto the SIMT program takes its tile and split overrides there)
     Overrides ot = o;
     if (op >= kOpRouterFwd && o.ffma == 1) ot.bn = ot.splits = ot.tail_splits = 0;
-    if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, ot, &c);
+    // (atomic split sums: FP32 outputs of single-problem calls that need not be
+    // bitwise repeatable)
+    const bool atomic_ok = !deterministic && out_bytes == 4 && batch == 1 && o.atomic != 0;
+    if (op != kOpWgrad || o.swap != 1) search(v, plan.nkb, sm, out_bytes, ot, &c, atomic_ok);
     if (op == kOpWgrad && o.swap != 0) {
       // thin outputs: let K fill the 128-row tile side and N be the MMA's N
       View sv = {K, N, T, true, true, 2, 2};
       sv.batch = batch;
       Choice cs;
-      search(sv, plan.nkb, sm, out_bytes, o, &cs);
+      search(sv, plan.nkb, sm, out_bytes, o, &cs, atomic_ok);
       if (cs.have && (!c.have || cs.t < c.t * 0.97 || o.swap == 1)) {
         c = cs;
         plan.swap = true;
@@ -394,6 +424,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   plan.bn = c.tiling.bn;
   plan.splits = static_cast<int>(c.splits);
   plan.stream_k = c.stream_k;
+  plan.atomic = c.atomic && c.splits > 1;
   plan.stages = v.terms > 1 ? stages_x3(plan.bn, plan.pair) : stages_for(plan.bn, plan.pair);
   plan.tiles_m = ceil_div(v.gm, plan.bm);
   plan.tiles_n = ceil_div(v.gn, plan.bn);
@@ -417,7 +448,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
 
   // workspace layout: [split partials | router's pre-split operands]
   size_t off = 0;
-  if (plan.splits > 1) {
+  if (plan.splits > 1 && !plan.atomic) {
     // one FP32 partial per split of every split tile, per CTA of the tile
     plan.off_partials = off;
     plan.bytes_partials = static_cast<size_t>(tiles - plan.full_units) * (plan.pair ? 2 : 1) * plan.splits *
@@ -446,7 +477,7 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
       plan.bytes_split_b = region(3 * static_cast<size_t>(N) * plan.ld_split_b * e, &plan.off_split_b);
     }
   }
-  plan.ws_bytes = (plan.splits > 1 || (router && T > 0)) ? round_up(off, 256) : 0;
+  plan.ws_bytes = ((plan.splits > 1 && !plan.atomic) || (router && T > 0)) ? round_up(off, 256) : 0;
   // D[m][n] goes out transposed for the swapped weight gradient, unless the weight
   // gradient is itself stored [K][N] (then the unswapped one is transposed instead)
   plan.out_trans = (op == kOpWgrad || op == kOpRouterWgrad) && (plan.swap != w_kn);

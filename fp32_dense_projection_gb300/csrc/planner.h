@@ -77,6 +77,9 @@ struct Plan {
   // slot boundaries is summed in pieces, up to `splits` of them, whose FP32 partials
   // the reduction adds in block order.  units = the pieces of all slots.
   bool stream_k = false;
+  // Non-deterministic (deterministic = 0, FP32 output): the split units add their FP32
+  // partials into the zero-filled output with atomic adds (no partials, no reduction).
+  bool atomic = false;
 };
 
 // Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows
@@ -121,14 +124,18 @@ struct Overrides {
   int fuse = -1;
   int ffma = -1;  // router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
   int stream_k = -1;  // 0 never, 1 only stream-K candidates (where the shape admits one)
+  int atomic = -1;    // non-deterministic calls: 0 ordered split sums, 1 atomic ones (where admitted)
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,
 // sm_count < 1, unknown op, or overrides that admit no plan).
 // batch > 1: `batch` independent GEMMs of this shape in one launch (BF16 ops);
 // w_kn: W (and dW) stored [K][N] rather than [N][K].
+// deterministic = false admits the atomic split sums (FP32 outputs of single-problem
+// calls), where the model finds them faster than the ordered sum.
 bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm_count, Plan* plan,
-               const Overrides& overrides = Overrides(), int64_t batch = 1, bool w_kn = false);
+               const Overrides& overrides = Overrides(), int64_t batch = 1, bool w_kn = false,
+               bool deterministic = true);
 
 // The backward pass of one layer: the input gradient and the weight gradient of
 // the same dY.  Either the two single-op plans, run one after the other, or one

@@ -26,6 +26,8 @@ struct SplitJobs {
   SplitJob job[2];
   int64_t quads[2];  // four-element groups of each job
   int njobs;
+  ZeroJob zero;      // FP32 matrix to zero-fill (out null: none)
+  int64_t zquads;    // its four-element groups
 };
 
 // Each thread converts four quads spaced one grid apart, all four loads issued
@@ -51,6 +53,14 @@ __device__ __forceinline__ void locate(const SplitJobs& jobs, uint64_t i, const 
 
 __global__ void __launch_bounds__(kSplitThreads) split_x3_kernel(const __grid_constant__ SplitJobs jobs) {
   pdl_launch_dependents();  // the GEMM may start staging its other operand meanwhile
+  // the zero fill of a non-deterministic call's output, one float4 per thread and step
+  const uint64_t gstep = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       i < static_cast<uint64_t>(jobs.zquads); i += gstep) {
+    const uint64_t per_row = static_cast<uint64_t>(jobs.zero.cols / 4);
+    const uint64_t r = i / per_row, q = i - r * per_row;
+    *reinterpret_cast<float4*>(jobs.zero.out + r * jobs.zero.ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const uint64_t total =
       static_cast<uint64_t>(jobs.quads[0]) + (jobs.njobs > 1 ? static_cast<uint64_t>(jobs.quads[1]) : 0);
   const uint64_t step = static_cast<uint64_t>(gridDim.x) * blockDim.x;
@@ -85,9 +95,16 @@ __global__ void __launch_bounds__(kSplitThreads) split_x3_kernel(const __grid_co
 
 }  // namespace
 
-cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream) {
+cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaStream_t stream,
+                            const ZeroJob* zero) {
   if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
   SplitJobs p = {};
+  if (zero && zero->rows > 0) {
+    if (zero->cols % 4 != 0 || zero->ld % 4 != 0 || (reinterpret_cast<uintptr_t>(zero->out) & 15u) != 0)
+      return cudaErrorInvalidValue;
+    p.zero = *zero;
+    p.zquads = zero->rows * (zero->cols / 4);
+  }
   int64_t total = 0;
   for (int j = 0; j < njobs; ++j) {
     const SplitJob& s = jobs[j];
@@ -101,9 +118,10 @@ cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaS
     total += p.quads[j];
   }
   p.njobs = njobs;
-  if (total == 0) return cudaSuccess;
+  if (total == 0 && p.zquads == 0) return cudaSuccess;
   const int64_t per_block = kSplitThreads * kSplitQuads;
-  const int64_t blocks = std::min<int64_t>((total + per_block - 1) / per_block, static_cast<int64_t>(sm_count) * 8);
+  const int64_t work = std::max<int64_t>(total, p.zquads);
+  const int64_t blocks = std::min<int64_t>((work + per_block - 1) / per_block, static_cast<int64_t>(sm_count) * 8);
   split_x3_kernel<<<static_cast<unsigned>(blocks), kSplitThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

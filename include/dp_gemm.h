@@ -55,11 +55,18 @@
  *   is enqueued on it; calls return before the GPU finishes.  Calls are legal
  *   inside CUDA stream capture after the first call on the device (which sets
  *   kernel attributes; dp_init() does it explicitly).
- * Determinism.  Every output is bitwise reproducible for the same inputs, shapes,
- *   strides and SM count: each output tile's contraction is split into a fixed
- *   partition chosen by a pure planner, and split partials are summed in split
- *   order.  `deterministic` is accepted for interface parity with the pages'
- *   entry points; 0 selects the same deterministic programs.
+ * Determinism.  With deterministic != 0 (the default of the pages' entry points)
+ *   every output is bitwise reproducible for the same inputs, shapes, strides and
+ *   SM count: each output tile's contraction is split into a fixed partition
+ *   chosen by a pure planner, and split partials are summed in split order.
+ *   deterministic = 0 (the pages' non-deterministic package) admits, for FP32
+ *   outputs of single-problem calls, plans whose split units add their FP32
+ *   partials into the output with atomic adds after a zero fill of the output
+ *   (a memset node, or a job of the router's split kernel): no partial workspace
+ *   and no reduction kernel, at the cost of run-to-run variation in the last bits
+ *   (the adds' order).  The planner takes it only where its model finds it
+ *   faster; BF16 outputs, batched calls and plans without split tiles stay
+ *   deterministic either way.
  * Errors.  Arguments are checked before anything is enqueued; a non-DP_OK status
  *   means nothing was launched (except DP_ERR_LAUNCH, reported by CUDA after the
  *   attempt).  No exception crosses the ABI.
@@ -177,7 +184,7 @@ dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int6
  * the B * tiles_m * tiles_n tiles in one persistent launch (its tile shape and
  * splits are chosen for the whole batch, so they can differ from a single
  * problem's); every problem's tiles use the same fixed contraction partition and
- * summation order, so the outputs are deterministic. */
+ * summation order, so the outputs are deterministic (whatever `deterministic`). */
 dp_status dp_gemm_fwd_batched(const void* X, int64_t ldx, int64_t bsx, const void* W, int64_t ldw, int64_t bsw,
                               int weight_kn, void* Y, int64_t ldy, int64_t bsy,
                               int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
@@ -268,7 +275,8 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * partials in the reduction kernel instead of inside the GEMM's clusters; the
  * two give the same bits), DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls
  * or as one co-scheduled launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never;
- * 1: a stream-K plan where the shape admits one).  A forced plan is still deterministic and keeps the
+ * 1: a stream-K plan where the shape admits one), DP_FORCE_ATOMIC (calls with
+ * deterministic = 0: 0 ordered split sums, 1 atomic ones wherever admitted).  A forced plan is still deterministic and keeps the
  * accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of
@@ -310,12 +318,20 @@ typedef struct dp_plan_info {
     int32_t program;          /* router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
                                  (64 x block_n tiles, `splits` CTAs per tile, block_k
                                  contraction elements per stage); BF16 ops: 0 */
+    int32_t atomic;           /* 1: split units add into the zero-filled FP32 output with
+                                 atomic adds (deterministic = 0 only) */
+    int32_t reserved3;
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs
  * (sm_count <= 0: query the current device).  Pure host function. */
 dp_status dp_plan_query(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                         int sm_count, dp_plan_info* info);
+/* The same for a call with the given `deterministic` flag (dp_plan_query is
+ * deterministic = 1).  A non-deterministic plan needs no more workspace than the
+ * deterministic one of the same call. */
+dp_status dp_plan_query_ex(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dtype out, int deterministic,
+                           int sm_count, dp_plan_info* info);
 /* The same for a batched BF16 call (op DP_OP_FWD / DGRAD / WGRAD, B >= 1). */
 dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                                 int weight_kn, int sm_count, dp_plan_info* info);

@@ -408,3 +408,34 @@ def test_stream_k_plan(monkeypatch, op, T, N, K):
     # the planner's own choice for these shapes is not stream-K (measured slower on GB300)
     monkeypatch.delenv("DP_FORCE_STREAM_K")
     assert dp.plan(op, T, N, K, sm_count=SM)["stream_k"] == 0
+
+
+# ------------------------------------------------------- non-deterministic plans
+
+@pytest.mark.parametrize("op", list(dp.OP_NAMES))
+@pytest.mark.parametrize("T,N,K", [(64, 1024, 4096), (1024, 256, 4096), (65537, 64, 4096), (16384, 12288, 4096)])
+def test_non_deterministic_plans(op, T, N, K):
+    for f32 in (False, True):
+        det = dp.plan(op, T, N, K, out_f32=f32, sm_count=SM)
+        nd = dp.plan(op, T, N, K, out_f32=f32, sm_count=SM, deterministic=False)
+        assert det["atomic"] == 0
+        out32 = f32 or op.startswith("router")
+        if not out32:  # BF16 outputs: the deterministic plan, whatever the flag
+            assert nd == det
+            continue
+        # atomic sums only for split tiles, and never more workspace than the ordered sums
+        assert nd["atomic"] == 0 or nd["splits"] > 1
+        assert nd["workspace_bytes"] <= det["workspace_bytes"]
+        if nd["atomic"] and not op.startswith("router"):
+            assert nd["workspace_bytes"] == 0
+
+
+def test_atomic_override(monkeypatch):
+    monkeypatch.setenv("DP_FORCE_ATOMIC", "1")
+    monkeypatch.setenv("DP_FORCE_SPLITS", "3")
+    assert dp.plan("dgrad", 200, 512, 2048, out_f32=True, sm_count=SM, deterministic=False)["atomic"] == 1
+    # deterministic calls and BF16 outputs never take it
+    assert dp.plan("dgrad", 200, 512, 2048, out_f32=True, sm_count=SM)["atomic"] == 0
+    assert dp.plan("dgrad", 200, 512, 2048, out_f32=False, sm_count=SM, deterministic=False)["atomic"] == 0
+    monkeypatch.setenv("DP_FORCE_ATOMIC", "0")
+    assert dp.plan("dgrad", 200, 512, 2048, out_f32=True, sm_count=SM, deterministic=False)["atomic"] == 0

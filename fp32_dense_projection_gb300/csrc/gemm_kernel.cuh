@@ -262,13 +262,14 @@ __device__ __forceinline__ bool slot_unit(int k, int slot, int step, int total, 
   const int u = slot + k * step;
   if (u >= total) return false;
   *ur = unit_ref(u, args, mA, mB, sec);
-  *w = decode_unit(*ur->a, ur->u);
+  *w = decode_unit(DUAL ? *ur->a : args, ur->u);
   return true;
 }
 
-// Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.
+// Store 32 FP32 accumulator values (one row segment) as BF16 or FP32.  add (FP32
+// output of a non-deterministic split unit): add them into the output atomically.
 __device__ __forceinline__ void store_row32(const GemmArgs& a, void* out, int64_t m, int64_t col0,
-                                            const float (&v)[32]) {
+                                            const float (&v)[32], bool add = false) {
   if (m >= a.gm) return;
   if (a.out_trans) {
     // D[m][n] goes to out[n][m]: the 32 lanes of a warp hold 32 consecutive m, so
@@ -277,7 +278,9 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, void* out, int64_
     for (int j = 0; j < 32; ++j) {
       if (col0 + j >= a.gn) break;
       const int64_t o = (col0 + j) * a.ldo + m;
-      if (a.out_f32)
+      if (add)
+        red_add_f32(static_cast<float*>(out) + o, v[j]);
+      else if (a.out_f32)
         static_cast<float*>(out)[o] = v[j];
       else
         static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.0f) & 0xFFFFu);
@@ -333,7 +336,7 @@ __device__ __forceinline__ void stage_block32(const GemmArgs& a, uint32_t buf, i
 }
 
 __device__ __forceinline__ void flush_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
-                                              int64_t col0) {
+                                              int64_t col0, bool add = false) {
   const int64_t rows_left = a.gm - m0;
   if (a.out_f32) {
     const int ch = lane & 7, r0 = lane >> 3;
@@ -344,7 +347,12 @@ __device__ __forceinline__ void flush_block32(const GemmArgs& a, void* out, uint
     for (int i = 0; i < 8; ++i, p += step) {
       const int r = 4 * i + r0;
       const uint4 x = ld_shared_u4(buf + r * 128 + ((ch ^ (r & 7)) << 4));
-      if (col_ok && r < rows_left) *reinterpret_cast<uint4*>(p) = x;
+      if (col_ok && r < rows_left) {
+        if (add)
+          red_add_v4_f32(p, x);
+        else
+          *reinterpret_cast<uint4*>(p) = x;
+      }
     }
   } else {
     const int ch = lane & 3, r0 = lane >> 2;
@@ -360,45 +368,17 @@ __device__ __forceinline__ void flush_block32(const GemmArgs& a, void* out, uint
   }
 }
 
+// (add: a non-deterministic split unit's FP32 partial, added into the zero-filled
+// output with atomic adds: 16-byte vector adds of whole 128-byte row segments, or
+// for the transposed output coalesced scalar adds)
 __device__ __forceinline__ void store_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
-                                              int64_t col0, const float (&v)[32]) {
+                                              int64_t col0, const float (&v)[32], bool add = false) {
   if (a.out_trans) {
-    store_row32(a, out, m0 + lane, col0, v);
+    store_row32(a, out, m0 + lane, col0, v, add);
     return;
   }
   stage_block32(a, buf, lane, v);
-  flush_block32(a, out, buf, lane, m0, col0);
-}
-
-// Non-deterministic split units: add a 32 x 32 FP32 block (lane i: row m0 + i,
-// columns [col0, col0 + 32)) into the zero-filled FP32 output.  Row-major outputs go
-// through the warp's shared-memory block, so each instruction adds whole 128-byte
-// row segments (16-byte vector atomics); the transposed output adds straight from
-// the registers (the lanes' rows are consecutive elements).
-__device__ __forceinline__ void add_block32(const GemmArgs& a, void* out, uint32_t buf, int lane, int64_t m0,
-                                            int64_t col0, const float (&v)[32]) {
-  float* o = static_cast<float*>(out);
-  if (a.out_trans) {
-    const int64_t m = m0 + lane;
-    if (m >= a.gm) return;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (col0 + j < a.gn) atomicAdd(o + (col0 + j) * a.ldo + m, v[j]);
-    return;
-  }
-  stage_block32(a, buf, lane, v);
-  const int64_t rows_left = a.gm - m0;
-  const int ch = lane & 7, r0 = lane >> 3;
-  const bool col_ok = col0 + 4 * ch < a.gn;
-  float* p = o + (m0 + r0) * a.ldo + col0 + 4 * ch;
-#pragma unroll
-  for (int i = 0; i < 8; ++i, p += 4 * a.ldo) {
-    const int r = 4 * i + r0;
-    const uint4 x = ld_shared_u4(buf + r * 128 + ((ch ^ (r & 7)) << 4));
-    if (col_ok && r < rows_left)
-      atomicAdd(reinterpret_cast<float4*>(p),
-                make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)));
-  }
+  flush_block32(a, out, buf, lane, m0, col0, add);
 }
 
 // In-kernel ordered sum for cluster plans: the S CTAs of a cluster computed the S
@@ -696,7 +676,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         UnitRef ur;
         Unit w;
         if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
-        const GemmArgs& ga = *ur.a;
+        // (one problem: the kernel's own parameters, read from the parameter space)
+        const GemmArgs& ga = DUAL ? *ur.a : args;
+        const CUtensorMap* mapA = DUAL ? ur.mA : &tmA;
+        const CUtensorMap* mapB = DUAL ? ur.mB : &tmB;
         const bool a_mn = DUAL ? ga.a_mn != 0 : A_MN;
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
@@ -732,20 +715,20 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           };
           // MN-major: 64-column groups of 64 contraction rows (8 KB each)
           if (a_mn && ga.a3d) {
-            load3(sa, ur.mA, kb * C::BK, a_row0 / 64);
+            load3(sa, mapA, kb * C::BK, a_row0 / 64);
           } else if (a_mn) {
-            load(sa, ur.mA, a_row0, kb * C::BK);
-            load(sa + 8192, ur.mA, a_row0 + 64, kb * C::BK);
+            load(sa, mapA, a_row0, kb * C::BK);
+            load(sa + 8192, mapA, a_row0 + 64, kb * C::BK);
           } else {
-            load(sa, ur.mA, kb * C::BK, a_row0);
+            load(sa, mapA, kb * C::BK, a_row0);
           }
           if (B_MN && ga.b3d) {
-            load3(sb, ur.mB, kb * C::BK, b_row0 / 64);
+            load3(sb, mapB, kb * C::BK, b_row0 / 64);
           } else if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, ur.mB, b_row0 + 64 * j, kb * C::BK);
+            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, mapB, b_row0 + 64 * j, kb * C::BK);
           } else {
-            load(sb, ur.mB, kb * C::BK, b_row0);
+            load(sb, mapB, kb * C::BK, b_row0);
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -781,7 +764,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         UnitRef ur;
         Unit w;
         if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
-        const bool a_mn = DUAL ? ur.a->a_mn != 0 : A_MN;
+        const bool a_mn = DUAL ? ur.a->a_mn != 0 : A_MN;  // (one problem: the template's)
         const uint32_t idesc = (DUAL && a_mn) ? IDESC_AMN : IDESC;
         const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
@@ -966,7 +949,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       UnitRef ur;
       Unit w;
       if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
-      const GemmArgs& ga = *ur.a;
+      const GemmArgs& ga = DUAL ? *ur.a : args;  // (one problem: the kernel's own parameters)
       const int tm = w.tm, tn = w.tn;
       const int slot = w.ptile * (PAIR ? 2 : 1) + static_cast<int>(rank);  // this CTA's partial slot
       const int acc = local & 1;
@@ -996,10 +979,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          if (w.split)  // (non-deterministic plans: into the zero-filled output)
-            add_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
-          else
-            store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v);
+          // (a split unit here: a non-deterministic plan's, added into the zero-filled output)
+          store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v, w.split);
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's

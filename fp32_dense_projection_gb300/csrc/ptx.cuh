@@ -383,6 +383,17 @@ __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
   return v;
 }
 
+// Atomic FP32 adds into global memory whose result is not needed (reductions):
+// one value, or four consecutive values (16-byte aligned) given as raw bits.
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_v4_f32(float* p, uint4 x) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(x.x)),
+               "f"(__uint_as_float(x.y)), "f"(__uint_as_float(x.z)), "f"(__uint_as_float(x.w))
+               : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core) before signalling that the data is ready.
 __device__ __forceinline__ void fence_proxy_async_shared() {

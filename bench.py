@@ -254,52 +254,70 @@ def run_gpu(args, world, rank, local):
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, the three ops, D2H of the three results, all timed
     e2e = None
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(2, min(args.steps, 10))
     hX, hW, hdY = (t.cpu().pin_memory() for t in (X, W, dY))
-    hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
     h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
-    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
+    d2h = sum(t.numel() * t.element_size() for t in (Y, dX, dW))
 
-    # Copies overlap the GEMMs on two copy streams (CUDA events order them): X and W
-    # go up first so the forward starts while dY (the largest input) is still in
-    # flight; Y comes back while the gradients run, each result as soon as it exists.
+    # As a training loop prefetches its next batch: two sets of device buffers (and
+    # of pinned host results) alternate between steps, so step k + 1's inputs go up
+    # and step k's results come down while the other set's GEMMs run.  Within a step
+    # X and W go up first, so the forward starts while dY (the largest input) is
+    # still in flight, and each result comes back as soon as it exists.  Events
+    # order everything: a set is refilled only after its previous step's GEMMs are
+    # done with it, and its outputs are rewritten only after they have been read back.
     up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    sets = []
+    for k in range(2):
+        dev_set = (X, W, dY, Y, dX, dW) if k == 0 else tuple(torch.empty_like(t) for t in (X, W, dY, Y, dX, dW))
+        host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
+        sets.append({"dev": dev_set, "host": host_out, "gemm_done": None, "down_done": None})
 
-    def e2e_step():
-        ev = {k: torch.cuda.Event() for k in ("xw", "dy", "y", "dx", "dw", "free")}
-        up.wait_stream(stream)  # the previous step's GEMMs are done with X, W, dY
+    def e2e_step(i):
+        st = sets[i % 2]
+        sX, sW, sdY, sY, sdX, sdW = st["dev"]
+        hY, hdX, hdW = st["host"]
+        ev = {k: torch.cuda.Event() for k in ("xw", "dy", "y", "dx", "dw", "gemm", "down")}
         with torch.cuda.stream(up):
-            X.copy_(hX, non_blocking=True)
-            W.copy_(hW, non_blocking=True)
+            if st["gemm_done"] is not None:
+                up.wait_event(st["gemm_done"])  # this set's previous GEMMs are done with its inputs
+            sX.copy_(hX, non_blocking=True)
+            sW.copy_(hW, non_blocking=True)
             ev["xw"].record(up)
-            dY.copy_(hdY, non_blocking=True)
+            sdY.copy_(hdY, non_blocking=True)
             ev["dy"].record(up)
-        stream.wait_stream(down)  # the previous step's downloads are done with Y, dX, dW
+        if st["down_done"] is not None:
+            stream.wait_event(st["down_done"])  # this set's previous results have been read back
         stream.wait_event(ev["xw"])
-        dp.dp_gemm_fwd(X, W, out=Y, workspace=wsbuf)
+        dp.dp_gemm_fwd(sX, sW, out=sY, workspace=wsbuf)
         ev["y"].record(stream)
         stream.wait_event(ev["dy"])
-        dp.dp_gemm_dgrad(dY, W, out=dX, workspace=wsbuf)
+        dp.dp_gemm_dgrad(sdY, sW, out=sdX, workspace=wsbuf)
         ev["dx"].record(stream)
-        dp.dp_gemm_wgrad(dY, X, out=dW, workspace=wsbuf)
+        dp.dp_gemm_wgrad(sdY, sX, out=sdW, workspace=wsbuf)
         ev["dw"].record(stream)
+        st["gemm_done"] = ev["dw"]
         with torch.cuda.stream(down):
             down.wait_event(ev["y"])
-            hY.copy_(Y, non_blocking=True)
+            hY.copy_(sY, non_blocking=True)
             down.wait_event(ev["dx"])
-            hdX.copy_(dX, non_blocking=True)
+            hdX.copy_(sdX, non_blocking=True)
             down.wait_event(ev["dw"])
-            hdW.copy_(dW, non_blocking=True)
+            hdW.copy_(sdW, non_blocking=True)
+            ev["down"].record(down)
+        st["down_done"] = ev["down"]
 
-    e2e_step()
+    for i in range(2):  # warm-up: both buffer sets
+        e2e_step(i)
     torch.cuda.synchronize()
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     ea.record(stream)
     up.wait_stream(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    down.wait_stream(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
     stream.wait_stream(down)  # every download of every step is inside the timed region
     stream.wait_stream(up)
     eb.record(stream)

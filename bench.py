@@ -556,10 +556,12 @@ def run_suite(args, local):
         bound = "tensor" if ai > ridge else "hbm"
         for mode, timer in (("eager", eager), ("graph", graph), ("kernel span", span)):
             us = timer(fn)
+            us_repeat = timer(fn)  # the A/A repeat: the same measurement once more
             tflops = flop / us / 1e6
             gbs = nbytes / us / 1e3
             frac = (tc_flop / us / 1e6) / tc_peak if bound == "tensor" else gbs / hbm_peak
-            line = {"suite": cfg, "case": case, "mode": mode, "us": round(us, 2), "tflops": round(tflops, 1),
+            line = {"suite": cfg, "case": case, "mode": mode, "us": round(us, 2), "us_repeat": round(us_repeat, 2),
+                    "tflops": round(tflops, 1),
                     "gbs": round(gbs, 1), "bound": bound, "frac": round(frac, 3),
                     "of": f"{peak_src} {'bf16 burst' if bound == 'tensor' else 'HBM copy'} peak"}
             if plans:

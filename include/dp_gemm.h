@@ -45,7 +45,9 @@
  *   run concurrently.
  * Launches.  Each call enqueues one GEMM kernel; a plan that splits contractions
  *   adds the kernel that sums the partials, and a router call adds the kernel
- *   that splits its reused FP32 operand into bf16 hi/lo before the GEMM.  The GEMM
+ *   that splits its reused FP32 operand into bf16 hi/lo before the GEMM (a router
+ *   call on the small-T SIMT program is that one kernel alone; a non-deterministic
+ *   plan adds a memset of its FP32 output instead of the reduction).  The GEMM
  *   and the reduction launch as programmatic dependents of the kernel before them
  *   on the stream: their setup overlaps that kernel's tail, and they wait for its
  *   completion before touching global memory, so stream order between calls (one

@@ -281,9 +281,10 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       // Stream-K, for tile counts that fit in one wave: every slot takes an even share
       // of all tiles' blocks, so no SM idles while others finish a wider split.  (More
       // tiles keep the raster-ordered waves, whose neighbouring tiles share operands in
-      // L2.)  Each piece stays within the accumulation bound; BF16 operands only.
+      // L2.)  Each piece stays within the accumulation bound; BF16 operands of one
+      // problem only.
       const int64_t per_slot = ceil_div(tiles * nkb, slots);
-      if (o.stream_k != 0 && v.terms == 1 && o.splits <= 0 && o.tail_splits <= 0 && tiles <= slots &&
+      if (o.stream_k != 0 && v.terms == 1 && v.batch == 1 && o.splits <= 0 && o.tail_splits <= 0 && tiles <= slots &&
           tiles * nkb >= 2 * slots && std::min(per_slot, nkb) <= max_blocks) {
         const int64_t most = stream_k_pieces(tiles, nkb, slots, nullptr);
         if (most >= 2 && cta_tiles * most <= kMaxSplitTiles) {

@@ -35,13 +35,19 @@ def force(monkeypatch, fuse, pair=None, bn=None):
 
 @pytest.mark.parametrize("pair,bn", TILINGS)
 @pytest.mark.parametrize("fuse", [2, 3])
-@pytest.mark.parametrize("T,N,K", [(1000, 384, 640), (333, 136, 520)])
+@pytest.mark.parametrize("T,N,K", [(1000, 384, 640), (333, 136, 520), (1, 136, 264), (65, 272, 200)])
 def test_co_scheduled_integer_exact(monkeypatch, pair, bn, fuse, T, N, K):
     # small-integer operands: every product and partial sum is exact in FP32, so both
     # gradients equal the oracle exactly, whatever the tile shape and tile order
     force(monkeypatch, fuse, pair, bn)
-    b = dp.plan_bwd(T, N, K, True, True)
-    assert b["fused"] and b["wgrad_first"] == (fuse == 2)
+    try:
+        b = dp.plan_bwd(T, N, K, True, True)
+    except dp.DPError:  # (a pair needs two row tiles of work in both problems)
+        b = {"fused": 0}
+    if not b["fused"]:
+        assert pair == 1
+        pytest.skip("no co-scheduled plan of this tile shape for the shape")
+    assert b["wgrad_first"] == (fuse == 2)
     assert (b["dgrad"]["cta_pair"], b["dgrad"]["block_n"]) == (pair, bn)
     c = inputs.integer_case(T, N, K, seed=T + bn + fuse)
     d = on_device(c)

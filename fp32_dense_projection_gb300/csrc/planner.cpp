@@ -36,6 +36,17 @@ constexpr double kNarrowB = 1.35;             // tiles whose B slice per CTA is 
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
+// The epilogue of one unit (TMEM -> registers -> shared -> global), per CTA: a fixed
+// cost (a CTA pair's two epilogues release one accumulator together: more), and the
+// output bytes at its store rate.  It overlaps the next unit's main loop, so it only
+// shows when it is the longer of the two (short contractions: measured on batched
+// per-head GEMMs with 2 contraction blocks per tile).
+constexpr double kEpiNs = 670.0;
+constexpr double kEpiPairNs = 1420.0;
+constexpr double kEpiBytesPerNs = 37.0;
+// A CTA pair's MMA waits for both CTAs' operand stages, so a load-bound pair runs at
+// its slower CTA's pace (measured on the batched per-head shapes: pairs 1.2x slower)
+constexpr double kPairLoadPenalty = 1.2;
 constexpr double kLaunchNs = 3000.0;          // a launch's fixed cost: setup, first loads, last tile's epilogue
 // Non-deterministic atomic split sums: the zero fill's fixed cost (a memset node
 // before the GEMM; for the router, a job of its operand-split kernel, nearly free),
@@ -126,9 +137,11 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
   const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) * narrow / kL2BytesPerNsPerSm);
-  const double t_load = kb * bytes_per_kb / bw;
+  const double t_load = kb * bytes_per_kb / bw * (t.pair ? kPairLoadPenalty : 1.0);
   const double out_tile = a_rows * static_cast<double>(std::min<int64_t>(t.bn, v.gn)) * (split ? 4.0 : out_bytes);
-  return std::max(std::max(t_mma, t_load), t_split) + out_tile / dram;
+  const double t_main = std::max(std::max(t_mma, t_load), t_split) + out_tile / dram;
+  const double t_epi = (t.pair ? kEpiPairNs : kEpiNs) + out_tile / kEpiBytesPerNs;
+  return std::max(t_main, t_epi);
 }
 
 // How many times the tiles load each unique operand byte (at least 1).

@@ -64,6 +64,10 @@ constexpr double kFfmaWaveNs = 3000.0;
 constexpr double kFfmaClusterNs = 1000.0;
 constexpr int kFfmaCtasPerSm = 1;
 constexpr double kFuseGain = 0.97;            // co-schedule the backward pass only for >= 3% modelled gain
+// what a launch of the backward pass costs beyond its modelled work, in a sequence of
+// calls (measured: two calls 24.1 us vs one co-scheduled launch 19.2 us at T = 1024,
+// 4096 -> 1024, where the model's work differs by ~1 us)
+constexpr double kBwdLaunchNs = 5000.0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t ffma_stage_k_host(int bn) { return 4096 / bn; }  // contraction elements per stage of the SIMT program
@@ -562,7 +566,7 @@ bool make_plan_bwd(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int 
   BwdPlan r;
   if (!make_plan(kOpDgrad, T, N, K, dx_f32, sm, &r.dgrad, o) || !make_plan(kOpWgrad, T, N, K, dw_f32, sm, &r.wgrad, o))
     return false;
-  r.separate_ns = r.dgrad.model_ns + r.wgrad.model_ns + 2 * kLaunchNs;
+  r.separate_ns = r.dgrad.model_ns + r.wgrad.model_ns + 2 * kBwdLaunchNs;
   r.model_ns = r.separate_ns;
   r.ws_bytes = std::max(r.dgrad.ws_bytes, r.wgrad.ws_bytes);
   // Co-scheduled candidates: one tiling for both problems, whole K per tile (no
@@ -586,7 +590,7 @@ bool make_plan_bwd(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int 
         if (d.splits != 1 || w.splits != 1 || d.units < 1 || w.units < 1) continue;
         for (int wf = 0; wf < 2; ++wf) {
           if (o.fuse >= 2 && wf != (o.fuse == 2 ? 1 : 0)) continue;
-          const double t = fused_model_ns(wf ? w : d, wf ? d : w, sm) + kLaunchNs;
+          const double t = fused_model_ns(wf ? w : d, wf ? d : w, sm) + kBwdLaunchNs;
           if (!have || t < best.model_ns) {
             have = true;
             best.fused = true;

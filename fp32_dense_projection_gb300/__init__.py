@@ -50,12 +50,12 @@ class PlanInfo(ctypes.Structure):
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
         ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double),
         ("batch", ctypes.c_int64), ("tiles", ctypes.c_int64), ("weight_kn", ctypes.c_int32),
-        ("program", ctypes.c_int32), ("atomic", ctypes.c_int32), ("reserved3", ctypes.c_int32)]
+        ("program", ctypes.c_int32), ("atomic", ctypes.c_int32), ("blocks_per_stage", ctypes.c_int32)]
 
 
 class BwdPlanInfo(ctypes.Structure):
     _fields_ = [("fused", ctypes.c_int32), ("wgrad_first", ctypes.c_int32), ("grid", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("model_us", ctypes.c_double), ("separate_us", ctypes.c_double),
+                ("blocks_per_stage", ctypes.c_int32), ("model_us", ctypes.c_double), ("separate_us", ctypes.c_double),
                 ("workspace_bytes", ctypes.c_uint64), ("dgrad", PlanInfo), ("wgrad", PlanInfo)]
 
 
@@ -155,8 +155,8 @@ def _info_dict(info: PlanInfo) -> dict:
 
 
 def plan_bwd(T: int, N: int, K: int, dx_f32: bool = False, dw_f32: bool = False, sm_count: int = 0) -> dict:
-    """The backward pass's plan: {"fused", "wgrad_first", "grid", "model_us", "separate_us",
-    "workspace_bytes", "dgrad": {...}, "wgrad": {...}}."""
+    """The backward pass's plan: {"fused", "wgrad_first", "grid", "blocks_per_stage", "model_us",
+    "separate_us", "workspace_bytes", "dgrad": {...}, "wgrad": {...}}."""
     info = BwdPlanInfo()
     _check(lib().dp_plan_query_bwd(T, N, K, int(bool(dx_f32)), int(bool(dw_f32)), int(sm_count),
                                    ctypes.byref(info)), "dp_plan_query_bwd")

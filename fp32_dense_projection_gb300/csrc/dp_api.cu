@@ -221,9 +221,31 @@ int env_int(const char* name) {
 
 // Plan overrides for tuning and tests, read on every call (DP_FORCE_CLUSTER_SUM=0,
 // read in cluster_fixup, keeps split sums in the reduction kernel): DP_FORCE_BN,
-// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS (> 0 forces), DP_FORCE_SWAP (0 or 1: the
-// weight-gradient orientation) and DP_FORCE_PAIR (0 or 1: single-CTA or CTA-pair
-// tiles).  Unset in normal use.
+// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS, DP_FORCE_KPS (> 0 forces), DP_FORCE_SWAP (0
+// or 1: the weight-gradient orientation), DP_FORCE_PAIR (0 or 1: single-CTA or
+// CTA-pair tiles), DP_FORCE_FUSE, DP_FORCE_FFMA, DP_FORCE_STREAM_K and
+// DP_FORCE_ATOMIC (0 or 1).  Unset in normal use.
+Overrides env_overrides() {
+  const char* sw = std::getenv("DP_FORCE_SWAP");
+  const char* pr = std::getenv("DP_FORCE_PAIR");
+  const char* fu = std::getenv("DP_FORCE_FUSE");
+  Overrides o;
+  o.bn = env_int("DP_FORCE_BN");
+  o.splits = env_int("DP_FORCE_SPLITS");
+  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
+  o.swap = sw ? std::atoi(sw) : -1;
+  o.pair = pr ? std::atoi(pr) : -1;
+  o.fuse = fu ? std::atoi(fu) : -1;
+  const char* ff = std::getenv("DP_FORCE_FFMA");
+  o.ffma = ff ? std::atoi(ff) : -1;
+  const char* sk = std::getenv("DP_FORCE_STREAM_K");
+  o.stream_k = sk ? std::atoi(sk) : -1;
+  const char* at = std::getenv("DP_FORCE_ATOMIC");
+  o.atomic = at ? std::atoi(at) : -1;
+  o.kps = env_int("DP_FORCE_KPS");
+  return o;
+}
+
 struct PlanEntry {
   bool valid = false;
   int op, out_f32, sm, w_kn, det;
@@ -236,32 +258,20 @@ thread_local PlanEntry t_plans[kPlanCacheSize];
 bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan* plan, int64_t batch = 1,
               int w_kn = 0, int deterministic = 1) {
   deterministic = deterministic ? 1 : 0;
-  const char* sw = std::getenv("DP_FORCE_SWAP");
-  const char* pr = std::getenv("DP_FORCE_PAIR");
-  Overrides o;
-  o.bn = env_int("DP_FORCE_BN");
-  o.splits = env_int("DP_FORCE_SPLITS");
-  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
-  o.swap = sw ? std::atoi(sw) : -1;
-  o.pair = pr ? std::atoi(pr) : -1;
-  const char* ff = std::getenv("DP_FORCE_FFMA");
-  o.ffma = ff ? std::atoi(ff) : -1;
-  const char* sk = std::getenv("DP_FORCE_STREAM_K");
-  o.stream_k = sk ? std::atoi(sk) : -1;
-  const char* at = std::getenv("DP_FORCE_ATOMIC");
-  o.atomic = at ? std::atoi(at) : -1;
+  const Overrides o = env_overrides();
   uint64_t h = mix(mix(mix(static_cast<uint64_t>(op), static_cast<uint64_t>(T)), static_cast<uint64_t>(N)),
                    static_cast<uint64_t>(K));
   h = mix(mix(h, static_cast<uint64_t>(out_f32 * 4096 + sm)),
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
               (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919 +
-              static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.atomic + 1) * 1299709);
+              static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.atomic + 1) * 1299709 +
+              static_cast<uint64_t>(o.kps) * 15485863);
   h = mix(h, static_cast<uint64_t>(batch) * 4 + static_cast<uint64_t>(w_kn) * 2 + static_cast<uint64_t>(deterministic));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
       e.batch == batch && e.w_kn == w_kn && e.det == deterministic && e.o.bn == o.bn && e.o.splits == o.splits &&
       e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma &&
-      e.o.stream_k == o.stream_k && e.o.atomic == o.atomic) {
+      e.o.stream_k == o.stream_k && e.o.atomic == o.atomic && e.o.kps == o.kps) {
     *plan = e.plan;
     return true;
   }
@@ -395,6 +405,7 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   a.atomic = p.atomic ? 1 : 0;
   a.sk_work = p.tiles * p.nkb;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
+  a.kps = (!x3 && p.kps == 2 && p.stages % 2 == 0) ? 2 : 1;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;
@@ -568,6 +579,7 @@ void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
   info->program = p.ffma ? 1 : 0;
   info->stream_k = p.stream_k ? 1 : 0;
   info->atomic = p.atomic ? 1 : 0;
+  info->blocks_per_stage = p.kps;
   info->model_us = p.model_ns * 1e-3;
 }
 
@@ -621,23 +633,6 @@ dp_status run_batched(int op, const void* a, int64_t lda, int64_t bsa, const voi
 
 // ------------------------------------------------------------ backward pass
 
-Overrides env_overrides() {
-  const char* sw = std::getenv("DP_FORCE_SWAP");
-  const char* pr = std::getenv("DP_FORCE_PAIR");
-  const char* fu = std::getenv("DP_FORCE_FUSE");
-  Overrides o;
-  o.bn = env_int("DP_FORCE_BN");
-  o.splits = env_int("DP_FORCE_SPLITS");
-  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
-  o.swap = sw ? std::atoi(sw) : -1;
-  o.pair = pr ? std::atoi(pr) : -1;
-  o.fuse = fu ? std::atoi(fu) : -1;
-  const char* ff = std::getenv("DP_FORCE_FFMA");
-  o.ffma = ff ? std::atoi(ff) : -1;
-  const char* sk = std::getenv("DP_FORCE_STREAM_K");
-  o.stream_k = sk ? std::atoi(sk) : -1;
-  return o;
-}
 
 struct BwdEntry {
   bool valid = false;
@@ -654,11 +649,12 @@ bool bwd_plan_for(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int s
                    static_cast<uint64_t>(dx_f32 * 2 + dw_f32) * 4096 + static_cast<uint64_t>(sm));
   h = mix(h, static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
                  (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.fuse + 1) * 1000003 +
-                 static_cast<uint64_t>(o.stream_k + 1) * 104729);
+                 static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.kps) * 15485863);
   BwdEntry& e = t_bwd_plans[h & 15];
   if (e.valid && e.T == T && e.N == N && e.K == K && e.dx_f32 == dx_f32 && e.dw_f32 == dw_f32 && e.sm == sm &&
       e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
-      e.o.pair == o.pair && e.o.fuse == o.fuse && e.o.stream_k == o.stream_k && e.o.ffma == o.ffma) {
+      e.o.pair == o.pair && e.o.fuse == o.fuse && e.o.stream_k == o.stream_k && e.o.ffma == o.ffma &&
+      e.o.atomic == o.atomic && e.o.kps == o.kps) {
     *plan = e.plan;
     return true;
   }
@@ -712,6 +708,7 @@ dp_status run_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const
   first.second.tmA = second.tmA;
   first.second.tmB = second.tmB;
   first.second.args = second.args;
+  first.args.kps = first.second.args.kps = bp.kps;  // (the two problems share one ring)
   first.grid = bp.grid;
   return launch_gemm_bwd(bp.dgrad.bn, bp.dgrad.pair, first, stream) == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
 }
@@ -721,6 +718,7 @@ void fill_bwd_info(const BwdPlan& bp, int64_t T, dp_bwd_plan_info* info) {
   info->fused = bp.fused ? 1 : 0;
   info->wgrad_first = bp.wgrad_first ? 1 : 0;
   info->grid = bp.fused ? bp.grid : 0;
+  info->blocks_per_stage = bp.fused ? bp.kps : 0;
   info->model_us = bp.model_ns * 1e-3;
   info->separate_us = bp.separate_ns * 1e-3;
   info->workspace_bytes = T == 0 ? 0 : bp.ws_bytes;

@@ -4,7 +4,8 @@
 // One CTA per SM walks a static list of work units (output tile x contraction
 // split).  Roles inside the 256-thread CTA:
 //   warp 0      TMA producer: loads 128x64 A and BNx64 B bf16 tiles (128-byte
-//               swizzle) into a STAGES-deep shared-memory ring;
+//               swizzle) into a shared-memory ring of STAGES block slots, one
+//               or two contraction blocks per ring stage (GemmArgs::kps);
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer (M=128,
 //               N=BN, K=16 per instruction), accumulating into one of two TMEM
 //               accumulators so the epilogue of a tile overlaps the next tile's
@@ -79,6 +80,11 @@ struct GemmArgs {
   // into the output, which the launch zero-filled, with atomic adds; no partials
   // and no reduction.  The order of the adds, and so the last bits, vary by run.
   int32_t atomic;
+  // contraction blocks per stage of the operand ring (1 or 2; 1 for BF16x3 and
+  // co-scheduled launches): a stage's loads complete on one barrier, and an SM's
+  // TMA streams from DRAM at about one stage per round trip slot whatever the
+  // stage's size, so streaming plans carry two blocks per stage
+  int32_t kps;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
 };
@@ -672,6 +678,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
       if (!X3) pdl_wait();  // the previous kernel on the stream (launched as its dependent) is done
+      const int kps = (X3 || args.kps != 2) ? 1 : 2;
+      const int nst = STAGES / kps;  // stages of the ring, kps block slots each
       for (int k = 0; !X3 && ok; ++k) {
         UnitRef ur;
         Unit w;
@@ -683,17 +691,16 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         const bool a_mn = DUAL ? ga.a_mn != 0 : A_MN;
         const int a_row0 = w.tm * C::TM + static_cast<int>(rank) * C::BM;
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        for (int kbs = w.kb0; kbs < w.kb1; kbs += kps) {
+          const int nb = min(kps, w.kb1 - kbs);  // blocks in this stage
           if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
             break;
           }
-          const uint32_t sa = base + stage * C::STAGE_BYTES;
-          const uint32_t sb = sa + C::A_BYTES;
           // a pair's loads all complete on the leader's full barrier
           const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
-          if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES);
+          if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES * nb);
           // (batched plans: every map has a trailing batch dimension)
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
             if (ga.batch > 1) {
@@ -713,26 +720,31 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             else
               tma_load_3d(dst, map, fb, 0, y, z);
           };
-          // MN-major: 64-column groups of 64 contraction rows (8 KB each)
-          if (a_mn && ga.a3d) {
-            load3(sa, mapA, kb * C::BK, a_row0 / 64);
-          } else if (a_mn) {
-            load(sa, mapA, a_row0, kb * C::BK);
-            load(sa + 8192, mapA, a_row0 + 64, kb * C::BK);
-          } else {
-            load(sa, mapA, kb * C::BK, a_row0);
-          }
-          if (B_MN && ga.b3d) {
-            load3(sb, mapB, kb * C::BK, b_row0 / 64);
-          } else if (B_MN) {
+          for (int j = 0; j < nb; ++j) {
+            const int kb = kbs + j;
+            const uint32_t sa = base + (stage * kps + j) * C::STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
+            // MN-major: 64-column groups of 64 contraction rows (8 KB each)
+            if (a_mn && ga.a3d) {
+              load3(sa, mapA, kb * C::BK, a_row0 / 64);
+            } else if (a_mn) {
+              load(sa, mapA, a_row0, kb * C::BK);
+              load(sa + 8192, mapA, a_row0 + 64, kb * C::BK);
+            } else {
+              load(sa, mapA, kb * C::BK, a_row0);
+            }
+            if (B_MN && ga.b3d) {
+              load3(sb, mapB, kb * C::BK, b_row0 / 64);
+            } else if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < C::BNH / 64; ++j) load(sb + 8192 * j, mapB, b_row0 + 64 * j, kb * C::BK);
-          } else {
-            load(sb, mapB, kb * C::BK, b_row0);
+              for (int g = 0; g < C::BNH / 64; ++g) load(sb + 8192 * g, mapB, b_row0 + 64 * g, kb * C::BK);
+            } else {
+              load(sb, mapB, kb * C::BK, b_row0);
+            }
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -760,6 +772,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
+      const int kps = (X3 || args.kps != 2) ? 1 : 2;
+      const int nst = STAGES / kps;
       for (int k = 0; ok; ++k, ++local) {
         UnitRef ur;
         Unit w;
@@ -775,56 +789,60 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kbs = kb0; kbs < kb1; kbs += kps) {
           if (!mbar_wait<PAIR>(full_bar(stage), phase)) {
             atomicOr(args.fault, kFaultMmaWait);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * C::STAGE_BYTES;
-          const uint32_t sb = sa + C::A_BYTES;
+          const int nb = min(kps, kb1 - kbs);
+          for (int j = 0; j < nb; ++j) {
+            const int kb = kbs + j;
+            const uint32_t sa = base + (stage * kps + j) * C::STAGE_BYTES;
+            const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk) {
-            if (X3) {
-              // bf16 hi/lo tiles, 32 contraction elements: K-major rows are 64 bytes
-              // (64-byte swizzle, 8-row groups 512 B apart, step 32 B per 16 elements);
-              // MN-major tiles keep 128-byte rows (64-element groups 4 KB apart).
-              auto d_a = [&](uint32_t t) {
-                return A_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
-              };
-              auto d_b = [&](uint32_t t) {
-                return B_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
-              };
-              const uint64_t a_hi = d_a(sa), a_lo = d_a(sa + C::A_HALF);
-              const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
-              // x*w ~ lo_x*hi_w + hi_x*lo_w + hi_x*hi_w (lo*lo dropped), small terms first
-              if (PAIR) {
-                mma_bf16_pair(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
-                mma_bf16_pair(d_tmem, a_hi, b_lo, IDESC, 1u);
-                mma_bf16_pair(d_tmem, a_hi, b_hi, IDESC, 1u);
-              } else {
-                mma_bf16(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
-                mma_bf16(d_tmem, a_hi, b_lo, IDESC, 1u);
-                mma_bf16(d_tmem, a_hi, b_hi, IDESC, 1u);
+            for (int kk = 0; kk < C::BK / 16; ++kk) {
+              if (X3) {
+                // bf16 hi/lo tiles, 32 contraction elements: K-major rows are 64 bytes
+                // (64-byte swizzle, 8-row groups 512 B apart, step 32 B per 16 elements);
+                // MN-major tiles keep 128-byte rows (64-element groups 4 KB apart).
+                auto d_a = [&](uint32_t t) {
+                  return A_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
+                };
+                auto d_b = [&](uint32_t t) {
+                  return B_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
+                };
+                const uint64_t a_hi = d_a(sa), a_lo = d_a(sa + C::A_HALF);
+                const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
+                // x*w ~ lo_x*hi_w + hi_x*lo_w + hi_x*hi_w (lo*lo dropped), small terms first
+                if (PAIR) {
+                  mma_bf16_pair(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                  mma_bf16_pair(d_tmem, a_hi, b_lo, IDESC, 1u);
+                  mma_bf16_pair(d_tmem, a_hi, b_hi, IDESC, 1u);
+                } else {
+                  mma_bf16(d_tmem, a_lo, b_hi, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                  mma_bf16(d_tmem, a_hi, b_lo, IDESC, 1u);
+                  mma_bf16(d_tmem, a_hi, b_hi, IDESC, 1u);
+                }
+                continue;
               }
-              continue;
+              // K-major: step 16 elements (32 bytes) along the swizzled row;
+              // MN-major: step 16 contraction rows (16 x 128 bytes).
+              const uint64_t ad = a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+              if (PAIR)
+                mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
-            // K-major: step 16 elements (32 bytes) along the swizzled row;
-            // MN-major: step 16 contraction rows (16 x 128 bytes).
-            const uint64_t ad = a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            if (PAIR)
-              mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-            else
-              mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           // frees the stage (in both CTAs of a pair) once these MMAs have read it
           if (PAIR)
             mma_commit_pair_multicast(empty_bar(stage), 0x3);
           else
             mma_commit(empty_bar(stage));
-          if (++stage == STAGES) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }

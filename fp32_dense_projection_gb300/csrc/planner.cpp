@@ -70,6 +70,20 @@ constexpr double kFuseGain = 0.97;            // co-schedule the backward pass o
 constexpr double kBwdLaunchNs = 5000.0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Contraction blocks per ring stage.  One SM's TMA completes about one stage's
+// loads per barrier round trip, whatever the stage's size, so two blocks per stage
+// (half as many stages) speed up both the short latency-bound calls and the
+// tensor-bound ones whose operands come from L2 (measured on GB300: -10% at
+// T = 64 and 1025, -5% for the 4096 -> 12288 forward at T = 16384).  Long DRAM
+// streams (units of >= 48 blocks, at most three per SM) keep single-block stages:
+// they need the deeper ring (+2-5% with two blocks per stage at T = 16173 and
+// 65537).  Only even ring depths split into two-block stages.
+int blocks_per_stage(int stages, int64_t kb_unit, int64_t units, int64_t slots, int forced) {
+  if (stages % 2 != 0) return 1;
+  if (forced == 1 || forced == 2) return forced;
+  return (kb_unit >= 48 && units <= 3 * slots) ? 1 : 2;
+}
 int64_t ffma_stage_k_host(int bn) { return 4096 / bn; }  // contraction elements per stage of the SIMT program
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
@@ -463,6 +477,9 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   // (stream-K: every slot, each with its share of the blocks)
   plan.grid = static_cast<int>((plan.stream_k ? slots_all : std::min<int64_t>(plan.units, slots_all)) *
                                (plan.pair ? 2 : 1));
+  // (BF16x3 keeps one block per stage: its converter warps fill the stages block by block)
+  const int64_t kb_unit = plan.full_units > 0 ? plan.nkb : ceil_div(plan.nkb, plan.splits);
+  plan.kps = v.terms == 1 ? blocks_per_stage(plan.stages, kb_unit, plan.units, slots_all, o.kps) : 1;
 
   // workspace layout: [split partials | router's pre-split operands]
   size_t off = 0;
@@ -600,6 +617,8 @@ bool make_plan_bwd(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int 
             best.model_ns = t;
             const int64_t slots = pair ? sm / 2 : sm;
             best.grid = static_cast<int>(std::min<int64_t>(d.units + w.units, slots) * (pair ? 2 : 1));
+            // (one ring for both problems' units)
+            best.kps = blocks_per_stage(d.stages, std::max(d.nkb, w.nkb), d.units + w.units, slots, o.kps);
           }
         }
       }

@@ -80,6 +80,12 @@ struct Plan {
   // Non-deterministic (deterministic = 0, FP32 output): the split units add their FP32
   // partials into the zero-filled output with atomic adds (no partials, no reduction).
   bool atomic = false;
+  // Contraction blocks per stage of the operand ring (1 or 2): each stage's loads
+  // complete on one barrier, and one SM's TMA streams from DRAM at about one stage
+  // per barrier round trip whatever the stage's size (measured on GB300), so plans
+  // that stream their operands from DRAM move two blocks per stage (half as many
+  // stages).  BF16x3 plans keep one.
+  int kps = 1;
 };
 
 // Shared-memory pipeline depth: as many stages of a 128 x 64 A tile plus a b_rows
@@ -125,6 +131,7 @@ struct Overrides {
   int ffma = -1;  // router: 0 tensor-core BF16x3 program, 1 SIMT FP32 program
   int stream_k = -1;  // 0 never, 1 only stream-K candidates (where the shape admits one)
   int atomic = -1;    // non-deterministic calls: 0 ordered split sums, 1 atomic ones (where admitted)
+  int kps = 0;        // > 0: contraction blocks per ring stage (1 or 2; BF16 plans only)
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,
@@ -147,6 +154,7 @@ struct BwdPlan {
   bool wgrad_first = false;  // fused: the weight gradient's units come first in the list
   Plan dgrad, wgrad;         // fused: whole-K plans of one tiling; else the single-op plans
   int grid = 0;              // fused: CTAs of the launch
+  int kps = 1;               // fused: contraction blocks per ring stage (both problems)
   double model_ns = 0.0;     // the chosen form's modelled duration
   double separate_ns = 0.0;  // the two single-op launches' modelled duration
   size_t ws_bytes = 0;       // workspace (the two single-op calls share one)

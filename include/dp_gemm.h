@@ -278,8 +278,9 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * two give the same bits), DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls
  * or as one co-scheduled launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never;
  * 1: a stream-K plan where the shape admits one), DP_FORCE_ATOMIC (calls with
- * deterministic = 0: 0 ordered split sums, 1 atomic ones wherever admitted).  A forced plan is still deterministic and keeps the
- * accumulation-length bound. */
+ * deterministic = 0: 0 ordered split sums, 1 atomic ones wherever admitted),
+ * DP_FORCE_KPS (1 / 2 contraction blocks per ring stage; BF16x3 plans keep 1).
+ * A forced plan is still deterministic and keeps the accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of
  * (op, T, N, K, out, sm_count), so a workspace sized here fits the call. */
@@ -322,7 +323,9 @@ typedef struct dp_plan_info {
                                  contraction elements per stage); BF16 ops: 0 */
     int32_t atomic;           /* 1: split units add into the zero-filled FP32 output with
                                  atomic adds (deterministic = 0 only) */
-    int32_t reserved3;
+    int32_t blocks_per_stage; /* contraction blocks per stage of the operand ring (1 or 2: a
+                                 stage's loads complete on one barrier, so streaming plans
+                                 carry two blocks per stage in half as many stages) */
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs
@@ -344,7 +347,8 @@ typedef struct dp_bwd_plan_info {
     int32_t fused;            /* 1: one co-scheduled launch; 0: two single-op calls */
     int32_t wgrad_first;      /* co-scheduled: the weight gradient's tiles are dealt first */
     int32_t grid;             /* co-scheduled: persistent CTAs of the launch (else 0) */
-    int32_t reserved;
+    int32_t blocks_per_stage; /* co-scheduled: contraction blocks per ring stage, for both
+                                 problems (else 0; each call's own is in dgrad / wgrad) */
     double model_us;          /* modelled duration of the chosen form */
     double separate_us;       /* modelled duration of the two single-op calls */
     uint64_t workspace_bytes; /* == dp_workspace_size_bwd() */

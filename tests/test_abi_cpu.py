@@ -108,6 +108,9 @@ def test_plan_is_valid(op, T, N, K):
     assert not p["swap_ab"] or op.endswith("wgrad")
     if op.startswith("router"):  # the pre-split bf16 operands live in the workspace
         assert p["workspace_bytes"] > 0
+    # blocks per ring stage: 1 or 2, two only on an even ring depth, one for BF16x3
+    assert p["blocks_per_stage"] in (1, 2) and p["stages"] % p["blocks_per_stage"] == 0
+    assert not x3 or p["blocks_per_stage"] == 1
     # pure function: same answer twice, and the workspace query agrees
     assert dp.plan(op, T, N, K, sm_count=SM) == p
     assert dp.workspace_size(op, T, N, K, sm_count=SM) == p["workspace_bytes"]
@@ -439,3 +442,30 @@ def test_atomic_override(monkeypatch):
     assert dp.plan("dgrad", 200, 512, 2048, out_f32=False, sm_count=SM, deterministic=False)["atomic"] == 0
     monkeypatch.setenv("DP_FORCE_ATOMIC", "0")
     assert dp.plan("dgrad", 200, 512, 2048, out_f32=True, sm_count=SM, deterministic=False)["atomic"] == 0
+
+
+@pytest.mark.parametrize("op,T,N,K,kps", [
+    ("fwd", 64, 1024, 4096, 2), ("dgrad", 64, 1024, 4096, 2),      # short, latency-bound units
+    ("wgrad", 1025, 64, 4096, 2),
+    ("fwd", 16384, 12288, 4096, 2), ("dgrad", 16384, 12288, 4096, 2),  # many waves of L2-fed units
+    ("wgrad", 16384, 12288, 4096, 2),
+    ("wgrad", 16173, 64, 4096, 1), ("wgrad", 65537, 64, 4096, 1),     # long DRAM streams, one wave
+    ("wgrad", 65537, 512, 4096, 1), ("dgrad", 1024, 12288, 4096, 1),
+    ("router_fwd", 1024, 256, 4096, 1), ("router_wgrad", 1024, 256, 4096, 1)])
+def test_blocks_per_stage_rule(op, T, N, K, kps):
+    """Two contraction blocks per ring stage except for long streams (units of >= 48
+    blocks, at most three per SM) and the BF16x3 program."""
+    assert dp.plan(op, T, N, K, sm_count=SM, out_f32=op.startswith("router"))["blocks_per_stage"] == kps
+
+
+def test_blocks_per_stage_override(monkeypatch):
+    monkeypatch.setenv("DP_FORCE_KPS", "1")
+    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["blocks_per_stage"] == 1
+    monkeypatch.setenv("DP_FORCE_KPS", "2")
+    assert dp.plan("wgrad", 16173, 64, 4096, sm_count=SM)["blocks_per_stage"] == 2
+    # the BF16x3 program keeps one block per stage; the co-scheduled backward takes it too
+    assert dp.plan("router_fwd", 1024, 256, 4096, sm_count=SM, out_f32=True)["blocks_per_stage"] == 1
+    b = dp.plan_bwd(1024, 1024, 4096, sm_count=SM)
+    assert b["fused"] == 1 and b["blocks_per_stage"] == 2
+    monkeypatch.setenv("DP_FORCE_KPS", "1")
+    assert dp.plan_bwd(1024, 1024, 4096, sm_count=SM)["blocks_per_stage"] == 1

@@ -78,11 +78,13 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // T = 64 and 1025, -5% for the 4096 -> 12288 forward at T = 16384).  Long DRAM
 // streams (units of >= 48 blocks, at most three per SM) keep single-block stages:
 // they need the deeper ring (+2-5% with two blocks per stage at T = 16173 and
-// 65537).  Only even ring depths split into two-block stages.
+// 65537) unless their ring has eight block slots (four two-block stages).  Only
+// even ring depths split into two-block stages.
+bool long_stream(int64_t kb_unit, int64_t units, int64_t slots) { return kb_unit >= 48 && units <= 3 * slots; }
 int blocks_per_stage(int stages, int64_t kb_unit, int64_t units, int64_t slots, int forced) {
   if (stages % 2 != 0) return 1;
   if (forced == 1 || forced == 2) return forced;
-  return (kb_unit >= 48 && units <= 3 * slots) ? 1 : 2;
+  return (stages < 8 && long_stream(kb_unit, units, slots)) ? 1 : 2;
 }
 int64_t ffma_stage_k_host(int bn) { return 4096 / bn; }  // contraction elements per stage of the SIMT program
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -439,7 +441,17 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
       sv.batch = batch;
       Choice cs;
       search(sv, plan.nkb, sm, out_bytes, o, &cs, atomic_ok);
-      if (cs.have && (!c.have || cs.t < c.t * 0.97 || o.swap == 1)) {
+      // Thin N (<= 64) streamed over a long contraction: the swapped 128 x 64 tiles
+      // (eight block slots, two blocks per stage) stream X faster than tiles with N
+      // as their 128 rows, half of them padding, in six or four slots (measured
+      // 35.3 -> 32.4 us at T = 16173, 4096 -> 64, and 45.2 -> 39.5 us at 5120 -> 48);
+      // the rates of the model do not tell them apart, so this is a rule, taken
+      // where the swapped plan models within 10%
+      const int64_t s_tiles = ceil_div(sv.gm, kBlockM) * ceil_div(sv.gn, cs.tiling.bn);
+      const int64_t s_units = cs.full + (s_tiles - cs.full) * cs.splits;
+      const bool thin_stream = cs.have && !cs.tiling.pair && cs.tiling.bn == 64 && !cs.stream_k && N <= 64 &&
+                               long_stream(cs.full > 0 ? plan.nkb : ceil_div(plan.nkb, cs.splits), s_units, sm);
+      if (cs.have && (!c.have || cs.t < c.t * 0.97 || o.swap == 1 || (thin_stream && cs.t < c.t * 1.10))) {
         c = cs;
         plan.swap = true;
         v = sv;

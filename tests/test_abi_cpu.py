@@ -449,12 +449,14 @@ def test_atomic_override(monkeypatch):
     ("wgrad", 1025, 64, 4096, 2),
     ("fwd", 16384, 12288, 4096, 2), ("dgrad", 16384, 12288, 4096, 2),  # many waves of L2-fed units
     ("wgrad", 16384, 12288, 4096, 2),
-    ("wgrad", 16173, 64, 4096, 1), ("wgrad", 65537, 64, 4096, 1),     # long DRAM streams, one wave
+    ("wgrad", 16173, 128, 4096, 1), ("wgrad", 65537, 64, 4096, 1),    # long DRAM streams, one wave
     ("wgrad", 65537, 512, 4096, 1), ("dgrad", 1024, 12288, 4096, 1),
+    ("wgrad", 16173, 64, 4096, 2),   # a long stream in eight block slots (swapped 128 x 64 tiles)
     ("router_fwd", 1024, 256, 4096, 1), ("router_wgrad", 1024, 256, 4096, 1)])
 def test_blocks_per_stage_rule(op, T, N, K, kps):
     """Two contraction blocks per ring stage except for long streams (units of >= 48
-    blocks, at most three per SM) and the BF16x3 program."""
+    blocks, at most three per SM) in rings of fewer than eight block slots, and the
+    BF16x3 program."""
     assert dp.plan(op, T, N, K, sm_count=SM, out_f32=op.startswith("router"))["blocks_per_stage"] == kps
 
 
@@ -462,10 +464,22 @@ def test_blocks_per_stage_override(monkeypatch):
     monkeypatch.setenv("DP_FORCE_KPS", "1")
     assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["blocks_per_stage"] == 1
     monkeypatch.setenv("DP_FORCE_KPS", "2")
-    assert dp.plan("wgrad", 16173, 64, 4096, sm_count=SM)["blocks_per_stage"] == 2
+    assert dp.plan("wgrad", 16173, 128, 4096, sm_count=SM)["blocks_per_stage"] == 2
     # the BF16x3 program keeps one block per stage; the co-scheduled backward takes it too
     assert dp.plan("router_fwd", 1024, 256, 4096, sm_count=SM, out_f32=True)["blocks_per_stage"] == 1
     b = dp.plan_bwd(1024, 1024, 4096, sm_count=SM)
     assert b["fused"] == 1 and b["blocks_per_stage"] == 2
     monkeypatch.setenv("DP_FORCE_KPS", "1")
     assert dp.plan_bwd(1024, 1024, 4096, sm_count=SM)["blocks_per_stage"] == 1
+
+
+@pytest.mark.parametrize("T,N,K,swap", [(16173, 64, 4096, 1), (16173, 48, 5120, 1), (16173, 128, 4096, 0),
+                                        (1025, 64, 4096, 0), (65537, 64, 4096, 0)])
+def test_thin_stream_orientation(T, N, K, swap):
+    """N <= 64 over a long contraction takes the swapped 128 x 64 tiles, whose ring has
+    eight block slots, where that plan keeps one wave; short contractions and
+    plans that would need a second wave keep N as the tile rows."""
+    p = dp.plan("wgrad", T, N, K, sm_count=SM)
+    assert p["swap_ab"] == swap
+    if swap:
+        assert p["block_n"] == 64 and p["cta_pair"] == 0 and p["units"] <= SM and p["blocks_per_stage"] == 2

@@ -406,6 +406,20 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   a.sk_work = p.tiles * p.nkb;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
   a.kps = (!x3 && p.kps == 2 && p.stages % 2 == 0) ? 2 : 1;
+  // Whole-tile results leave through TMA stores of the epilogue's staged blocks:
+  // FP32 outputs always, BF16 outputs of units of >= 8 contraction blocks (measured on
+  // GB300: -4 to -15% for FP32-output calls whose epilogue is their bound, <= 1% either
+  // way for the long BF16 ones, 2-4% slower for BF16 units of 2 blocks).  The
+  // transposed store of the swapped weight gradient keeps its own path;
+  // DP_FORCE_TMA_STORE=0 / 1 turns them off / on everywhere else (tests, comparisons).
+  const char* ts = std::getenv("DP_FORCE_TMA_STORE");
+  const int64_t kb_unit = p.full_units > 0 ? p.nkb : (p.nkb + p.splits - 1) / p.splits;
+  const bool want_tma_store = ts ? std::atoi(ts) != 0 : (p.out_f32 != 0 || kb_unit >= 8);
+  a.tma_store = (!p.out_trans && p.gm > 0 && want_tma_store &&
+                 make_map(&a.tmO, out, p.gm, p.gn, ldo, 32, p.out_f32 != 0, p.out_f32 ? 32 : 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B, 0, nb, bso))
+                    ? 1
+                    : 0;
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;

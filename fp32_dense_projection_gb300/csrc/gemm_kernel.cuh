@@ -44,6 +44,12 @@
 namespace dp {
 
 struct GemmArgs {
+  // tma_store = 1: the output as a TMA map ([batch][gm][gn], leading dimension ldo;
+  // boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16 columns) with the 128-byte
+  // swizzle the epilogue stages them in): whole-tile results leave through TMA
+  // stores instead of the epilogue warps' own stores
+  CUtensorMap tmO;
+  int32_t tma_store;
   int64_t gm, gn;      // output rows and columns of the contraction view
   int32_t nkb;         // 64-wide contraction blocks in total
   int32_t splits;      // contraction splits of each split tile
@@ -338,6 +344,19 @@ __device__ __forceinline__ void stage_block32(const GemmArgs& a, uint32_t buf, i
                    make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
                               pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7])));
   }
+  __syncwarp();
+}
+
+// BF16 half h (columns [32h, 32h + 32)) of a 32 x 64 block staged for a TMA store:
+// rows of 128 bytes, 16-byte chunk j of row r at chunk j ^ (r % 8) (the 128-byte
+// swizzle of the output map).  Lane i holds row i.
+__device__ __forceinline__ void stage_half64_bf16(uint32_t buf, int lane, int h, const float (&v)[32]) {
+  __syncwarp();  // the block's previous reader is done (and half 0 is written before half 1)
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_u4(buf + lane * 128 + (((4 * h + j) ^ (lane & 7)) << 4),
+                 make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                            pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7])));
   __syncwarp();
 }
 
@@ -988,6 +1007,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
       if (!w.split || ga.atomic) {
+        const bool tstore = ga.tma_store && !w.split;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -997,7 +1017,34 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          // (a split unit here: a non-deterministic plan's, added into the zero-filled output)
+          if (tstore) {
+            // Stage and hand to TMA (which clips rows >= gm, columns >= gn) 4 KB at a
+            // time: an FP32 32 x 32 block, or two BF16 32 x 32 blocks side by side
+            // (32 rows of 128 bytes).  The warp's previous bulk store must have read
+            // the staging block before it is rewritten.
+            const int h = ga.out_f32 ? 0 : (c & 1);
+            if (h == 0 && lane == 0) bulk_wait_group_read0();
+            if (ga.out_f32)
+              stage_block32(ga, ebuf, lane, v);
+            else
+              stage_half64_bf16(ebuf, lane, h, v);
+            if (ga.out_f32 || h == 1) {
+              fence_proxy_async_shared();
+              __syncwarp();
+              const int32_t x = static_cast<int32_t>(n0 + (c - h) * 32), y = static_cast<int32_t>(m0);
+              if (lane == 0 && x < ga.gn && y < ga.gm) {  // (blocks wholly outside: nothing to store)
+                if (ga.batch > 1)
+                  tma_store_3d(&ga.tmO, ebuf, x, y, w.b);
+                else
+                  tma_store_2d(&ga.tmO, ebuf, x, y);
+                bulk_commit_group();
+              }
+            }
+            continue;
+          }
+          // (a split unit here: a non-deterministic plan's, added into the zero-filled output;
+          // its staging waits for this warp's earlier bulk stores to have read the block)
+          if (ga.tma_store && lane == 0) bulk_wait_group_read0();
           store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v, w.split);
         }
       } else {
@@ -1020,6 +1067,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
     }
+    // this warp's bulk stores have completed before the CTA (and its shared memory) goes
+    if (lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();

@@ -251,3 +251,66 @@ def test_dependent_calls_keep_their_order():
         bits = torch.int16 if u.dtype == torch.bfloat16 else torch.int32
         assert torch.equal(u.view(bits), v.view(bits))
     no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K", [("fwd", 300, 520, 1000), ("dgrad", 300, 520, 1000), ("wgrad", 300, 520, 1000),
+                                      ("fwd", 16384, 1024, 512), ("wgrad", 64, 1024, 4096), ("fwd", 64, 40, 256),
+                                      ("router_dgrad", 1000, 256, 4096), ("router_fwd", 300, 256, 4096)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_tma_store_matches_direct_store(monkeypatch, op, T, N, K, out_dtype):
+    # Whole tiles leave through TMA stores of the staged 32-row blocks, or through the
+    # epilogue warps' own stores: the same values, so the same bits, ragged edges
+    # clipped either way (the output sits in a NaN-padded wider buffer)
+    if op.startswith("router") and out_dtype == torch.bfloat16:
+        pytest.skip("router output is FP32")
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K, seed=5).items()}
+    a, b = operands(op, c)
+    kw = {} if op.startswith("router") else {"out_dtype": out_dtype}
+    if not op.startswith("router"):
+        monkeypatch.setenv("DP_FORCE_SPLITS", "1")  # whole-K tiles: the results the stores carry
+    outs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("DP_FORCE_TMA_STORE", mode)
+        probe = gpu(op, a, b, **kw)
+        R, C = probe.shape
+        wide = torch.full((R, C + 16), float("nan"), dtype=probe.dtype, device=DEV)
+        view = wide[:, 8:8 + C]
+        gpu(op, a, b, out=view, **kw)
+        torch.cuda.synchronize()
+        assert torch.isnan(wide[:, :8].float()).all() and torch.isnan(wide[:, 8 + C:].float()).all(), mode
+        outs[mode] = view.clone()
+    bits = torch.int16 if outs["1"].dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(outs["1"].view(bits), outs["0"].view(bits))
+    no_device_fault()
+
+
+@pytest.mark.parametrize("weight_layout", ["nk", "kn"])
+def test_tma_store_matches_direct_store_batched_and_bwd(monkeypatch, weight_layout):
+    H, T, N, K = 6, 300, 192, 136
+    g = torch.Generator().manual_seed(11)
+    X = torch.randn(T, H, K, generator=g).bfloat16().to(DEV).permute(1, 0, 2)
+    dY = torch.randn(T, H, N, generator=g).bfloat16().to(DEV).permute(1, 0, 2)
+    W = (torch.randn(H, N, K, generator=g) / 16).bfloat16().to(DEV)
+    if weight_layout == "kn":
+        W = W.transpose(1, 2).contiguous()
+    # (the backward pass, co-scheduled where a tiling admits it: T = 300, N = 520, K = 1000)
+    X2 = torch.randn(300, 1000, generator=g).bfloat16().to(DEV)
+    W2 = (torch.randn(520, 1000, generator=g) / 32).bfloat16().to(DEV)
+    dY2 = torch.randn(300, 520, generator=g).bfloat16().to(DEV)
+    res = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("DP_FORCE_TMA_STORE", mode)
+        r = []
+        for od in (torch.bfloat16, torch.float32):
+            r.append(dp.dp_gemm_fwd_batched(X, W, out_dtype=od, weight_layout=weight_layout))
+            r.append(dp.dp_gemm_dgrad_batched(dY, W, out_dtype=od, weight_layout=weight_layout))
+            r.append(dp.dp_gemm_wgrad_batched(dY, X, out_dtype=od, weight_layout=weight_layout))
+            monkeypatch.setenv("DP_FORCE_FUSE", "1")
+            r.extend(dp.dp_gemm_bwd(dY2, X2, W2, dx_dtype=od, dw_dtype=od))
+            monkeypatch.delenv("DP_FORCE_FUSE")
+        torch.cuda.synchronize()
+        res[mode] = r
+    for i, (x, y) in enumerate(zip(res["1"], res["0"])):
+        bits = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(x.contiguous().view(bits), y.contiguous().view(bits)), i
+    no_device_fault()

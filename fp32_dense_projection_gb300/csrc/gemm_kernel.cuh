@@ -11,9 +11,11 @@
 //               accumulators so the epilogue of a tile overlaps the next tile's
 //               main loop;
 //   warps 4..7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//               32*(w%4)...), BF16 round-to-nearest-even or FP32, 16-byte stores;
-//               for split units, FP32 partial tiles in the workspace and a
-//               last-arriver reduction in ascending split order.
+//               32*(w%4)...), BF16 round-to-nearest-even or FP32, staged in
+//               shared memory and written by TMA stores or 16-byte stores; for
+//               split units, FP32 partial tiles in the workspace, summed in
+//               ascending split order by the tile's cluster after the main loop
+//               (cluster_fixup_sum) or by the reduction kernel (split_reduce.cu).
 //
 // Operand "majorness" is a template parameter.  A K-major operand is a row-major
 // [rows][contraction] matrix (one TMA box of 64 contraction elements x rows);

@@ -46,12 +46,6 @@
 namespace dp {
 
 struct GemmArgs {
-  // tma_store = 1: the output as a TMA map ([batch][gm][gn], leading dimension ldo;
-  // boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16 columns) with the 128-byte
-  // swizzle the epilogue stages them in): whole-tile results leave through TMA
-  // stores instead of the epilogue warps' own stores
-  CUtensorMap tmO;
-  int32_t tma_store;
   int64_t gm, gn;      // output rows and columns of the contraction view
   int32_t nkb;         // 64-wide contraction blocks in total
   int32_t splits;      // contraction splits of each split tile
@@ -95,6 +89,12 @@ struct GemmArgs {
   int32_t kps;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
+  // tma_store = 1: whole-tile results leave through TMA stores instead of the
+  // epilogue warps' own stores, with tmO the output as a TMA map ([batch][gm][gn],
+  // leading dimension ldo; boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16
+  // columns) with the 128-byte swizzle the epilogue stages them in)
+  int32_t tma_store;
+  CUtensorMap tmO;
 };
 
 // X3: the FP32 router's BF16x3 mode.  A stage of the MMA ring then holds the bf16
@@ -1008,8 +1008,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       void* outb = out_at(ga, w.b);
       const int64_t n0 = static_cast<int64_t>(tn) * BN;
       const uint32_t tcol = lane_addr + static_cast<uint32_t>(acc * BN);
-      if (!w.split || ga.atomic) {
-        const bool tstore = ga.tma_store && !w.split;
+      if ((!w.split && !ga.tma_store) || (w.split && ga.atomic)) {
+        // (the warp's own stores; a split unit here is a non-deterministic plan's, added
+        // into the zero-filled output.  Its staging waits for earlier bulk stores to
+        // have read the block.)
+        if (ga.tma_store && lane == 0) bulk_wait_group_read0();
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -1019,35 +1022,40 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          if (tstore) {
-            // Stage and hand to TMA (which clips rows >= gm, columns >= gn) 4 KB at a
-            // time: an FP32 32 x 32 block, or two BF16 32 x 32 blocks side by side
-            // (32 rows of 128 bytes).  The warp's previous bulk store must have read
-            // the staging block before it is rewritten.
-            const int h = ga.out_f32 ? 0 : (c & 1);
-            if (h == 0 && lane == 0) bulk_wait_group_read0();
-            if (ga.out_f32)
-              stage_block32(ga, ebuf, lane, v);
-            else
-              stage_half64_bf16(ebuf, lane, h, v);
-            if (ga.out_f32 || h == 1) {
-              fence_proxy_async_shared();
-              __syncwarp();
-              const int32_t x = static_cast<int32_t>(n0 + (c - h) * 32), y = static_cast<int32_t>(m0);
-              if (lane == 0 && x < ga.gn && y < ga.gm) {  // (blocks wholly outside: nothing to store)
-                if (ga.batch > 1)
-                  tma_store_3d(&ga.tmO, ebuf, x, y, w.b);
-                else
-                  tma_store_2d(&ga.tmO, ebuf, x, y);
-                bulk_commit_group();
-              }
-            }
-            continue;
-          }
-          // (a split unit here: a non-deterministic plan's, added into the zero-filled output;
-          // its staging waits for this warp's earlier bulk stores to have read the block)
-          if (ga.tma_store && lane == 0) bulk_wait_group_read0();
           store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v, w.split);
+        }
+      } else if (!w.split) {
+        // Stage and hand to TMA (which clips rows >= gm, columns >= gn) 4 KB at a
+        // time: an FP32 32 x 32 block, or two BF16 32 x 32 blocks side by side (32
+        // rows of 128 bytes).  The warp's previous bulk store must have read the
+        // staging block before it is rewritten.
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tcol + c * 32, r);
+          tmem_wait_ld();
+          if (c == BN / 32 - 1) release_acc(acc);  // accumulator may be reused
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          const int h = ga.out_f32 ? 0 : (c & 1);
+          if (h == 0 && lane == 0) bulk_wait_group_read0();
+          if (ga.out_f32)
+            stage_block32(ga, ebuf, lane, v);
+          else
+            stage_half64_bf16(ebuf, lane, h, v);
+          if (ga.out_f32 || h == 1) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            const int32_t x = static_cast<int32_t>(n0 + (c - h) * 32), y = static_cast<int32_t>(m0);
+            if (lane == 0 && x < ga.gn && y < ga.gm) {  // (blocks wholly outside: nothing to store)
+              if (ga.batch > 1)
+                tma_store_3d(&ga.tmO, ebuf, x, y, w.b);
+              else
+                tma_store_2d(&ga.tmO, ebuf, x, y);
+              bulk_commit_group();
+            }
+          }
         }
       } else {
         // FP32 partial of this split, laid out [BN/4][128] float4 so a warp's

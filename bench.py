@@ -142,7 +142,10 @@ class ClockSampler:
 # ------------------------------------------------------------ GPU arm
 
 def run_profile_case(args, local):
-    """A small single-op case for ncu captures: one op, `--profile-T` tokens, a few GB."""
+    """A small single-op case for ncu captures: one op, `--profile-T` tokens, a few GB.
+    BF16 ops take N, K (default 4096 -> 12288); router ops FP32 operands (N default 256
+    experts); batched ops `--profile-B` per-head problems of T x K -> N over [T, B, D]
+    views."""
     import fp32_dense_projection_gb300 as dp
     from fp32_dense_projection_gb300 import build as dpbuild
 
@@ -151,29 +154,54 @@ def run_profile_case(args, local):
     torch.cuda.set_device(device)
     dp.init(local)
     op, T = args.profile_op, args.profile_T
-    N, K = (args.profile_N or N_OUT), (args.profile_K or K_IN)
+    router = op.startswith("router")
+    batched = op.endswith("_batched")
+    N = args.profile_N or (256 if router else N_OUT)
+    K = args.profile_K or K_IN
     g = torch.Generator(device=device)
     g.manual_seed(7)
-    X = torch.randn(T, K, generator=g, device=device).to(torch.bfloat16)
-    W = (torch.randn(N, K, generator=g, device=device) / 64.0).to(torch.bfloat16)
-    dY = torch.randn(T, N, generator=g, device=device).to(torch.bfloat16)
-    a, b = {"fwd": (X, W), "dgrad": (dY, W), "wgrad": (dY, X)}[op]
-    fn = {"fwd": dp.dp_gemm_fwd, "dgrad": dp.dp_gemm_dgrad, "wgrad": dp.dp_gemm_wgrad}[op]
-    out_dtype = torch.float32 if args.profile_f32 else torch.bfloat16
-    out = fn(a, b, out_dtype=out_dtype)
+    out_dtype = torch.float32 if (args.profile_f32 or router) else torch.bfloat16
+    if router:
+        X = torch.randn(T, K, generator=g, device=device)
+        W = torch.randn(N, K, generator=g, device=device) * 0.02
+        dY = torch.randn(T, N, generator=g, device=device)
+        a, b = {"router_fwd": (X, W), "router_dgrad": (dY, W), "router_wgrad": (dY, X)}[op]
+        fn = {"router_fwd": dp.router_fwd, "router_dgrad": dp.router_dgrad, "router_wgrad": dp.router_wgrad}[op]
+        call = lambda out=None: fn(a, b, out=out)
+        plan = dp.plan(op, T, N, K, True)
+    elif batched:
+        B = args.profile_B
+        X = torch.randn(T, B, K, generator=g, device=device).to(torch.bfloat16).permute(1, 0, 2)
+        dY = torch.randn(T, B, N, generator=g, device=device).to(torch.bfloat16).permute(1, 0, 2)
+        W = (torch.randn(B, N, K, generator=g, device=device) / 16.0).to(torch.bfloat16)
+        base = op[:-len("_batched")]
+        a, b = {"fwd": (X, W), "dgrad": (dY, W), "wgrad": (dY, X)}[base]
+        fn = {"fwd": dp.dp_gemm_fwd_batched, "dgrad": dp.dp_gemm_dgrad_batched, "wgrad": dp.dp_gemm_wgrad_batched}[base]
+        call = lambda out=None: fn(a, b, out=out, out_dtype=out_dtype)
+        plan = dp.plan_batched(base, B, T, N, K, out_dtype == torch.float32)
+    else:
+        X = torch.randn(T, K, generator=g, device=device).to(torch.bfloat16)
+        W = (torch.randn(N, K, generator=g, device=device) / 64.0).to(torch.bfloat16)
+        dY = torch.randn(T, N, generator=g, device=device).to(torch.bfloat16)
+        a, b = {"fwd": (X, W), "dgrad": (dY, W), "wgrad": (dY, X)}[op]
+        fn = {"fwd": dp.dp_gemm_fwd, "dgrad": dp.dp_gemm_dgrad, "wgrad": dp.dp_gemm_wgrad}[op]
+        call = lambda out=None: fn(a, b, out=out, out_dtype=out_dtype)
+        plan = dp.plan(op, T, N, K, out_dtype == torch.float32)
+    out = call()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     times = []
     for _ in range(args.steps):
         ev[0].record()
-        fn(a, b, out=out, out_dtype=out_dtype)
+        call(out)
         ev[1].record()
         torch.cuda.synchronize()
         times.append(ev[0].elapsed_time(ev[1]))
     assert dp.device_error() == 0
-    flop = 2.0 * T * N * K
+    flop = 2.0 * T * N * K * (args.profile_B if batched else 1)
     us = statistics.median(times) * 1e3
-    return {"profile_case": op, "T": T, "N": N, "K": K, "out": "f32" if args.profile_f32 else "bf16",
-            "us": round(us, 2), "tflops": round(flop / us / 1e6, 1), "plan": dp.plan(op, T, N, K, args.profile_f32)}
+    return {"profile_case": op, "T": T, "N": N, "K": K, "B": args.profile_B if batched else 1,
+            "out": "f32" if out_dtype == torch.float32 else "bf16",
+            "us": round(us, 2), "tflops": round(flop / us / 1e6, 1), "plan": plan}
 
 
 def run_gpu(args, world, rank, local):
@@ -713,12 +741,15 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-op", choices=["fwd", "dgrad", "wgrad"], default=None,
+    ap.add_argument("--profile-op", default=None,
+                    choices=["fwd", "dgrad", "wgrad", "router_fwd", "router_dgrad", "router_wgrad",
+                             "fwd_batched", "dgrad_batched", "wgrad_batched"],
                     help="run only a small single-op case (for ncu captures)")
     ap.add_argument("--profile-T", type=int, default=4096)
     ap.add_argument("--profile-N", type=int, default=0)
     ap.add_argument("--profile-K", type=int, default=0)
     ap.add_argument("--profile-f32", action="store_true")
+    ap.add_argument("--profile-B", type=int, default=128, help="batched profile cases: problems (heads)")
     ap.add_argument("--suite", default=None,
                     help="comma list of cfg1..cfg5 (and 'batched'): per-op eager/graph/kernel-span measurements")
     ap.add_argument("--suite-reps", type=int, default=10)

@@ -221,8 +221,9 @@ int env_int(const char* name) {
 
 // Plan overrides for tuning and tests, read on every call (DP_FORCE_CLUSTER_SUM=0,
 // read in cluster_fixup, keeps split sums in the reduction kernel): DP_FORCE_BN,
-// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS, DP_FORCE_KPS (> 0 forces), DP_FORCE_SWAP (0
-// or 1: the weight-gradient orientation), DP_FORCE_PAIR (0 or 1: single-CTA or
+// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS, DP_FORCE_KPS, DP_FORCE_GROUP (> 0 forces),
+// DP_FORCE_RASTER_M and DP_FORCE_SWAP (0 or 1: raster groups of row tiles, the
+// weight-gradient orientation), DP_FORCE_PAIR (0 or 1: single-CTA or
 // CTA-pair tiles), DP_FORCE_FUSE, DP_FORCE_FFMA, DP_FORCE_STREAM_K and
 // DP_FORCE_ATOMIC (0 or 1).  Unset in normal use.
 Overrides env_overrides() {
@@ -243,6 +244,9 @@ Overrides env_overrides() {
   const char* at = std::getenv("DP_FORCE_ATOMIC");
   o.atomic = at ? std::atoi(at) : -1;
   o.kps = env_int("DP_FORCE_KPS");
+  o.group = env_int("DP_FORCE_GROUP");
+  const char* rm = std::getenv("DP_FORCE_RASTER_M");
+  o.raster_m = rm ? std::atoi(rm) : -1;
   return o;
 }
 
@@ -265,13 +269,15 @@ bool plan_for(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Plan
           static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
               (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.ffma + 1) * 7919 +
               static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.atomic + 1) * 1299709 +
-              static_cast<uint64_t>(o.kps) * 15485863);
+              static_cast<uint64_t>(o.kps) * 15485863 + static_cast<uint64_t>(o.group) * 32452843 +
+              static_cast<uint64_t>(o.raster_m + 1) * 49979687);
   h = mix(h, static_cast<uint64_t>(batch) * 4 + static_cast<uint64_t>(w_kn) * 2 + static_cast<uint64_t>(deterministic));
   PlanEntry& e = t_plans[h & (kPlanCacheSize - 1)];
   if (e.valid && e.op == op && e.T == T && e.N == N && e.K == K && e.out_f32 == out_f32 && e.sm == sm &&
       e.batch == batch && e.w_kn == w_kn && e.det == deterministic && e.o.bn == o.bn && e.o.splits == o.splits &&
       e.o.tail_splits == o.tail_splits && e.o.swap == o.swap && e.o.pair == o.pair && e.o.ffma == o.ffma &&
-      e.o.stream_k == o.stream_k && e.o.atomic == o.atomic && e.o.kps == o.kps) {
+      e.o.stream_k == o.stream_k && e.o.atomic == o.atomic && e.o.kps == o.kps && e.o.group == o.group &&
+      e.o.raster_m == o.raster_m) {
     *plan = e.plan;
     return true;
   }
@@ -663,12 +669,13 @@ bool bwd_plan_for(int64_t T, int64_t N, int64_t K, int dx_f32, int dw_f32, int s
                    static_cast<uint64_t>(dx_f32 * 2 + dw_f32) * 4096 + static_cast<uint64_t>(sm));
   h = mix(h, static_cast<uint64_t>(o.bn) * 131 + static_cast<uint64_t>(o.splits) * 17 + o.tail_splits * 7 +
                  (o.swap + 1) * 3 + (o.pair + 1) + static_cast<uint64_t>(o.fuse + 1) * 1000003 +
-                 static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.kps) * 15485863);
+                 static_cast<uint64_t>(o.stream_k + 1) * 104729 + static_cast<uint64_t>(o.kps) * 15485863 +
+                 static_cast<uint64_t>(o.group) * 32452843 + static_cast<uint64_t>(o.raster_m + 1) * 49979687);
   BwdEntry& e = t_bwd_plans[h & 15];
   if (e.valid && e.T == T && e.N == N && e.K == K && e.dx_f32 == dx_f32 && e.dw_f32 == dw_f32 && e.sm == sm &&
       e.o.bn == o.bn && e.o.splits == o.splits && e.o.tail_splits == o.tail_splits && e.o.swap == o.swap &&
       e.o.pair == o.pair && e.o.fuse == o.fuse && e.o.stream_k == o.stream_k && e.o.ffma == o.ffma &&
-      e.o.atomic == o.atomic && e.o.kps == o.kps) {
+      e.o.atomic == o.atomic && e.o.kps == o.kps && e.o.group == o.group && e.o.raster_m == o.raster_m) {
     *plan = e.plan;
     return true;
   }

@@ -47,7 +47,9 @@ constexpr double kEpiBytesPerNs = 37.0;
 // A CTA pair's MMA waits for both CTAs' operand stages, so a load-bound pair runs at
 // its slower CTA's pace (measured on the batched per-head shapes: pairs 1.2x slower)
 constexpr double kPairLoadPenalty = 1.2;
-constexpr double kLaunchNs = 3000.0;          // a launch's fixed cost: setup, first loads, last tile's epilogue
+constexpr double kLaunchNs = 3000.0;
+constexpr double kL2Bytes = 129e6;     // GB300 L2
+constexpr double kL2Resident = 104e6;  // what a raster group's reused operand slabs may occupy of it          // a launch's fixed cost: setup, first loads, last tile's epilogue
 // Non-deterministic atomic split sums: the zero fill's fixed cost (a memset node
 // before the GEMM; for the router, a job of its operand-split kernel, nearly free),
 // and the rate of FP32 atomic adds into L2
@@ -483,9 +485,21 @@ bool make_plan(int op, int64_t T, int64_t N, int64_t K, int out_f32, int sm, Pla
   }
   // Group along the dimension whose operand is larger, so the tiles that share
   // its blocks run in the same wave and it crosses from DRAM about once.
-  plan.raster_m = v.gn > v.gm;
-  plan.group = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(16, plan.raster_m ? plan.tiles_m : plan.tiles_n)));
+  plan.raster_m = o.raster_m >= 0 ? o.raster_m != 0 : v.gn > v.gm;
+  int group = 16;
+  // When B is large too (more than half the L2), groups of row tiles instead, as wide as
+  // their A slabs fit in ~104 MB of the L2: each group's A stays resident while B streams
+  // through it once per group (measured on GB300 at 4096 -> 12288, T = 16384: forward
+  // 843 -> 830 us, input gradient 893 -> 871, weight gradient 880 -> 869 with groups of 8;
+  // shapes whose B fits keep the rule above, measured equal or better).
+  const double b_bytes = static_cast<double>(batch) * v.gn * v.gk * v.b_elem;
+  if (o.raster_m < 0 && b_bytes > kL2Bytes / 2) {
+    plan.raster_m = true;
+    const double slab = static_cast<double>(plan.bm) * v.gk * v.a_elem;
+    while (group > 1 && group * slab > kL2Resident) group /= 2;
+  }
+  plan.group = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(o.group > 0 ? o.group : group, plan.raster_m ? plan.tiles_m : plan.tiles_n)));
   // (stream-K: every slot, each with its share of the blocks)
   plan.grid = static_cast<int>((plan.stream_k ? slots_all : std::min<int64_t>(plan.units, slots_all)) *
                                (plan.pair ? 2 : 1));

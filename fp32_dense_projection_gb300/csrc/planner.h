@@ -132,6 +132,8 @@ struct Overrides {
   int stream_k = -1;  // 0 never, 1 only stream-K candidates (where the shape admits one)
   int atomic = -1;    // non-deterministic calls: 0 ordered split sums, 1 atomic ones (where admitted)
   int kps = 0;        // > 0: contraction blocks per ring stage (1 or 2; BF16 plans only)
+  int group = 0;      // > 0: raster group width in tiles
+  int raster_m = -1;  // >= 0: raster groups of row tiles (1) or of column tiles (0)
 };
 
 // Fill `plan`; returns false if the arguments cannot be planned (negative sizes,

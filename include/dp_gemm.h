@@ -279,7 +279,9 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * or as one co-scheduled launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never;
  * 1: a stream-K plan where the shape admits one), DP_FORCE_ATOMIC (calls with
  * deterministic = 0: 0 ordered split sums, 1 atomic ones wherever admitted),
- * DP_FORCE_KPS (1 / 2 contraction blocks per ring stage; BF16x3 plans keep 1).
+ * DP_FORCE_KPS (1 / 2 contraction blocks per ring stage; BF16x3 plans keep 1),
+ * DP_FORCE_GROUP (raster group width in tiles) and DP_FORCE_RASTER_M (1: groups of
+ * row tiles, 0: of column tiles).
  * A forced plan is still deterministic and keeps the accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of

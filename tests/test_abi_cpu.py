@@ -177,7 +177,21 @@ def test_raster_groups_the_larger_operand():
     finally:
         del os.environ["DP_FORCE_SWAP"]
     assert p["raster_rows"] == 1
-    assert dp.plan("fwd", 16384, 12288, 4096, sm_count=SM)["raster_rows"] == 0
+    # B fits in L2: groups along the dimension whose operand is larger (here columns)
+    assert dp.plan("fwd", 16384, 1024, 4096, sm_count=SM)["raster_rows"] == 0
+
+
+@pytest.mark.parametrize("op,group", [("fwd", 16), ("dgrad", 16), ("wgrad", 8)])
+def test_raster_row_groups_keep_a_in_l2_when_b_is_large(monkeypatch, op, group):
+    # 4096 -> 12288 at T = 16384: B (W, or X for the weight gradient) is more than half the
+    # L2, so groups of row tiles, as many as keep their A slabs within ~104 MB
+    p = dp.plan(op, 16384, 12288, 4096, sm_count=SM)
+    assert p["raster_rows"] == 1 and p["raster_group"] == group
+    assert p["raster_group"] * p["block_m"] * p["gemm_k"] * 2 <= 104e6
+    monkeypatch.setenv("DP_FORCE_RASTER_M", "0")
+    monkeypatch.setenv("DP_FORCE_GROUP", "4")
+    q = dp.plan(op, 16384, 12288, 4096, sm_count=SM)
+    assert q["raster_rows"] == 0 and q["raster_group"] == 4
 
 
 def test_empty_tokens_need_no_workspace():

@@ -7,11 +7,12 @@
 // ...", PR body).  This planner replaces the table with a small analytic cost
 // model over the same decisions: tile shape (one CTA or a CTA pair, output tile
 // width), the contraction split (whole K per tile, every tile split, or only the
-// last partial wave's tiles), the weight gradient's orientation, the raster order
-// (groups of 16 tiles, as the pages' column-grouped raster) and a persistent grid
-// no larger than the SM count read at run time.  The plan is a pure function of
-// its arguments, so every launch of a shape partitions every tile's contraction
-// the same way.
+// last partial wave's tiles), the weight gradient's orientation and a persistent
+// grid no larger than the SM count read at run time; and, by rules measured on
+// GB300, the raster order (groups of 16 tiles as the pages' column-grouped raster,
+// or groups of row tiles sized to the L2 when B is large) and the contraction
+// blocks per ring stage.  The plan is a pure function of its arguments, so every
+// launch of a shape partitions every tile's contraction the same way.
 #include "planner.h"
 
 #include <algorithm>

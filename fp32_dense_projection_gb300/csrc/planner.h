@@ -45,7 +45,7 @@ struct Plan {
   // weight gradient computed as D[k][n] = sum_t X[t][k] dY[t][n] (A = X, B = dY) and
   // stored transposed into dW[n][k]: thin N becomes the MMA's N, K fills the tile rows
   bool swap = false;
-  bool raster_m = false;  // raster groups of row tiles, rows fastest (B is the larger operand)
+  bool raster_m = false;  // raster groups of row tiles, rows fastest (B the larger operand, or B > L2 / 2)
   bool pair = false;      // tiles of 256 rows computed by a cluster of two CTAs (bm = 256)
   bool out_trans = false; // D[m][n] stored at out[n][m]
   int64_t batch = 1;      // independent GEMMs; tiles of batch b follow those of batch b - 1

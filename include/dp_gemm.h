@@ -300,7 +300,8 @@ typedef struct dp_plan_info {
     int32_t swap_ab;          /* weight gradient as dW^T = X^T dY (thin N as the MMA's N),
                                  stored transposed into dW */
     int32_t cta_pair;         /* 1: tiles of 256 rows shared by a cluster of two CTAs */
-    int32_t raster_rows;      /* 1: raster groups of row tiles, rows fastest */
+    int32_t raster_rows;      /* 1: raster groups of row tiles, rows fastest (B is the larger
+                                 operand, or more than half the L2) */
     int32_t stream_k;         /* 1: the grid's slots share all tiles' contraction blocks evenly
                                  (slot c takes blocks [c W / grid_slots, (c + 1) W / grid_slots)
                                  of the tile-major order, W = tiles * k_blocks); a tile cut by

@@ -381,7 +381,7 @@ def run_gpu(args, world, rank, local):
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(sample_rows=args.cpu_rows)
+        result["cpu_baseline"] = cpu_baseline(sample_rows=args.cpu_rows, single_rows=args.cpu_single_rows)
     if world > 1:
         torch.distributed.destroy_process_group()
     return result if rank == 0 else None
@@ -454,17 +454,31 @@ def oracle_sample(rows: int, seed: int = 0):
     return 2.0 * macs / dt / 1e12, dt, oracle.num_threads()
 
 
-def cpu_baseline(sample_rows: int) -> dict:
+def cpu_baseline(sample_rows: int, single_rows: int) -> dict:
+    """The oracle on the host cores: all of them (OpenMP over output elements), and one
+    thread in a child process (OMP_NUM_THREADS=1), each on its own bounded sample."""
     tflops, dt, cores = oracle_sample(sample_rows)
-    return {"value": round(tflops, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{sample_rows} output rows of each of fwd/dgrad/wgrad at the full 4096->12288 T=16384 "
-                      f"shapes ({dt:.1f} s of FP64 CPU work)"}
+    out = {"value": round(tflops, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{sample_rows} output rows of each of fwd/dgrad/wgrad at the full 4096->12288 T=16384 "
+                     f"shapes ({dt:.1f} s of FP64 CPU work on {cores} threads)"}
+    if single_rows > 0:
+        code = ("import json, bench; v, dt, c = bench.oracle_sample(%d, seed=5); "
+                "print(json.dumps({'v': v, 'dt': dt, 'c': c}))" % single_rows)
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+        if r.returncode == 0:
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            out["single_thread"] = {"value": round(d["v"], 6), "unit": UNIT, "cores": d["c"],
+                                    "sample": f"{single_rows} output rows of each op ({d['dt']:.1f} s on one thread)"}
+        else:
+            out["single_thread"] = {"value": None, "error": (r.stderr or r.stdout).strip()[-300:]}
+    return out
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    rows = max(1, args.cpu_rows // 4)
+    rows = max(1, args.cpu_rows // 8)
     for _ in range(args.warmup):
         oracle_sample(1, seed=1)
     vals, times = [], []
@@ -473,14 +487,15 @@ def run_reference(args, world, rank):
         vals.append(v)
         times.append(dt)
     value = statistics.median(vals)
-    ms_equiv = 3 * FLOP_OP / (value * 1e12) * 1e3
-    sample = f"{rows} output rows of each op per step at the full shapes"
+    sample = (f"{rows} output rows of each of fwd/dgrad/wgrad per step at the full shapes "
+              f"({3 * rows} output rows, {statistics.median(times):.2f} s per step)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_equiv, 1), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "T": T_TOK, "N": N_OUT, "K": K_IN,
-                   "reference": "FP64 CPU oracle (plain definition), no GPU; ms_per_step extrapolated"},
+                   "reference": "FP64 CPU oracle (plain definition), no GPU",
+                   "step": f"a bounded sample of the workload: {sample}; value = the sample's FLOP / its time"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": cores,
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -739,7 +754,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--cpu-rows", type=int, default=160, help="oracle sample on all host cores (~10 s on 16)")
+    ap.add_argument("--cpu-single-rows", type=int, default=10, help="oracle sample on one thread (~7 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-op", default=None,
                     choices=["fwd", "dgrad", "wgrad", "router_fwd", "router_dgrad", "router_wgrad",

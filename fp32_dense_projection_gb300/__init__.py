@@ -480,6 +480,12 @@ def dp_gemm_wgrad_noalloc(dY, X, out, out_dtype=None, deterministic=True, stream
         raise ValueError("dp_gemm_wgrad_noalloc: dY[T,N], X[T,K], out[N,K]")
     if dY.dtype != torch.bfloat16 or X.dtype != torch.bfloat16:
         raise TypeError("dp_gemm_wgrad_noalloc: operands must be bf16")
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("dp_gemm_wgrad_noalloc: out must be float32 or bfloat16")
+    if out_dtype is not None and out.dtype != out_dtype:
+        raise TypeError(f"dp_gemm_wgrad_noalloc: out is {out.dtype}, out_dtype says {out_dtype}")
+    if not (dY.is_cuda and X.is_cuda and out.is_cuda) or not (dY.device == X.device == out.device):
+        raise ValueError("dp_gemm_wgrad_noalloc: dY, X and out must be CUDA tensors on one device")
     L = lib()
     fn = L.dp_gemm_wgrad_noalloc
     P, I, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int

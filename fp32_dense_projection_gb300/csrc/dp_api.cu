@@ -214,39 +214,46 @@ dp_status check_matrix(const void* p, int64_t rows, int64_t cols, int64_t* ld, i
   return DP_OK;
 }
 
-int env_int(const char* name) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : 0;
+// Tuning and test overrides come from the environment only in a process started
+// with DP_TUNING set (read once, at the first call that plans).  Then every call
+// reads the DP_FORCE_* variables again, so a test or a sweep can change them
+// between calls; otherwise no call reads the environment, and the plan caches
+// see the planner's own choices only.
+bool tuning_enabled() {
+  static const bool on = std::getenv("DP_TUNING") != nullptr;
+  return on;
 }
 
-// Plan overrides for tuning and tests, read on every call (DP_FORCE_CLUSTER_SUM=0,
-// read in cluster_fixup, keeps split sums in the reduction kernel): DP_FORCE_BN,
-// DP_FORCE_SPLITS, DP_FORCE_TAIL_SPLITS, DP_FORCE_KPS, DP_FORCE_GROUP (> 0 forces),
+// An override's value, or `unset` if the variable is absent or tuning is off.
+int env_int(const char* name, int unset) {
+  if (!tuning_enabled()) return unset;
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : unset;
+}
+
+// Plan overrides (with DP_TUNING only): DP_FORCE_BN, DP_FORCE_SPLITS,
+// DP_FORCE_TAIL_SPLITS, DP_FORCE_KPS, DP_FORCE_GROUP (> 0 forces),
 // DP_FORCE_RASTER_M and DP_FORCE_SWAP (0 or 1: raster groups of row tiles, the
-// weight-gradient orientation), DP_FORCE_PAIR (0 or 1: single-CTA or
-// CTA-pair tiles), DP_FORCE_FUSE, DP_FORCE_FFMA, DP_FORCE_STREAM_K and
-// DP_FORCE_ATOMIC (0 or 1).  Unset in normal use.
+// weight-gradient orientation), DP_FORCE_PAIR (0 or 1: single-CTA or CTA-pair
+// tiles), DP_FORCE_FUSE, DP_FORCE_FFMA, DP_FORCE_STREAM_K and DP_FORCE_ATOMIC (0
+// or 1).  Two more are read where the launch is prepared: DP_FORCE_CLUSTER_SUM=0
+// (split sums in the reduction kernel, never in the GEMM's clusters) and
+// DP_FORCE_TMA_STORE (0 / 1: the epilogue's TMA stores off / on everywhere).
 Overrides env_overrides() {
-  const char* sw = std::getenv("DP_FORCE_SWAP");
-  const char* pr = std::getenv("DP_FORCE_PAIR");
-  const char* fu = std::getenv("DP_FORCE_FUSE");
   Overrides o;
-  o.bn = env_int("DP_FORCE_BN");
-  o.splits = env_int("DP_FORCE_SPLITS");
-  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS");
-  o.swap = sw ? std::atoi(sw) : -1;
-  o.pair = pr ? std::atoi(pr) : -1;
-  o.fuse = fu ? std::atoi(fu) : -1;
-  const char* ff = std::getenv("DP_FORCE_FFMA");
-  o.ffma = ff ? std::atoi(ff) : -1;
-  const char* sk = std::getenv("DP_FORCE_STREAM_K");
-  o.stream_k = sk ? std::atoi(sk) : -1;
-  const char* at = std::getenv("DP_FORCE_ATOMIC");
-  o.atomic = at ? std::atoi(at) : -1;
-  o.kps = env_int("DP_FORCE_KPS");
-  o.group = env_int("DP_FORCE_GROUP");
-  const char* rm = std::getenv("DP_FORCE_RASTER_M");
-  o.raster_m = rm ? std::atoi(rm) : -1;
+  if (!tuning_enabled()) return o;
+  o.bn = env_int("DP_FORCE_BN", 0);
+  o.splits = env_int("DP_FORCE_SPLITS", 0);
+  o.tail_splits = env_int("DP_FORCE_TAIL_SPLITS", 0);
+  o.swap = env_int("DP_FORCE_SWAP", -1);
+  o.pair = env_int("DP_FORCE_PAIR", -1);
+  o.fuse = env_int("DP_FORCE_FUSE", -1);
+  o.ffma = env_int("DP_FORCE_FFMA", -1);
+  o.stream_k = env_int("DP_FORCE_STREAM_K", -1);
+  o.atomic = env_int("DP_FORCE_ATOMIC", -1);
+  o.kps = env_int("DP_FORCE_KPS", 0);
+  o.group = env_int("DP_FORCE_GROUP", 0);
+  o.raster_m = env_int("DP_FORCE_RASTER_M", -1);
   return o;
 }
 
@@ -322,8 +329,7 @@ std::vector<std::pair<ClusterKey, int>> g_cluster_capacity;
 int cluster_fixup(const Plan& p, bool x3, const DeviceState& dev) {
   if (p.pair || p.stream_k || p.atomic || p.splits < 2 || p.splits > 8 || p.full_units != 0 || p.units != p.grid)
     return 0;
-  const char* off = std::getenv("DP_FORCE_CLUSTER_SUM");  // "0": always the reduction kernel (tests)
-  if (off && std::atoi(off) == 0) return 0;
+  if (env_int("DP_FORCE_CLUSTER_SUM", 1) == 0) return 0;  // always the reduction kernel (tests)
   int cur = 0;
   if (cudaGetDevice(&cur) != cudaSuccess) return 0;
   const int view = p.a_mn ? 2 : (p.b_mn ? 1 : 0);
@@ -418,9 +424,9 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   // way for the long BF16 ones, 2-4% slower for BF16 units of 2 blocks).  The
   // transposed store of the swapped weight gradient keeps its own path;
   // DP_FORCE_TMA_STORE=0 / 1 turns them off / on everywhere else (tests, comparisons).
-  const char* ts = std::getenv("DP_FORCE_TMA_STORE");
+  const int ts = env_int("DP_FORCE_TMA_STORE", -1);
   const int64_t kb_unit = p.full_units > 0 ? p.nkb : (p.nkb + p.splits - 1) / p.splits;
-  const bool want_tma_store = ts ? std::atoi(ts) != 0 : (p.out_f32 != 0 || kb_unit >= 8);
+  const bool want_tma_store = ts >= 0 ? ts != 0 : (p.out_f32 != 0 || kb_unit >= 8);
   a.tma_store = (!p.out_trans && p.gm > 0 && want_tma_store &&
                  make_map(&a.tmO, out, p.gm, p.gn, ldo, 32, p.out_f32 != 0, p.out_f32 ? 32 : 64,
                           CU_TENSOR_MAP_SWIZZLE_128B, 0, nb, bso))

@@ -52,10 +52,11 @@ dp_status scratch_address(void** out) {
 extern "C" dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int64_t ldx, void* dW,
                                            int64_t ldw, int64_t T, int64_t N, int64_t K, dp_out_dtype out,
                                            int deterministic, dp_stream stream) {
-  size_t need = 0;
-  dp_status st = dp_workspace_size(DP_OP_WGRAD, T, N, K, out, 0, &need);
+  // the plan of this very call (its deterministic flag included) sizes the scratch
+  dp_plan_info info;
+  dp_status st = dp_plan_query_ex(DP_OP_WGRAD, T, N, K, out, deterministic, 0, &info);
   if (st != DP_OK) return st;
-  if (need > kScratchBytes) return DP_ERR_WORKSPACE;  // beyond the built-in 64 MiB scratch
+  if (info.workspace_bytes > kScratchBytes) return DP_ERR_WORKSPACE;  // beyond the built-in 64 MiB
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != DP_OK) return st;
   return dp_gemm_wgrad_ex(dY, ldg, X, ldx, dW, ldw, T, N, K, out, deterministic, scratch, kScratchBytes, stream);

@@ -300,17 +300,19 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       const Tiling t = {bn, pair != 0};
       const int64_t tiles = v.batch * ceil_div(v.gm, t.rows()) * ceil_div(v.gn, bn);
       const int64_t cta_tiles = tiles * (pair ? 2 : 1);  // partial slots: one per CTA tile
-      // bounded accumulation length, unless the tiles are too many to split at all
-      // (then whole K per tile: a longer running sum, the only case without the bound)
-      // (kMaxAccumBlocks counts 64-element blocks of one MMA each; BF16x3 accumulates three)
+      // bounded accumulation length: every accumulator sums at most max_blocks blocks, so
+      // a longer contraction is always split (kMaxAccumBlocks counts 64-element blocks of
+      // one MMA each; BF16x3 accumulates three per element)
       const int64_t max_blocks = kMaxAccumBlocks * kBlockK / (v.bk * v.terms);
-      const int64_t min_s = cta_tiles > kMaxSplitTiles ? 1 : ceil_div(nkb, max_blocks);
+      const int64_t min_s = ceil_div(nkb, max_blocks);
       const int64_t max_s = std::max<int64_t>(min_s, std::min<int64_t>(nkb, 64));
       // every tile split the same way (s = 1: whole K per tile)
       for (int64_t s = min_s; s <= max_s && o.tail_splits <= 0 && o.stream_k != 1; ++s) {
         if (o.splits > 0 && s != std::min<int64_t>(o.splits, nkb)) continue;
         if (o.splits <= 0 && s > min_s && tiles * s > 4LL * slots) break;  // beyond 4 waves never pays
-        if (s > 1 && cta_tiles > kMaxSplitTiles) break;                    // bounded partial workspace
+        // more splits than the bound needs only while the partials stay within
+        // kMaxSplitTiles tiles' worth of workspace
+        if (s > std::max<int64_t>(1, min_s) && cta_tiles > kMaxSplitTiles) break;
         consider(t, s == 1 ? tiles : 0, s,
                  model_ns(v, t, s == 1 ? tiles : 0, s, sm, out_bytes, atomic_ok, &atomic, o.atomic == 1));
       }

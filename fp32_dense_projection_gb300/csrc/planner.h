@@ -25,14 +25,17 @@ enum Op : int {
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
 // Most split tiles (tiles whose contraction is split, times CTAs per tile) a plan
-// may have; beyond that the whole contraction stays in each tile, which bounds the
-// workspace the FP32 partials take.
+// takes by choice: splits beyond what the accumulation bound below requires are
+// considered only up to this many, which bounds the workspace their FP32 partials
+// take.  (The bound itself always holds: a larger shape with a long contraction
+// gets the splits the bound needs and a workspace to match.)
 constexpr int kMaxSplitTiles = 4096;
 // Longest contraction one TMEM accumulator sums, in 64-wide blocks (16384 tokens).
 // The tensor core rounds each FP32 accumulate toward zero, so the error of a
 // running sum grows with its length; at 32768 tokens per accumulator a BF16
 // output of the 65537-token weight gradient fell outside the pages' budget.
-// Longer contractions are split (fixed partition, partials summed in order).
+// Longer contractions are always split (fixed partition, partials summed in
+// order), whatever the shape.
 constexpr int kMaxAccumBlocks = 256;
 
 struct Plan {

@@ -216,8 +216,9 @@ dp_status dp_gemm_wgrad_batched(const void* dY, int64_t ldg, int64_t bsg, const 
  *     single-op plan computes.
  * Chosen when the cost model expects the co-scheduled launch to be at least 3%
  * faster (small and mid-size T, where each single-op launch leaves SMs idle);
- * DP_FORCE_FUSE overrides (0: two calls; 1: co-scheduled; 2 / 3: co-scheduled
- * with the weight / input gradient's tiles first).  dX and dW must not overlap
+ * DP_FORCE_FUSE (with DP_TUNING, see below) overrides (0: two calls; 1:
+ * co-scheduled; 2 / 3: co-scheduled with the weight / input gradient's tiles
+ * first).  dX and dW must not overlap
  * dY, X or W.
  * Arguments and errors as the single-op calls; workspace: dp_workspace_size_bwd. */
 dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, const void* W, int64_t ldw,
@@ -241,8 +242,9 @@ dp_status dp_gemm_bwd(const void* dY, int64_t ldg, const void* X, int64_t ldx, c
  * and without workspace, each output tile's contraction split over the CTAs of a
  * thread-block cluster whose partials are summed in a fixed order (so the output
  * is bitwise repeatable; its error is the FP32 rounding of the sum, below the
- * BF16x3 program's).  DP_FORCE_FFMA=0 / 1 forces either program (1: where the
- * forced tile width and split count, if any, fit the shape). */
+ * BF16x3 program's).  DP_FORCE_FFMA=0 / 1 (with DP_TUNING, see below) forces
+ * either program (1: where the forced tile width and split count, if any, fit the
+ * shape). */
 
 /* Router forward: Y[t][n] = sum_k X[t][k] * W[n][k];  X: T x K, W: N x K, Y: T x N. */
 dp_status router_fwd(const float* X, const float* W, float* Y,
@@ -269,19 +271,24 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
                           void* workspace, size_t workspace_bytes, dp_stream stream);
 
 /* ------------------------------------------------------------ planning, misc */
-/* Tuning and test overrides, read from the environment on every call (unset in
- * normal use): DP_FORCE_BN (64 / 128 / 256), DP_FORCE_SPLITS (uniform split
- * count), DP_FORCE_TAIL_SPLITS (split only the last partial wave, this many
- * ways), DP_FORCE_SWAP (0 / 1: BF16 weight-gradient orientation), DP_FORCE_PAIR
- * (0 / 1: single-CTA or CTA-pair tiles), DP_FORCE_CLUSTER_SUM=0 (sum split
- * partials in the reduction kernel instead of inside the GEMM's clusters; the
- * two give the same bits), DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls
- * or as one co-scheduled launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never;
- * 1: a stream-K plan where the shape admits one), DP_FORCE_ATOMIC (calls with
- * deterministic = 0: 0 ordered split sums, 1 atomic ones wherever admitted),
- * DP_FORCE_KPS (1 / 2 contraction blocks per ring stage; BF16x3 plans keep 1),
- * DP_FORCE_GROUP (raster group width in tiles) and DP_FORCE_RASTER_M (1: groups of
- * row tiles, 0: of column tiles).
+/* Tuning and test overrides.  They are read from the environment only in a
+ * process that has DP_TUNING set when the library first plans a call; such a
+ * process reads them again on every call (so a test can change them between
+ * calls).  Without DP_TUNING no call reads the environment.  The variables:
+ * DP_FORCE_BN (64 / 128 / 256), DP_FORCE_SPLITS (uniform split count),
+ * DP_FORCE_TAIL_SPLITS (split only the last partial wave, this many ways),
+ * DP_FORCE_SWAP (0 / 1: BF16 weight-gradient orientation), DP_FORCE_PAIR (0 / 1:
+ * single-CTA or CTA-pair tiles), DP_FORCE_CLUSTER_SUM=0 (sum split partials in
+ * the reduction kernel instead of inside the GEMM's clusters; the two give the
+ * same bits), DP_FORCE_TMA_STORE (0 / 1: the epilogue's whole-tile TMA stores off
+ * / on for every non-transposed output; both store paths give the same bits),
+ * DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls or as one co-scheduled
+ * launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never; 1: a stream-K plan where
+ * the shape admits one), DP_FORCE_ATOMIC (calls with deterministic = 0: 0 ordered
+ * split sums, 1 atomic ones wherever admitted), DP_FORCE_KPS (1 / 2 contraction
+ * blocks per ring stage; BF16x3 plans keep 1), DP_FORCE_FFMA (0 / 1: the router's
+ * BF16x3 or SIMT program), DP_FORCE_GROUP (raster group width in tiles) and
+ * DP_FORCE_RASTER_M (1: groups of row tiles, 0: of column tiles).
  * A forced plan is still deterministic and keeps the accumulation-length bound. */
 
 /* The plan the library uses for one call.  The planner is a pure function of

@@ -3,6 +3,10 @@ import sys
 
 import pytest
 
+# The tests force plans through the DP_FORCE_* variables, which the library reads
+# only in a process started with DP_TUNING set (before its first call).
+os.environ.setdefault("DP_TUNING", "1")
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

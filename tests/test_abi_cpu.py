@@ -252,6 +252,28 @@ def test_workspace_only_when_needed():
                 assert n == 0
 
 
+def longest_accumulation(p) -> int:
+    """Most contraction elements one accumulator of the plan sums (x3 for BF16x3)."""
+    if p["program"] == 1:  # the router's SIMT program accumulates with FP32 FMAs (round to nearest)
+        return 0
+    if p["stream_k"]:  # a piece never spans more than one slot's share of the blocks
+        slots = p["grid"] // (2 if p["cta_pair"] else 1)
+        per = -(-p["tiles"] * p["k_blocks"] // slots)
+        return min(per, p["k_blocks"]) * p["block_k"]
+    split_tiles = p["tiles"] - p["full_units"]
+    per = p["k_blocks"] if p["full_units"] > 0 else 0
+    if split_tiles > 0:
+        per = max(per, -(-p["k_blocks"] // p["splits"]))
+    return per * p["block_k"]
+
+
+# The contraction view of each op: (rows, columns, contraction) of D = A B^T
+LONG_SHAPES = [  # (T, N, K) whose contraction exceeds 16384 in some op, with few and with many tiles
+    (16385, 64, 4096), (65537, 512, 4096), (200000, 256, 4096), (65536, 16384, 16384), (40000, 24576, 8192),
+    (64, 32768, 1024), (1024, 65536, 4096), (8192, 20480, 20480), (3, 17000, 8), (20000, 8, 17000),
+]
+
+
 @pytest.mark.parametrize("op", list(dp.OP_NAMES))
 @pytest.mark.parametrize("T", [1025, 16173, 16384, 65537, 200000])
 def test_accumulation_length_is_bounded(op, T):
@@ -261,9 +283,55 @@ def test_accumulation_length_is_bounded(op, T):
     terms = 3 if op in ("router_fwd", "router_wgrad") else 1
     for N, K in ((64, 4096), (512, 4096), (256, 4096), (12288, 4096)):
         p = dp.plan(op, T, N, K, sm_count=SM)
-        per_split = -(-p["k_blocks"] // p["splits"]) * p["block_k"]
-        if p["tiles_m"] * p["tiles_n"] * (2 if p["cta_pair"] else 1) <= 4096:  # else whole K (bounded workspace)
-            assert per_split * terms <= 16384 + p["block_k"] * terms, (op, T, N, K, p)
+        assert longest_accumulation(p) * terms <= 16384, (op, T, N, K, p)
+
+
+@pytest.mark.parametrize("op", list(dp.OP_NAMES))
+@pytest.mark.parametrize("T,N,K", LONG_SHAPES)
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_accumulation_bound_holds_for_every_shape(op, T, N, K, out_f32):
+    # including shapes with far more than 4096 output tiles, which split the contraction
+    # all the same (their partials take a workspace the size of a few outputs)
+    terms = 3 if op in ("router_fwd", "router_wgrad") else 1
+    for sm in (SM, 148, 8):
+        p = dp.plan(op, T, N, K, out_f32=out_f32, sm_count=sm)
+        assert longest_accumulation(p) * terms <= 16384, (op, T, N, K, sm, p)
+        if longest_accumulation(p) > 0 and p["k_blocks"] * p["block_k"] * terms > 16384 and p["program"] == 0:
+            assert p["splits"] > 1 and p["workspace_bytes"] > 0
+
+
+@pytest.mark.parametrize("env", [{"DP_FORCE_BN": "64"}, {"DP_FORCE_PAIR": "1"}, {"DP_FORCE_PAIR": "0"},
+                                 {"DP_FORCE_SWAP": "1"}, {"DP_FORCE_SWAP": "0"}, {"DP_FORCE_STREAM_K": "1"},
+                                 {"DP_FORCE_SPLITS": "2"}, {"DP_FORCE_TAIL_SPLITS": "3"}, {"DP_FORCE_KPS": "2"}])
+def test_forced_plans_keep_the_accumulation_bound(monkeypatch, env):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    for op in dp.OP_NAMES:
+        terms = 3 if op in ("router_fwd", "router_wgrad") else 1
+        for T, N, K in LONG_SHAPES[:6]:
+            try:
+                p = dp.plan(op, T, N, K, sm_count=SM)
+            except dp.DPError:
+                continue  # an override no plan of this shape admits
+            assert longest_accumulation(p) * terms <= 16384, (env, op, T, N, K, p)
+
+
+def test_tuning_overrides_need_the_tuning_switch(tmp_path):
+    # without DP_TUNING the library reads no DP_FORCE_* variable: the planner's own plan
+    import subprocess
+    import sys
+    code = ("import fp32_dense_projection_gb300 as dp;"
+            "p = dp.plan('fwd', 16384, 12288, 4096, sm_count=152);"
+            "print(p['block_n'], p['cta_pair'], p['blocks_per_stage'])")
+    env = {k: v for k, v in os.environ.items() if k != "DP_TUNING"}
+    env.update({"DP_FORCE_BN": "64", "DP_FORCE_PAIR": "0", "DP_FORCE_KPS": "1", "PYTHONPATH": ROOT})
+    plain = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    env["DP_TUNING"] = "1"
+    tuned = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True)
+    assert tuned.stdout.split() == ["64", "0", "1"]
+    p = dp.plan("fwd", 16384, 12288, 4096, sm_count=152)  # (this process: no override set)
+    assert plain.stdout.split() == [str(p["block_n"]), str(p["cta_pair"]), str(p["blocks_per_stage"])]
+    assert plain.stdout != tuned.stdout
 
 
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])

@@ -43,6 +43,22 @@ def test_noalloc_matches_workspace_entry_point(T, N, K, out_dtype):
     assert dp.device_error() == 0
 
 
+def test_noalloc_non_deterministic_fp32():
+    # deterministic = 0 admits atomic split sums where the planner finds them faster:
+    # the result is then checked against the workspace entry point within the FP32 budget
+    T, N, K = 16173, 64, 4096
+    c = inputs.thin_wgrad(T, N, K, seed=7)
+    dY, X = c["dY"].to(DEV), c["X"].to(DEV)
+    want = dp.dp_gemm_wgrad(dY, X, out_dtype=torch.float32, deterministic=False)
+    for call in range(2):
+        got = torch.full((N, K), float("nan"), dtype=torch.float32, device=DEV)
+        dp.dp_gemm_wgrad_noalloc(dY, X, out=got, deterministic=False)
+        torch.cuda.synchronize()
+        ok, msg = check(got.double().cpu().numpy(), want.double().cpu().numpy(), "f32")
+        assert ok, f"call {call}: {msg}"
+    assert dp.device_error() == 0
+
+
 def test_noalloc_rejects_plans_beyond_its_scratch():
     # 4096 -> 512 at T = 65537 splits 7 ways: 64 tiles x 7 x 128 KB of partials, under 64 MiB;
     # 8192 -> 1024 at T = 65537 needs far more than the built-in array and is refused.

@@ -97,6 +97,7 @@ def lib():
         L.dp_status_string.argtypes = [S]
         L.dp_status_string.restype = ctypes.c_char_p
         L.dp_version.argtypes = []
+        L.dp_wait_probe.argtypes = [ctypes.c_uint64, S, P]
         _lib = L
     return _lib
 
@@ -180,6 +181,14 @@ def init(device: int = -1):
 def device_error(clear: bool = True) -> int:
     """Synchronise and return the library's device fault status (0 = none)."""
     return int(lib().dp_device_error(int(bool(clear))))
+
+
+def wait_probe(limit_ns: int, arrive: bool = False, stream=None):
+    """Enqueue the library's bounded-wait probe (one CTA waiting on a barrier that
+    nothing arrives on, or that it arrived on itself): a wait that runs out after
+    ``limit_ns`` shows up as ``device_error() == 7`` (DP_ERR_TIMEOUT)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(lib().dp_wait_probe(int(limit_ns), int(bool(arrive)), _stream(dev, stream)), "dp_wait_probe")
 
 
 # ------------------------------------------------------------------ workspace

@@ -435,6 +435,7 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;
+  a.wait_ns = kWaitLimitNs;
   l.grid = p.grid;
   l.pair = p.pair;
   l.x3 = x3;
@@ -753,6 +754,22 @@ void fill_bwd_info(const BwdPlan& bp, int64_t T, dp_bwd_plan_info* info) {
   fill_info(bp.wgrad, T, &info->wgrad);
 }
 
+// The bounded wait on its own: one CTA whose first thread waits, through the same
+// mbar_wait the GEMM's roles use, on a shared-memory barrier of arrival count 1 --
+// one that nothing arrives on, or (arrive != 0) one it has just arrived on itself.
+// A wait that gives up after limit_ns records kFaultProbeWait in the status word
+// and the kernel returns; it holds no TMEM and issues no copies, so it ends either way.
+__global__ void wait_probe_kernel(uint32_t* fault, uint64_t limit_ns, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    if (arrive) mbar_arrive(b);
+    if (!mbar_wait(b, 0, limit_ns)) atomicOr(fault, kFaultProbeWait);
+  }
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -978,6 +995,15 @@ dp_status dp_device_error(int clear) {
     if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero)) != cudaSuccess) return DP_ERR_LAUNCH;
   }
   return word ? DP_ERR_TIMEOUT : DP_OK;
+}
+
+dp_status dp_wait_probe(uint64_t limit_ns, int arrive, dp_stream stream) {
+  if (limit_ns < 1000 || limit_ns > kWaitLimitNs) return DP_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  const dp_status st = current_device(&d);
+  if (st != DP_OK) return st;
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(d->fault, limit_ns, arrive ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_LAUNCH;
 }
 
 const char* dp_status_string(dp_status status) {

@@ -89,6 +89,7 @@ struct GemmArgs {
   int32_t kps;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
+  uint64_t wait_ns;    // limit of every barrier wait (ns); past it the kernel records a fault and unwinds
   // tma_store = 1: whole-tile results leave through TMA stores instead of the
   // epilogue warps' own stores, with tmO the output as a TMA map ([batch][gm][gn],
   // leading dimension ldo; boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16
@@ -682,14 +683,14 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             next(fc);
             progressed = true;
           }
-          // bounded: give up once neither ring has moved for kWaitLimitNs
+          // bounded: give up once neither ring has moved for the wait limit
           if (progressed) {
             idle = 0;
           } else if ((++idle & 255u) == 1u) {
             const uint64_t now = globaltimer_ns();
             if (idle == 1u) {
               t_idle = now;
-            } else if (now - t_idle > kWaitLimitNs) {
+            } else if (now - t_idle > args.wait_ns) {
               atomicOr(args.fault, kFaultProducerWait);
               ok = false;
               break;
@@ -713,7 +714,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         const int b_row0 = w.tn * BN + static_cast<int>(rank) * C::BNH;
         for (int kbs = w.kb0; kbs < w.kb1; kbs += kps) {
           const int nb = min(kps, w.kb1 - kbs);  // blocks in this stage
-          if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u)) {
+          if (!mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u, args.wait_ns)) {
             atomicOr(args.fault, kFaultProducerWait);
             ok = false;
             break;
@@ -785,12 +786,13 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u) {
           const uint32_t par = (issued_phase >> s) & 1u;
-          const bool landed = PAIR ? mbar_wait<true>(empty_bar(s), par) : mbar_wait(full_bar(s), par);
+          const bool landed = PAIR ? mbar_wait<true>(empty_bar(s), par, args.wait_ns)
+                                   : mbar_wait(full_bar(s), par, args.wait_ns);
           if (!landed) atomicOr(args.fault, kFaultDrainWait);
         }
       for (int s = 0; s < SSTAGES; ++s)
         if ((sissued >> s) & 1u) {
-          if (!mbar_wait(sfull_bar(s), (sissued_phase >> s) & 1u)) atomicOr(args.fault, kFaultDrainWait);
+          if (!mbar_wait(sfull_bar(s), (sissued_phase >> s) & 1u, args.wait_ns)) atomicOr(args.fault, kFaultDrainWait);
         }
     }
   } else if (warp == 1) {
@@ -811,14 +813,14 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u)) {
+        if (!mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, args.wait_ns)) {
           atomicOr(args.fault, kFaultMmaWait);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kbs = kb0; kbs < kb1; kbs += kps) {
-          if (!mbar_wait<PAIR>(full_bar(stage), phase)) {
+          if (!mbar_wait<PAIR>(full_bar(stage), phase, args.wait_ns)) {
             atomicOr(args.fault, kFaultMmaWait);
             ok = false;
             break;
@@ -887,7 +889,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         mma_commit_pair(drain_bar);
       else
         mma_commit(drain_bar);
-      if (!mbar_wait(drain_bar, 0)) atomicOr(args.fault, kFaultDrainWait);
+      if (!mbar_wait(drain_bar, 0, args.wait_ns)) atomicOr(args.fault, kFaultDrainWait);
     }
   } else if (X3 && (warp == 2 || warp == 3 || warp == 8 || warp == 9)) {
     // ------------------------------------------------------------ converter (X3)
@@ -933,7 +935,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       const Unit w = decode_unit(args, u);
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         // every lane waits itself; the warp leaves together if any wait gives up
-        const bool mine = mbar_wait(sfull_bar(sstage), sphase) && mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u);
+        const bool mine = mbar_wait(sfull_bar(sstage), sphase, args.wait_ns) &&
+                           mbar_wait<PAIR>(empty_bar(stage), phase ^ 1u, args.wait_ns);
         if (!__all_sync(0xffffffffu, mine)) {
           if (lane == 0) atomicOr(args.fault, kFaultProducerWait);
           ok = false;
@@ -1003,7 +1006,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       // One thread waits; the outcome reaches the other 127 through a named barrier,
       // so all of them leave together if the wait gives up.
       if (leader) {
-        const bool ready = mbar_wait<PAIR>(tfull_bar(acc), aph);
+        const bool ready = mbar_wait<PAIR>(tfull_bar(acc), aph, args.wait_ns);
         if (!ready) atomicOr(args.fault, kFaultEpilogueWait);
         flag_wait[local & 1] = ready ? 1u : 0u;
       }

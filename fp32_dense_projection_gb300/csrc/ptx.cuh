@@ -7,8 +7,9 @@
 
 namespace dp {
 
-// A wait that has not completed after this long is treated as a fault: the kernel
-// records it and unwinds instead of spinning forever.
+// A wait that has not completed after its limit is treated as a fault: the kernel
+// records it and unwinds instead of spinning forever.  The limit is a launch
+// argument of every kernel that waits (GemmArgs::wait_ns); this is its default.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Fault codes OR-ed into the device status word.
@@ -16,6 +17,7 @@ constexpr uint32_t kFaultProducerWait = 1u << 0;
 constexpr uint32_t kFaultMmaWait = 1u << 1;
 constexpr uint32_t kFaultEpilogueWait = 1u << 2;
 constexpr uint32_t kFaultDrainWait = 1u << 3;
+constexpr uint32_t kFaultProbeWait = 1u << 4;  // the wait probe (dp_wait_probe) gave up
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -97,10 +99,10 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
 }
 
 // Wait until the barrier phase of the given parity has completed.  Returns false
-// (without completing) once kWaitLimitNs has passed.  CLUSTER selects the
+// (without completing) once limit_ns has passed.  CLUSTER selects the
 // cluster-scope acquire (barriers signalled from the peer CTA of a pair).
 template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   auto test = [&]() { return CLUSTER ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity); };
   if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -108,7 +110,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
       if (test()) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

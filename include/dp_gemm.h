@@ -385,6 +385,20 @@ dp_status dp_init(int device);
  * `clear` != 0 resets the flag.  Not for use inside stream capture. */
 dp_status dp_device_error(int clear);
 
+/* Test entry for the kernels' bounded waits (the failure-detection path).  Every
+ * barrier wait in this library's kernels gives up after a time limit that is a
+ * launch argument (2 s in the calls above), records the fault in the device status
+ * word that dp_device_error() reports as DP_ERR_TIMEOUT, and lets the kernel
+ * unwind and return instead of hanging the GPU.  This call enqueues on `stream` one
+ * CTA that waits through that same bounded wait, with limit `limit_ns`
+ * (1e3 .. 2e9 ns, else DP_ERR_INVALID_ARG), on a shared-memory barrier that nothing
+ * arrives on (arrive = 0: the wait runs out and the kernel records the timeout) or
+ * that the waiting thread arrived on first (arrive != 0: it returns at once and
+ * records nothing).  The kernel holds no TMEM and issues no copies, so it ends
+ * either way and the stream stays usable.  No counterpart on the pages: it exists
+ * so the timeout path can be tested on a GPU without faulting or hanging one. */
+dp_status dp_wait_probe(uint64_t limit_ns, int arrive, dp_stream stream);
+
 /* Static description of a status code. */
 const char* dp_status_string(dp_status status);
 

@@ -565,3 +565,23 @@ def test_thin_stream_orientation(T, N, K, swap):
     assert p["swap_ab"] == swap
     if swap:
         assert p["block_n"] == 64 and p["cta_pair"] == 0 and p["units"] <= SM and p["blocks_per_stage"] == 2
+
+
+def test_test_helpers_cover_every_tile_and_block():
+    # the GPU tests' samplers: raster_tile visits every tile of a plan exactly once,
+    # stratified_points puts its points in every block and inside the matrix
+    import numpy as np
+    from gpu_common import raster_tile, stratified_points
+    for op, T, N, K in (("fwd", 16384, 12288, 4096), ("dgrad", 16231, 12288, 4096), ("wgrad", 16384, 12288, 4096),
+                        ("wgrad", 65537, 64, 4096), ("fwd", 300, 200, 64)):
+        p = dp.plan(op, T, N, K, sm_count=SM)
+        seen = {raster_tile(p, t) for t in range(p["tiles"])}
+        assert len(seen) == p["tiles"] == p["tiles_m"] * p["tiles_n"]
+        assert all(0 <= tm < p["tiles_m"] and 0 <= tn < p["tiles_n"] for tm, tn in seen)
+    rng = np.random.default_rng(0)
+    for R, C in ((16231, 4096), (64, 4096), (130, 129)):
+        r, c = stratified_points((R, C), rng)
+        assert r.min() >= 0 and c.min() >= 0 and r.max() < R and c.max() < C
+        blocks = set(zip((r // 128).tolist(), (c // 128).tolist()))
+        assert len(blocks) == (-(-R // 128)) * (-(-C // 128))
+        assert r.size == 8 * len(blocks)

@@ -418,6 +418,15 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
   a.sk_work = p.tiles * p.nkb;
   a.cluster_fixup = cluster_fixup(p, x3, dev);
   a.kps = (!x3 && p.kps == 2 && p.stages % 2 == 0) ? 2 : 1;
+  // An operand that one column tile (A) or one row tile (B) reads in full is read once
+  // by the launch (split units read disjoint contraction ranges): its loads take the L2
+  // evict-first policy, so the stream recycles its own lines and leaves the rest of the
+  // L2 (the other operand, split partials, and dirty lines a previous kernel left, whose
+  // write-back would share DRAM with the stream) in place.  Single-CTA tiles only.
+  // DP_FORCE_EVICT_FIRST=0 turns it off (comparisons).
+  a.evict_first = (p.pair || env_int("DP_FORCE_EVICT_FIRST", 1) == 0)
+                      ? 0
+                      : ((p.tiles_n == 1 ? 1 : 0) | (p.tiles_m == 1 ? 2 : 0));
   // Whole-tile results leave through TMA stores of the epilogue's staged blocks:
   // FP32 outputs always, BF16 outputs of units of >= 8 contraction blocks (measured on
   // GB300: -4 to -15% for FP32-output calls whose epilogue is their bound, <= 1% either

@@ -87,6 +87,11 @@ struct GemmArgs {
   // TMA streams from DRAM at about one stage per round trip slot whatever the
   // stage's size, so streaming plans carry two blocks per stage
   int32_t kps;
+  // bit 0 (A) / bit 1 (B): the operand's bytes are read once by the whole launch (one
+  // column tile reads all of A, or one row tile all of B; split units read disjoint
+  // contraction ranges), so its TMA loads carry an L2 evict-first policy and the
+  // stream replaces its own lines instead of the rest of the L2 (single-CTA tiles)
+  int32_t evict_first;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
   uint64_t wait_ns;    // limit of every barrier wait (ns); past it the kernel records a fault and unwinds
@@ -561,6 +566,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     if (lane == 0) {
       int stage = 0, sstage = 0;
       uint32_t phase = 0, sphase = 0;
+      const uint64_t pol_ef = l2_policy_evict_first();  // (for operands read once: evict_first)
       // per-stage bit masks of issued loads and their phases, for the final drain
       uint32_t issued = 0, issued_phase = 0, sissued = 0, sissued_phase = 0;
       bool ok = true;
@@ -608,14 +614,23 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             const uint32_t xf = sfull_bar(sstage);
             const int a_row0 = xc.tm * C::TM + static_cast<int>(rank) * C::BM;
             mbar_expect_tx(xf, C::SA_BYTES);
+            const bool ha = !PAIR && (args.evict_first & 1);
+            auto sload2 = [&](uint32_t dst, int32_t x, int32_t y) {
+              if (ha)
+                tma_load_2d_hint(dst, &tmA, xf, x, y, pol_ef);
+              else
+                tma_load_2d(dst, &tmA, xf, x, y);
+            };
             if (A_MN && args.a3d) {
-              tma_load_3d(xa, &tmA, xf, 0, xc.kb * C::BK, a_row0 / 32);
+              if (ha)
+                tma_load_3d_hint(xa, &tmA, xf, 0, xc.kb * C::BK, a_row0 / 32, pol_ef);
+              else
+                tma_load_3d(xa, &tmA, xf, 0, xc.kb * C::BK, a_row0 / 32);
             } else if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < C::BM / 32; ++j)
-                tma_load_2d(xa + 4096 * j, &tmA, xf, a_row0 + 32 * j, xc.kb * C::BK);
+              for (int j = 0; j < C::BM / 32; ++j) sload2(xa + 4096 * j, a_row0 + 32 * j, xc.kb * C::BK);
             } else {
-              tma_load_2d(xa, &tmA, xf, xc.kb * C::BK, a_row0);
+              sload2(xa, xc.kb * C::BK, a_row0);
             }
             sissued |= 1u << sstage;
             sissued_phase = (sissued_phase & ~(1u << sstage)) | (sphase << sstage);
@@ -638,15 +653,20 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
             const int b_row0 = bc.tn * BN + static_cast<int>(rank) * C::BNH;
             if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::B_BYTES);
+            const bool hb = !PAIR && (args.evict_first & 2);
             auto load2 = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
               if (PAIR)
                 tma_load_2d_pair(dst, map, fb, x, y);
+              else if (hb)
+                tma_load_2d_hint(dst, map, fb, x, y, pol_ef);
               else
                 tma_load_2d(dst, map, fb, x, y);
             };
             auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z) {
               if (PAIR)
                 tma_load_3d_pair(dst, map, fb, 0, y, z);
+              else if (hb)
+                tma_load_3d_hint(dst, map, fb, 0, y, z, pol_ef);
               else
                 tma_load_3d(dst, map, fb, 0, y, z);
             };
@@ -722,45 +742,53 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           // a pair's loads all complete on the leader's full barrier
           const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
           if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES * nb);
-          // (batched plans: every map has a trailing batch dimension)
-          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+          // (batched plans: every map has a trailing batch dimension; `hint`: the operand
+          // is read once by the launch, loaded with the evict-first policy)
+          auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, bool hint) {
             if (ga.batch > 1) {
               if (PAIR)
                 tma_load_3d_pair(dst, map, fb, x, y, w.b);
+              else if (hint)
+                tma_load_3d_hint(dst, map, fb, x, y, w.b, pol_ef);
               else
                 tma_load_3d(dst, map, fb, x, y, w.b);
             } else if (PAIR) {
               tma_load_2d_pair(dst, map, fb, x, y);
+            } else if (hint) {
+              tma_load_2d_hint(dst, map, fb, x, y, pol_ef);
             } else {
               tma_load_2d(dst, map, fb, x, y);
             }
           };
-          auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z) {
+          auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z, bool hint) {
             if (PAIR)
               tma_load_3d_pair(dst, map, fb, 0, y, z);
+            else if (hint)
+              tma_load_3d_hint(dst, map, fb, 0, y, z, pol_ef);
             else
               tma_load_3d(dst, map, fb, 0, y, z);
           };
+          const bool ha = (ga.evict_first & 1) != 0, hb = (ga.evict_first & 2) != 0;
           for (int j = 0; j < nb; ++j) {
             const int kb = kbs + j;
             const uint32_t sa = base + (stage * kps + j) * C::STAGE_BYTES;
             const uint32_t sb = sa + C::A_BYTES;
             // MN-major: 64-column groups of 64 contraction rows (8 KB each)
             if (a_mn && ga.a3d) {
-              load3(sa, mapA, kb * C::BK, a_row0 / 64);
+              load3(sa, mapA, kb * C::BK, a_row0 / 64, ha);
             } else if (a_mn) {
-              load(sa, mapA, a_row0, kb * C::BK);
-              load(sa + 8192, mapA, a_row0 + 64, kb * C::BK);
+              load(sa, mapA, a_row0, kb * C::BK, ha);
+              load(sa + 8192, mapA, a_row0 + 64, kb * C::BK, ha);
             } else {
-              load(sa, mapA, kb * C::BK, a_row0);
+              load(sa, mapA, kb * C::BK, a_row0, ha);
             }
             if (B_MN && ga.b3d) {
-              load3(sb, mapB, kb * C::BK, b_row0 / 64);
+              load3(sb, mapB, kb * C::BK, b_row0 / 64, hb);
             } else if (B_MN) {
 #pragma unroll
-              for (int g = 0; g < C::BNH / 64; ++g) load(sb + 8192 * g, mapB, b_row0 + 64 * g, kb * C::BK);
+              for (int g = 0; g < C::BNH / 64; ++g) load(sb + 8192 * g, mapB, b_row0 + 64 * g, kb * C::BK, hb);
             } else {
-              load(sb, mapB, kb * C::BK, b_row0);
+              load(sb, mapB, kb * C::BK, b_row0, hb);
             }
           }
           issued |= 1u << stage;

@@ -441,6 +441,7 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
                           CU_TENSOR_MAP_SWIZZLE_128B, 0, nb, bso))
                     ? 1
                     : 0;
+  a.epi_single = env_int("DP_FORCE_EPI_SINGLE", 0) != 0 ? 1 : 0;  // (comparisons)
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;
   a.fault = dev.fault;

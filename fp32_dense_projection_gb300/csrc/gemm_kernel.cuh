@@ -92,6 +92,9 @@ struct GemmArgs {
   // contraction ranges), so its TMA loads carry an L2 evict-first policy and the
   // stream replaces its own lines instead of the rest of the L2 (single-CTA tiles)
   int32_t evict_first;
+  // 1: the epilogue warps stage TMA stores in one block each even where two exist
+  // (comparisons of the two)
+  int32_t epi_single;
   float4* partials;    // split partial tiles: [split tile slot][split][BN/4][128] float4
   uint32_t* fault;     // device status word
   uint64_t wait_ns;    // limit of every barrier wait (ns); past it the kernel records a fault and unwinds
@@ -125,7 +128,11 @@ struct TileCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // one FP32 staging tile of A (X3)
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int EPI_BYTES = 4 * 4096;  // a 32 x 32 FP32 output block per epilogue warp
+  // Output staging blocks per epilogue warp (4 KB each: a 32 x 32 FP32 block, or two 32 x
+  // 32 BF16 blocks): two, so a warp stages its next block while the TMA store of the
+  // previous one still reads shared memory; one in BF16x3 mode, whose rings leave no room.
+  static constexpr int EPI_BUFS = X3 ? 1 : 2;
+  static constexpr int EPI_BYTES = 4 * 4096 * EPI_BUFS;
   // X3: four converter warps (2, 3, 8, 9: one per SM sub-partition) split A
   static constexpr int CONV_WARPS = X3 ? 4 : 0;
   static constexpr int THREADS = X3 ? 320 : 256;
@@ -574,42 +581,51 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         // Two cursors walk the same (unit, k-block) sequence: the FP32 staging loads
         // of A run ahead as far as the staging ring allows (DRAM latency), B's bf16
         // hi/lo loads as far as the MMA ring allows; neither waits for the other.
+        // (each cursor walks this slot's units -- or, for a stream-K plan, the pieces of
+        // its block range -- in order; k is the index in that list)
         struct Cursor {
-          int u, kb, kb1, tm, tn;
+          int k, kb, kb1, tm, tn;
+          bool done;
         };
-        auto seek = [&](Cursor& c, int u) {
-          for (c.u = u; c.u < args.units; c.u += unit_step) {
-            const Unit w = decode_unit(args, c.u);
+        auto seek = [&](Cursor& c, int k) {
+          for (c.k = k;; ++c.k) {
+            UnitRef ur;
+            Unit w;
+            if (!slot_unit(c.k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) {
+              c.done = true;
+              return;
+            }
             c.kb = w.kb0;
             c.kb1 = w.kb1;
             c.tm = w.tm;
             c.tn = w.tn;
-            if (c.kb < c.kb1) break;
+            c.done = false;
+            if (c.kb < c.kb1) return;
           }
         };
         auto next = [&](Cursor& c) {
-          if (++c.kb == c.kb1) seek(c, c.u + unit_step);
+          if (++c.kb == c.kb1) seek(c, c.k + 1);
         };
         Cursor xc, bc, fc;
-        seek(xc, unit0);
-        seek(bc, unit0);
-        seek(fc, unit0);
+        seek(xc, 0);
+        seek(bc, 0);
+        seek(fc, 0);
         // (a pair's peer: one arrival on the leader's full barrier per stage, once this
         // CTA's converters have filled it)
         const bool forward = PAIR && rank != 0;
         int fstage = 0;
         uint32_t fphase = 0;
-        if (!forward) fc.u = args.units;
+        if (!forward) fc.done = true;
         uint32_t idle = 0;
         uint64_t t_idle = 0;
         // The staging ring is filled first: A (FP32, the caller's) does not depend on
         // the split kernel, so its loads overlap that kernel's tail.
         bool b_ready = false;
         int issued_x = 0;
-        while (xc.u < args.units || bc.u < args.units || fc.u < args.units) {
-          if (xc.u >= args.units) issued_x = SSTAGES;  // (fewer blocks than staging slots)
+        while (!xc.done || !bc.done || !fc.done) {
+          if (xc.done) issued_x = SSTAGES;  // (fewer blocks than staging slots)
           bool progressed = false;
-          if (xc.u < args.units && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
+          if (!xc.done && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
             const uint32_t xa = sbase + sstage * C::SA_BYTES;
             const uint32_t xf = sfull_bar(sstage);
             const int a_row0 = xc.tm * C::TM + static_cast<int>(rank) * C::BM;
@@ -642,11 +658,11 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             ++issued_x;
             progressed = true;
           }
-          if (bc.u < args.units && !b_ready && issued_x >= SSTAGES) {
+          if (!bc.done && !b_ready && issued_x >= SSTAGES) {
             pdl_wait();  // B's planes come from the split kernel launched before this grid
             b_ready = true;
           }
-          if (b_ready && bc.u < args.units &&
+          if (b_ready && !bc.done &&
               (PAIR ? mbar_peek_cluster(empty_bar(stage), phase ^ 1u) : mbar_peek(empty_bar(stage), phase ^ 1u))) {
             const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
             // a pair's B loads all complete on the leader's full barrier
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             next(bc);
             progressed = true;
           }
-          if (fc.u < args.units && mbar_peek(full_bar(fstage), fphase)) {
+          if (!fc.done && mbar_peek(full_bar(fstage), fphase)) {
             mbar_arrive_cluster(map_shared_rank(full_bar(fstage), 0));
             if (++fstage == STAGES) {
               fstage = 0;
@@ -959,8 +975,10 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     int stage = 0, sstage = 0;
     uint32_t phase = 0, sphase = 0;
     bool ok = true;
-    for (int u = unit0; ok && u < args.units; u += unit_step) {
-      const Unit w = decode_unit(args, u);
+    for (int k = 0; ok; ++k) {
+      UnitRef ur;
+      Unit w;
+      if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         // every lane waits itself; the warp leaves together if any wait gives up
         const bool mine = mbar_wait(sfull_bar(sstage), sphase, args.wait_ns) &&
@@ -1007,7 +1025,12 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     const int q = warp & 3;          // TMEM sub-partition this warp may read
     const int row = q * 32 + lane;   // accumulator row == TMEM lane
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t ebuf = ebase + q * 4096;  // this warp's output block
+    const uint32_t ebuf = ebase + q * (4096 * C::EPI_BUFS);  // this warp's output block(s)
+    // TMA-store staging: the block the next store stages in (alternating when there are
+    // two), and whether the most recent bulk store, from the other block, may still be
+    // reading it
+    int sbuf = 0;
+    bool store_pending = false;
     const bool leader = threadIdx.x == 128;
     int local = 0;
     // the epilogue warps (of both CTAs of a pair) release the accumulator on the
@@ -1051,6 +1074,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         // into the zero-filled output.  Its staging waits for earlier bulk stores to
         // have read the block.)
         if (ga.tma_store && lane == 0) bulk_wait_group_read0();
+        store_pending = false;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -1065,8 +1089,9 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       } else if (!w.split) {
         // Stage and hand to TMA (which clips rows >= gm, columns >= gn) 4 KB at a
         // time: an FP32 32 x 32 block, or two BF16 32 x 32 blocks side by side (32
-        // rows of 128 bytes).  The warp's previous bulk store must have read the
-        // staging block before it is rewritten.
+        // rows of 128 bytes).  A staging block is rewritten only once the bulk store
+        // that last used it has read it: with two blocks, every store but the most
+        // recent (which used the other block) has; with one, every store.
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -1077,22 +1102,31 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           const int h = ga.out_f32 ? 0 : (c & 1);
-          if (h == 0 && lane == 0) bulk_wait_group_read0();
+          const uint32_t sb = ebuf + static_cast<uint32_t>(sbuf) * 4096u;
+          if (h == 0 && lane == 0) {
+            if (C::EPI_BUFS == 2 && !ga.epi_single && store_pending)
+              bulk_wait_group_read1();
+            else
+              bulk_wait_group_read0();
+          }
           if (ga.out_f32)
-            stage_block32(ga, ebuf, lane, v);
+            stage_block32(ga, sb, lane, v);
           else
-            stage_half64_bf16(ebuf, lane, h, v);
+            stage_half64_bf16(sb, lane, h, v);
           if (ga.out_f32 || h == 1) {
             fence_proxy_async_shared();
             __syncwarp();
             const int32_t x = static_cast<int32_t>(n0 + (c - h) * 32), y = static_cast<int32_t>(m0);
-            if (lane == 0 && x < ga.gn && y < ga.gm) {  // (blocks wholly outside: nothing to store)
+            const bool inside = x < ga.gn && y < ga.gm;  // (blocks wholly outside: nothing to store)
+            if (lane == 0 && inside) {
               if (ga.batch > 1)
-                tma_store_3d(&ga.tmO, ebuf, x, y, w.b);
+                tma_store_3d(&ga.tmO, sb, x, y, w.b);
               else
-                tma_store_2d(&ga.tmO, ebuf, x, y);
+                tma_store_2d(&ga.tmO, sb, x, y);
               bulk_commit_group();
             }
+            store_pending = inside;
+            if (C::EPI_BUFS == 2 && !ga.epi_single) sbuf ^= 1;
           }
         }
       } else {

@@ -36,6 +36,14 @@ constexpr double kNarrowB = 1.35;             // tiles whose B slice per CTA is 
                                               // 256 x 128) run their main loop this much slower than the rates say
 constexpr double kX3SplitPerNs = 20.0;        // FP32 values one SM's converter warps split into bf16 hi/lo
 constexpr double kX3BlockNs = 450.0;          // least time of one 32-wide BF16x3 block (shared-memory traffic)
+// ... in units of >= 8 blocks on tiles of <= 128 columns: forced-plan sweeps of the router at
+// T = 64-4031 (CUPTI span, cold L2) put their blocks at ~650 ns (T = 1024: forward 128 x 128 x
+// 8 splits 22.5 us against 128 x 256 x 16 splits 20.9 us; weight gradient 128 x 128 x 2
+// splits 23.4 us against 128 x 256 x 4 splits 20.2 us, where the rates above predicted the
+// opposite); in shorter units the fixed costs hide the difference (T = 64 forward: 128 x 128
+// and 128 x 256 tiles of 4 blocks within 3%)
+constexpr double kX3NarrowBlockNs = 650.0;
+constexpr int kX3NarrowMinBlocks = 8;
 constexpr bool kAutoPair = true;              // CTA-pair tiles chosen automatically (else only when forced)
 // The epilogue of one unit (TMEM -> registers -> shared -> global), per CTA: a fixed
 // cost (a CTA pair's two epilogues release one accumulator together: more), and the
@@ -156,7 +164,8 @@ double unit_ns(const View& v, const Tiling& t, int64_t kb, bool split, int64_t a
   const double narrow = (t.pair ? t.bn / 2 : t.bn) == 64 ? kNarrowB : 1.0;
   const double t_mma = kb * flop_per_kb / kFlopPerNsPerSm * (t.pair ? kPairGain : 1.0) * narrow;
   // BF16x3: the converter warps split every A element of the block
-  const double t_split = v.terms > 1 ? kb * std::max(kBlockM * v.bk / kX3SplitPerNs, kX3BlockNs) : 0.0;
+  const double x3_block = (t.bn >= 256 || kb < kX3NarrowMinBlocks) ? kX3BlockNs : kX3NarrowBlockNs;
+  const double t_split = v.terms > 1 ? kb * std::max(kBlockM * v.bk / kX3SplitPerNs, x3_block) : 0.0;
   const double dram =
       std::min(kSmDramBytesPerNs, kHbmBytesPerNs / static_cast<double>(std::max<int64_t>(1, active_sms)));
   const double bw = 1.0 / ((1.0 / reuse) / dram + (1.0 - 1.0 / reuse) * narrow / kL2BytesPerNsPerSm);
@@ -319,11 +328,11 @@ void search(const View& v, int64_t nkb, int sm, int out_bytes, const Overrides& 
       // Stream-K, for tile counts that fit in one wave: every slot takes an even share
       // of all tiles' blocks, so no SM idles while others finish a wider split.  (More
       // tiles keep the raster-ordered waves, whose neighbouring tiles share operands in
-      // L2.)  Each piece stays within the accumulation bound; BF16 operands of one
-      // problem only.
+      // L2.)  Each piece stays within the accumulation bound; one problem per launch,
+      // single-CTA tiles for BF16x3 (whose pairs are not used).
       const int64_t per_slot = ceil_div(tiles * nkb, slots);
-      if (o.stream_k != 0 && v.terms == 1 && v.batch == 1 && o.splits <= 0 && o.tail_splits <= 0 && tiles <= slots &&
-          tiles * nkb >= 2 * slots && std::min(per_slot, nkb) <= max_blocks) {
+      if (o.stream_k != 0 && (v.terms == 1 || !pair) && v.batch == 1 && o.splits <= 0 && o.tail_splits <= 0 &&
+          tiles <= slots && tiles * nkb >= 2 * slots && std::min(per_slot, nkb) <= max_blocks) {
         const int64_t most = stream_k_pieces(tiles, nkb, slots, nullptr);
         if (most >= 2 && cta_tiles * most <= kMaxSplitTiles) {
           consider(t, 0, most, stream_k_model_ns(v, t, tiles, nkb, sm, out_bytes), true);

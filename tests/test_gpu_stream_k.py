@@ -91,3 +91,49 @@ def test_stream_k_repeats_and_replays(monkeypatch):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
     no_device_fault()
+
+
+@pytest.mark.parametrize("op,T,N,K", [("router_fwd", 1000, 256, 1024), ("router_fwd", 129, 136, 4096),
+                                      ("router_wgrad", 4100, 256, 512), ("router_wgrad", 300, 136, 2048)])
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_stream_k_router_integer_exact(monkeypatch, op, T, N, K, bn):
+    # BF16x3 pieces: the in-kernel split of the streamed FP32 operand walks the slot's
+    # pieces like the MMA issuer and the epilogue; integer operands are bf16-exact
+    force(monkeypatch, bn=bn)
+    monkeypatch.setenv("DP_FORCE_FFMA", "0")
+    p = stream_k_plan(op, T, N, K, True)
+    if p is None:
+        pytest.skip("no stream-K plan of this tile width for the shape")
+    c = inputs.integer_case(T, N, K, seed=T + N + bn, dtype=torch.float32)
+    a, b = operands(op, c)
+    got = gpu(op, a.to(DEV), b.to(DEV))
+    assert np.array_equal(as_f64(got), full_ref(op, a, b)), (op, T, N, K, bn, p)
+    no_device_fault()
+
+
+@pytest.mark.parametrize("op", ["router_fwd", "router_wgrad"])
+@pytest.mark.parametrize("T", [1024, 16384])
+def test_stream_k_router_budget_and_repeats(monkeypatch, op, T):
+    force(monkeypatch)
+    monkeypatch.setenv("DP_FORCE_FFMA", "0")
+    p = stream_k_plan(op, T, 256, 4096, True)
+    assert p is not None and p["program"] == 0
+    c = inputs.router(T, 4096, seed=T % 7, experts=256)
+    a, b = operands(op, c)
+    d = {k: v.to(DEV) for k, v in c.items()}
+    got = gpu(op, *operands(op, d))
+    if T == 1024:
+        assert_budget(as_f64(got), full_ref(op, a, b), "f32", f"stream-K {op} T={T}")
+    else:  # sampled: eight elements in every 128 x 128 block, plus the last row and column
+        from gpu_common import sampled_ref, stratified_points
+        shape = tuple(got.shape)
+        rows, cols = stratified_points(shape, np.random.default_rng(T))
+        rows = np.concatenate([rows, np.full(shape[1], shape[0] - 1), np.arange(shape[0])])
+        cols = np.concatenate([cols, np.arange(shape[1]), np.full(shape[0], shape[1] - 1)])
+        ref = sampled_ref(op, a, b, rows, cols)
+        g = got[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].double().cpu().numpy()
+        assert_budget(g, ref, "f32", f"stream-K {op} T={T}")
+    for _ in range(3):
+        again = gpu(op, *operands(op, d))
+        assert torch.equal(again.view(torch.int32), got.view(torch.int32))
+    no_device_fault()

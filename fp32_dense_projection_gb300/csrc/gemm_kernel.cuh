@@ -123,11 +123,28 @@ struct TileCfg {
   static constexpr int SSTAGES = X3 ? staging_stages_x3(BN, PAIR) : 0;  // FP32 staging ring (X3)
   static constexpr int A_HALF = BM * BK * 2;     // one bf16 copy of the A tile
   static constexpr int B_HALF = BNH * BK * 2;
-  static constexpr int A_BYTES = X3 ? 2 * A_HALF : A_HALF;
+  // (X3 on a single CTA: A's halves in tensor memory, none in the stage)
+  static constexpr int A_BYTES = X3 ? (PAIR ? 2 * A_HALF : 0) : A_HALF;
   static constexpr int B_BYTES = X3 ? 2 * B_HALF : B_HALF;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SA_BYTES = X3 ? BM * BK * 4 : 0;  // one FP32 staging tile of A (X3)
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // X3 on single CTAs: the converter warps write A's bf16 hi and lo halves into tensor
+  // memory (32 columns per ring stage: hi in the first 16, lo in the next 16, two bf16 per
+  // 32-bit column, row = lane) and the MMAs read A from there, which takes A's writes and
+  // its three reads per slice off the shared-memory port (CTA pairs keep A in shared memory)
+  static constexpr bool A_TMEM = X3 && !PAIR;
+  static_assert(!X3 || A_TMEM == (A_BYTES == 0), "BF16x3 stage layout");
+  // accumulators: two (a unit's epilogue overlaps the next unit's main loop), or one where
+  // the A stages would not fit beside two (256-wide BF16x3 tiles)
+  static constexpr int NACC = (A_TMEM && 2 * BN + STAGES * 32 > 512) ? 1 : 2;
+  static constexpr int A_TMEM_COL = NACC * BN;  // first column of the A stages
+  static constexpr int TMEM_NEED = NACC * BN + (A_TMEM ? STAGES * 32 : 0);
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
+                                   : TMEM_NEED <= 64  ? 64
+                                   : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256
+                                                      : 512;
+  static_assert(TMEM_NEED <= 512, "tensor memory");
   // Output staging blocks per epilogue warp (4 KB each: a 32 x 32 FP32 block, or two 32 x
   // 32 BF16 blocks): two, so a warp stages its next block while the TMA store of the
   // previous one still reads shared memory; one in BF16x3 mode, whose rings leave no room.
@@ -495,6 +512,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
   constexpr int SSTAGES = C::SSTAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(C::TM, BN, A_MN, B_MN);
   constexpr uint32_t IDESC_AMN = idesc_bf16_f32(C::TM, BN, true, B_MN);  // (DUAL: MN-major A)
+  constexpr uint32_t IDESC_TS = idesc_bf16_f32(C::TM, BN, false, B_MN);  // (A in tensor memory: K-major)
   const int total_units = args.units + second_units(second);
   // With PAIR, a cluster of two CTAs computes one TM x BN tile: rank r loads A rows
   // [r*128, r*128+128) and B rows [r*BN/2, (r+1)*BN/2) of the tile into the same
@@ -855,8 +873,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         const bool a_mn = DUAL ? ur.a->a_mn != 0 : A_MN;  // (one problem: the template's)
         const uint32_t idesc = (DUAL && a_mn) ? IDESC_AMN : IDESC;
         const int kb0 = w.kb0, kb1 = w.kb1;
-        const int acc = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+        const int acc = C::NACC == 2 ? (local & 1) : 0;
+        const uint32_t aph = C::NACC == 2 ? ((local >> 1) & 1) : (local & 1);
         if (!mbar_wait<PAIR>(tempty_bar(acc), aph ^ 1u, args.wait_ns)) {
           atomicOr(args.fault, kFaultMmaWait);
           break;
@@ -887,6 +905,16 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
                 auto d_b = [&](uint32_t t) {
                   return B_MN ? sdesc(t + kk * 2048, 4096, 1024, 2) : sdesc(t + kk * 32, 16, 512, 4);
                 };
+                if constexpr (C::A_TMEM) {
+                  // A's halves of this stage in tensor memory: hi in columns [0, 16), lo in
+                  // [16, 32); 8 columns (16 contraction elements) per MMA
+                  const uint32_t a_t = tmem_base + static_cast<uint32_t>(C::A_TMEM_COL + stage * 32 + kk * 8);
+                  const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
+                  mma_bf16_ts(d_tmem, a_t + 16, b_hi, IDESC_TS, (kb > kb0 || kk > 0) ? 1u : 0u);
+                  mma_bf16_ts(d_tmem, a_t, b_lo, IDESC_TS, 1u);
+                  mma_bf16_ts(d_tmem, a_t, b_hi, IDESC_TS, 1u);
+                  continue;
+                }
                 const uint64_t a_hi = d_a(sa), a_lo = d_a(sa + C::A_HALF);
                 const uint64_t b_hi = d_b(sb), b_lo = d_b(sb + C::B_HALF);
                 // x*w ~ lo_x*hi_w + hi_x*lo_w + hi_x*hi_w (lo*lo dropped), small terms first
@@ -949,6 +977,81 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     // The 512 tasks of a stage are dealt round-robin to the 128 converter threads;
     // their shared-memory offsets do not depend on the stage, so they are computed
     // once, and each thread loads all of its chunks before converting any.
+    // Single CTAs (A_TMEM) write the halves into tensor memory instead: thread i of
+    // warp w converts row 32 (w % 4) + i (the TMEM lane quarter warp w may access) and
+    // stores its 32 hi and 32 lo values as two 16-column rows of the stage's columns.
+    if constexpr (C::A_TMEM) {
+      const int sub = warp & 3;
+      const int r = sub * 32 + lane;  // row of A == TMEM lane
+      const uint32_t trow = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(C::A_TMEM_COL);
+      // this thread's FP32 row in a staging tile -- K-major: 8 16-byte chunks of row r,
+      // chunk j at j ^ (r % 8); MN-major: element (k, r) of the 32 x 32 box r / 32, at row
+      // k, 16-byte chunk (r % 32) / 4 ^ (k % 8), word r % 4
+      const uint32_t kmaj_row = static_cast<uint32_t>(r) * 128u;
+      const uint32_t mn_col = static_cast<uint32_t>(r >> 5) * 4096u + static_cast<uint32_t>(r & 3) * 4u;
+      const int mn_c4 = (r & 31) >> 2;
+      int stage = 0, sstage = 0;
+      uint32_t phase = 0, sphase = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        UnitRef ur;
+        Unit w;
+        if (!slot_unit(k, unit0, unit_step, total_units, args, tmA, tmB, second, &ur, &w)) break;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          // every lane waits itself; the warp leaves together if any wait gives up
+          const bool mine = mbar_wait(sfull_bar(sstage), sphase, args.wait_ns) &&
+                             mbar_wait(empty_bar(stage), phase ^ 1u, args.wait_ns);
+          if (!__all_sync(0xffffffffu, mine)) {
+            if (lane == 0) atomicOr(args.fault, kFaultProducerWait);
+            ok = false;
+            break;
+          }
+          const uint32_t xs = sbase + sstage * C::SA_BYTES;
+          float4 v[8];
+          if (A_MN) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float e[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int kk = 4 * j + q;
+                e[q] = ld_shared_f32(xs + mn_col + kk * 128 + ((mn_c4 ^ (kk & 7)) << 4));
+              }
+              v[j] = make_float4(e[0], e[1], e[2], e[3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = ld_shared_f4(xs + kmaj_row + ((j ^ (r & 7)) << 4));
+          }
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 h, l;
+            split8_bf16x3(v[2 * j], v[2 * j + 1], h, l);
+            hi[4 * j] = h.x, hi[4 * j + 1] = h.y, hi[4 * j + 2] = h.z, hi[4 * j + 3] = h.w;
+            lo[4 * j] = l.x, lo[4 * j + 1] = l.y, lo[4 * j + 2] = l.z, lo[4 * j + 3] = l.w;
+          }
+          const uint32_t ta = trow + static_cast<uint32_t>(stage * 32);
+          tmem_st_32x32b_x16(ta, hi);
+          tmem_st_32x32b_x16(ta + 16, lo);
+          tmem_wait_st();     // the halves are in tensor memory
+          tc_fence_before();  // ... before the arrival that lets the MMAs read them
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(sempty_bar(sstage));  // staging tile may be reloaded
+            mbar_arrive(full_bar(stage));     // this warp's quarter of A is ready
+          }
+          if (++sstage == SSTAGES) {
+            sstage = 0;
+            sphase ^= 1u;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    } else {
     constexpr int NCT = (X3 ? C::CONV_WARPS : 4) * 32;  // (the branch only runs with X3)
     constexpr int kTasks = 512 / NCT;
     static_assert(512 % NCT == 0, "converter tasks");
@@ -1020,6 +1123,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
     }
+    }  // (A in shared memory)
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // TMEM sub-partition this warp may read
@@ -1052,8 +1156,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       const GemmArgs& ga = DUAL ? *ur.a : args;  // (one problem: the kernel's own parameters)
       const int tm = w.tm, tn = w.tn;
       const int slot = w.ptile * (PAIR ? 2 : 1) + static_cast<int>(rank);  // this CTA's partial slot
-      const int acc = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+      const int acc = C::NACC == 2 ? (local & 1) : 0;
+      const uint32_t aph = C::NACC == 2 ? ((local >> 1) & 1) : (local & 1);
       // One thread waits; the outcome reaches the other 127 through a named barrier,
       // so all of them leave together if the wait gives up.
       if (leader) {

@@ -104,19 +104,30 @@ constexpr int stages_for(int bn, bool pair = false) { return stages_for_rows(pai
 // The FP32 router's BF16x3 GEMM (forward and weight gradient) streams 32-wide
 // contraction blocks.  The streamed FP32 operand A is loaded by TMA into a staging
 // ring (128 x 32 FP32 = 16 KB per stage) and split into bf16 hi/lo by converter
-// warps; the reused operand B arrives already split, as two bf16 planes.  A stage
-// of the MMA ring holds [A_hi | A_lo | B_hi | B_lo] ((128 + bn) x 32 x 2 x 2 bytes).
-// The staging ring is one stage deeper than the MMA ring; both fit in 208 KB.
+// warps; the reused operand B arrives already split, as two bf16 planes.  On a single
+// CTA the converters write A's halves into tensor memory, so a stage of the MMA ring
+// holds [B_hi | B_lo] (bn x 32 x 2 x 2 bytes): 3 stages for 256-wide tiles, 4 for
+// narrower ones; the staging ring of A's DRAM stream takes the rest of 208 KB (7, 9 and
+// 11 slots for 256-, 128- and 64-wide tiles).  (Measured on GB300 against 3 + 4 slots and
+// against 4 + 5: the same time within 2%.)  A CTA pair keeps A in shared memory: a stage holds
+// [A_hi | A_lo | B_hi | B_lo] (half of B's rows) and the staging ring is one stage
+// deeper than the MMA ring.
 constexpr int kRouterBlockK = 32;
 constexpr int kX3StagingBytes = kBlockM * kRouterBlockK * 4;
-// (a CTA of a pair holds half of B's rows)
-constexpr int x3_stage_bytes(int bn, bool pair = false) { return (kBlockM + (pair ? bn / 2 : bn)) * kRouterBlockK * 4; }
-constexpr int stages_x3(int bn, bool pair = false) {
-  return (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes) < 6
-             ? (208 * 1024 - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes)
-             : 6;
+constexpr int kX3RingBytes = 208 * 1024;
+constexpr int x3_stage_bytes(int bn, bool pair = false) {
+  return pair ? (kBlockM + bn / 2) * kRouterBlockK * 4 : bn * kRouterBlockK * 4;
 }
-constexpr int staging_stages_x3(int bn, bool pair = false) { return stages_x3(bn, pair) + 1; }
+constexpr int stages_x3(int bn, bool pair = false) {
+  return pair ? ((kX3RingBytes - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes) < 6
+                     ? (kX3RingBytes - kX3StagingBytes) / (x3_stage_bytes(bn, pair) + kX3StagingBytes)
+                     : 6)
+              : (bn >= 256 ? 3 : 4);
+}
+constexpr int staging_stages_x3(int bn, bool pair = false) {
+  return pair ? stages_x3(bn, pair) + 1
+              : (kX3RingBytes - stages_x3(bn, pair) * x3_stage_bytes(bn, pair)) / kX3StagingBytes;
+}
 
 // Overrides of the planner's choices, for tests and tuning (all unset in normal
 // use): > 0 forces the tile width / uniform split count / last-wave split count;

@@ -18,7 +18,7 @@ Budgets (FlashInfer page "perf(cake_dense_projection_gemm): restore the K1
 weight-gradient routes ...", PR body): BF16 output atol = rtol = 1e-2 with zero
 violations; FP32 output rel_fro <= 5e-5 and max_abs <= 1e-3 * max|ref|.  That page's
 accuracy sweep records that its deterministic program misses the BF16 budget for
-some seeds at T around 47k-65k; the margins here show where this build stands.
+some seeds at T around 47k-65k; the margins recorded here show how far each cell stays from it.
 """
 import numpy as np
 import pytest

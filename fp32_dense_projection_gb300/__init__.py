@@ -50,7 +50,8 @@ class PlanInfo(ctypes.Structure):
         "gemm_m", "gemm_n", "gemm_k", "tiles_m", "tiles_n", "k_blocks", "units", "full_units")] + [
         ("workspace_bytes", ctypes.c_uint64), ("model_us", ctypes.c_double),
         ("batch", ctypes.c_int64), ("tiles", ctypes.c_int64), ("weight_kn", ctypes.c_int32),
-        ("program", ctypes.c_int32), ("atomic", ctypes.c_int32), ("blocks_per_stage", ctypes.c_int32)]
+        ("program", ctypes.c_int32), ("atomic", ctypes.c_int32), ("blocks_per_stage", ctypes.c_int32),
+        ("cluster_sum", ctypes.c_int32)]
 
 
 class BwdPlanInfo(ctypes.Structure):

@@ -618,6 +618,14 @@ void fill_info(const Plan& p, int64_t T, dp_plan_info* info) {
   info->atomic = p.atomic ? 1 : 0;
   info->blocks_per_stage = p.kps;
   info->model_us = p.model_ns * 1e-3;
+  info->cluster_sum = -1;  // (known for the current device only: set by the plan queries)
+}
+
+// The in-cluster sum of a plan on the current device (dp_plan_info::cluster_sum).
+int32_t cluster_sum_here(const Plan& p) {
+  DeviceState* ds = nullptr;
+  if (current_device(&ds) != DP_OK) return -1;  // (current_device sets the kernels' attributes)
+  return p.ffma ? 0 : cluster_fixup(p, p.op == kOpRouterFwd || p.op == kOpRouterWgrad, *ds);
 }
 
 // Batched BF16 ops: B independent problems in one launch.  Operand / output matrix
@@ -868,6 +876,7 @@ dp_status dp_plan_query_ex(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dty
   if (!info || static_cast<int>(op) < 0 || static_cast<int>(op) > kOpRouterWgrad) return DP_ERR_INVALID_ARG;
   const dp_status st = check_sizes(T, N, K, static_cast<int>(op));
   if (st != DP_OK) return st;
+  const bool this_device = sm_count <= 0;
   if (sm_count <= 0) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -880,6 +889,7 @@ dp_status dp_plan_query_ex(dp_op op, int64_t T, int64_t N, int64_t K, dp_out_dty
                 deterministic))
     return DP_ERR_INVALID_ARG;
   fill_info(p, T, info);
+  if (this_device) info->cluster_sum = cluster_sum_here(p);
   return DP_OK;
 }
 
@@ -917,6 +927,7 @@ dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64
   if (B > 0xFFFFFF) return DP_ERR_UNSUPPORTED;
   const dp_status st = check_sizes(T, N, K, static_cast<int>(op));
   if (st != DP_OK) return st;
+  const bool this_device = sm_count <= 0;
   if (sm_count <= 0) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -927,6 +938,7 @@ dp_status dp_plan_query_batched(dp_op op, int64_t B, int64_t T, int64_t N, int64
   if (!plan_for(static_cast<int>(op), T, N, K, out == DP_OUT_F32 ? 1 : 0, sm_count, &p, B, weight_kn))
     return DP_ERR_INVALID_ARG;
   fill_info(p, T, info);
+  if (this_device) info->cluster_sum = cluster_sum_here(p);
   return DP_OK;
 }
 
@@ -964,6 +976,7 @@ dp_status dp_plan_query_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx
     return DP_ERR_INVALID_ARG;
   const dp_status st = check_sizes(T, N, K, kOpDgrad);
   if (st != DP_OK) return st;
+  const bool this_device = sm_count <= 0;
   if (sm_count <= 0) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -974,6 +987,10 @@ dp_status dp_plan_query_bwd(int64_t T, int64_t N, int64_t K, dp_out_dtype out_dx
   if (!bwd_plan_for(T, N, K, out_dx == DP_OUT_F32 ? 1 : 0, out_dw == DP_OUT_F32 ? 1 : 0, sm_count, &bp))
     return DP_ERR_INVALID_ARG;
   fill_bwd_info(bp, T, info);
+  if (this_device) {  // (a co-scheduled launch keeps whole K per tile: no split sums)
+    info->dgrad.cluster_sum = cluster_sum_here(bp.dgrad);
+    info->wgrad.cluster_sum = cluster_sum_here(bp.wgrad);
+  }
   return DP_OK;
 }
 

@@ -438,13 +438,48 @@ __device__ __forceinline__ void store_block32(const GemmArgs& a, void* out, uint
   flush_block32(a, out, buf, lane, m0, col0, add);
 }
 
+// Four output rows of a transposed store: D[m..m+3][col..col+3] (acc[i] = row m+i,
+// columns col..col+3) go to out[(col+t)*ldo + m .. m+3], one 16-byte (FP32) or 8-byte
+// (BF16) store per column.  m is a multiple of 4 and ldo, the output's base and its
+// batch stride are 16-byte multiples, so every store is aligned.
+__device__ __forceinline__ void store_trans4x4(const GemmArgs& a, void* out, int64_t m, int64_t col,
+                                               const float4 (&acc)[4]) {
+  const float c[4][4] = {{acc[0].x, acc[1].x, acc[2].x, acc[3].x},
+                         {acc[0].y, acc[1].y, acc[2].y, acc[3].y},
+                         {acc[0].z, acc[1].z, acc[2].z, acc[3].z},
+                         {acc[0].w, acc[1].w, acc[2].w, acc[3].w}};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int64_t o = (col + t) * a.ldo + m;
+    if (a.out_f32)
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = make_float4(c[t][0], c[t][1], c[t][2], c[t][3]);
+    else
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + o) =
+          make_uint2(pack_bf16x2(c[t][0], c[t][1]), pack_bf16x2(c[t][2], c[t][3]));
+  }
+}
+
+// acc = x (k == 0) or acc += x: the ordered sum's step.
+__device__ __forceinline__ void sum_step(float4& acc, const float4& x, bool first) {
+  if (first) {
+    acc = x;
+  } else {
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
+  }
+}
+
 // In-kernel ordered sum for cluster plans: the S CTAs of a cluster computed the S
 // splits of one tile (CTA rank r = split r, one unit each) and wrote their FP32
 // partials.  After a cluster barrier (release / acquire, so every partial is
-// visible), CTA r sums rows [r*128/S, (r+1)*128/S) of the tile over all S partials
-// in ascending split order and rounds once: the same arithmetic as the reduction
-// kernel, so the two give the same bits.  One float4 per step, its S loads issued
-// together; consecutive threads take consecutive rows (512-byte partial reads).
+// visible), CTA r sums its rows of the tile, [4*floor(32r/S), 4*floor(32(r+1)/S)),
+// over all S partials in ascending split order and rounds once: the same arithmetic
+// as the reduction kernel, so the two give the same bits.  Row-major output: one
+// float4 per step, consecutive threads on consecutive rows (512-byte partial reads).
+// Transposed output (the swapped weight gradient): four rows per step, so each output
+// column gets one 8- or 16-byte store instead of four element stores.
 template <int BN>
 __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthreads) {
   __threadfence();
@@ -452,11 +487,38 @@ __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthread
   const int S = a.splits;
   const int u = static_cast<int>(blockIdx.x);  // this CTA's only unit
   const Unit w = decode_unit(a, u);
-  const int r0 = w.s * kBlockM / S, r1 = (w.s + 1) * kBlockM / S, rows = r1 - r0;
+  const int r0 = 4 * (w.s * (kBlockM / 4) / S), r1 = 4 * ((w.s + 1) * (kBlockM / 4) / S), rows = r1 - r0;
   const int64_t m_tile = static_cast<int64_t>(w.tm) * kBlockM, n0 = static_cast<int64_t>(w.tn) * BN;
   const size_t pstride = static_cast<size_t>(kBlockM) * BN / 4;
   const float4* p0 = a.partials + static_cast<size_t>(w.ptile) * S * pstride;
   void* out = out_at(a, w.b);
+  if (a.out_trans) {
+    const int groups = rows / 4, total = groups * (BN / 4);
+    for (int e = static_cast<int>(threadIdx.x); e < total; e += nthreads) {
+      const int j4 = e / groups, row = r0 + 4 * (e - j4 * groups);
+      const int64_t m = m_tile + row, col = n0 + 4 * j4;
+      if (m >= a.gm || col >= a.gn) continue;  // (gm and gn are multiples of 4)
+      const float4* src = p0 + static_cast<size_t>(j4) * kBlockM + row;
+      float4 acc[4];
+#pragma unroll
+      for (int k0 = 0; k0 < 8; k0 += 4) {  // four splits' loads in flight at a time
+        if (k0 >= S) break;
+        float4 x[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (k0 + k < S) x[k][i] = __ldcg(src + (k0 + k) * pstride + i);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k0 + k < S)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sum_step(acc[i], x[k][i], k0 + k == 0);
+      }
+      store_trans4x4(a, out, m, col, acc);
+    }
+    return;
+  }
   const int total = rows * (BN / 4);
   for (int e = static_cast<int>(threadIdx.x); e < total; e += nthreads) {
     const int j4 = e / rows, row = r0 + (e - j4 * rows);
@@ -470,27 +532,8 @@ __device__ __forceinline__ void cluster_fixup_sum(const GemmArgs& a, int nthread
       if (k < S) x[k] = __ldcg(src + k * pstride);
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      if (k < S) {
-        if (k == 0) {
-          acc = x[k];
-        } else {
-          acc.x += x[k].x;
-          acc.y += x[k].y;
-          acc.z += x[k].z;
-          acc.w += x[k].w;
-        }
-      }
-    if (a.out_trans) {
-      const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int64_t o = (col + t) * a.ldo + m;
-        if (a.out_f32)
-          static_cast<float*>(out)[o] = v[t];
-        else
-          static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(v[t], 0.0f) & 0xFFFFu);
-      }
-    } else if (a.out_f32) {
+      if (k < S) sum_step(acc, x[k], k == 0);
+    if (a.out_f32) {
       *reinterpret_cast<float4*>(static_cast<float*>(out) + m * a.ldo + col) = acc;
     } else {
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * a.ldo + col) =

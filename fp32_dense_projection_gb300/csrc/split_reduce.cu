@@ -27,23 +27,26 @@ struct ReduceArgs {
   int32_t chunks;          // 32-column chunks per tile
 };
 
-// One thread per float4 of the split tiles: thread t of the (slot, 32-column chunk)
-// handles row t % 128 and float4 column t / 128 of the chunk, so a warp's loads are
-// 512 contiguous bytes of each partial, and loads all splits (up to 16 at a time)
-// before adding them in order.  Partial layout: [slot][split][bn/4][128] float4.
-// A thread stores its 4 values to the row-major output as one 16-byte store (or 8
-// bytes of bf16), or to the transposed output (swapped weight gradient) as 4
-// elements, each next to its neighbouring rows' (consecutive lanes, consecutive m).
+// Row-major output: one thread per float4 of the split tiles.  Thread t of the (slot,
+// 32-column chunk) handles row t % 128 and float4 column t / 128 of the chunk, so a
+// warp's loads are 512 contiguous bytes of each partial, and loads all splits (up to
+// 16 at a time) before adding them in order; it stores its 4 values as one 16-byte
+// store (or 8 bytes of bf16).  Transposed output (the swapped weight gradient): one
+// thread per 4 rows of a float4 column (thread t: rows 4(t % 32) .. +3, float4 column
+// t / 32), which it writes as one 16-byte (8-byte) store per output column, next to
+// its neighbouring lanes' rows.  Partial layout: [slot][split][bn/4][128] float4.
 constexpr int kReduceThreads = 128;
 constexpr int kReduceBatch = 16;
+constexpr int kReduceBatchTrans = 4;  // (four rows each: 16 float4 loads in flight)
 
 __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __grid_constant__ ReduceArgs ra) {
   pdl_wait();  // the GEMM's partials are complete and visible
   const GemmArgs& a = ra.g;
-  const int per_slice = kBlockM * 8 / kReduceThreads;  // CTAs per (slot, chunk): 1024 float4
+  // CTAs per (slot, chunk): 1024 float4, one or four per thread
+  const int per_slice = (a.out_trans ? kBlockM * 8 / 4 : kBlockM * 8) / kReduceThreads;
   const int cta = static_cast<int>(blockIdx.x);
   const int slice = cta / per_slice;
-  const int t = (cta - slice * per_slice) * kReduceThreads + static_cast<int>(threadIdx.x);  // 0..1023
+  const int t = (cta - slice * per_slice) * kReduceThreads + static_cast<int>(threadIdx.x);  // 0..1023 (255)
   const int chunk = slice % ra.chunks;
   const int slot = slice / ra.chunks;
   const int ptile = slot / ra.slots_per_tile, rank = slot - ptile * ra.slots_per_tile;
@@ -58,13 +61,32 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
   int bt, tm, tn;
   tile_coords(a, a.full_units + ptile, &bt, &tm, &tn);
   void* out = out_at(a, bt);
-  const int row = t & (kBlockM - 1), j = t >> 7;  // row of the slot, float4 column in the chunk
+  // row of the slot (the first of four: transposed output), float4 column in the chunk
+  const int row = a.out_trans ? 4 * (t & 31) : t & (kBlockM - 1), j = a.out_trans ? t >> 5 : t >> 7;
   const int64_t m = static_cast<int64_t>(tm) * ra.tile_rows + rank * kBlockM + row;
   const int64_t col = static_cast<int64_t>(tn) * ra.bn + chunk * 32 + 4 * j;
-  if (m >= a.gm || col >= a.gn) return;
+  if (m >= a.gm || col >= a.gn) return;  // (transposed: gm and gn are multiples of 4)
   const size_t pstride = static_cast<size_t>(kBlockM) * ra.bn / 4;  // float4 per partial tile
   const float4* src = a.partials + static_cast<size_t>(slot) * a.splits * pstride +
                       static_cast<size_t>(chunk * 8 + j) * kBlockM + row;
+  if (a.out_trans) {
+    float4 acc[4];
+    for (int s0 = 0; s0 < nparts; s0 += kReduceBatchTrans) {
+      float4 x[kReduceBatchTrans][4];
+#pragma unroll
+      for (int k = 0; k < kReduceBatchTrans; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (s0 + k < nparts) x[k][i] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride + i);
+#pragma unroll
+      for (int k = 0; k < kReduceBatchTrans; ++k)
+        if (s0 + k < nparts)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sum_step(acc[i], x[k][i], s0 + k == 0);
+    }
+    store_trans4x4(a, out, m, col, acc);
+    return;
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // splits in ascending order: acc = p_0, then acc += p_s
   for (int s0 = 0; s0 < nparts; s0 += kReduceBatch) {
@@ -74,28 +96,9 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
       if (s0 + k < nparts) x[k] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride);
 #pragma unroll
     for (int k = 0; k < kReduceBatch; ++k)
-      if (s0 + k < nparts) {
-        if (s0 + k == 0) {
-          acc = x[k];
-        } else {
-          acc.x += x[k].x;
-          acc.y += x[k].y;
-          acc.z += x[k].z;
-          acc.w += x[k].w;
-        }
-      }
+      if (s0 + k < nparts) sum_step(acc, x[k], s0 + k == 0);
   }
-  if (a.out_trans) {
-    const float e[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t o = (col + q) * a.ldo + m;
-      if (a.out_f32)
-        static_cast<float*>(out)[o] = e[q];
-      else
-        static_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(pack_bf16x2(e[q], 0.0f) & 0xFFFFu);
-    }
-  } else if (a.out_f32) {
+  if (a.out_f32) {
     *reinterpret_cast<float4*>(static_cast<float*>(out) + m * a.ldo + col) = acc;
   } else {
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + m * a.ldo + col) =
@@ -112,7 +115,8 @@ cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t 
   ra.tile_rows = pair ? 2 * kBlockM : kBlockM;
   ra.slots_per_tile = pair ? 2 : 1;
   ra.chunks = bn / 32;
-  const int64_t blocks = split_tiles * ra.slots_per_tile * ra.chunks * (kBlockM * 8 / kReduceThreads);
+  const int64_t blocks = split_tiles * ra.slots_per_tile * ra.chunks *
+                        ((l.args.out_trans ? kBlockM * 8 / 4 : kBlockM * 8) / kReduceThreads);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};

@@ -336,6 +336,13 @@ typedef struct dp_plan_info {
     int32_t blocks_per_stage; /* contraction blocks per stage of the operand ring (1 or 2: a
                                  stage's loads complete on one barrier, so streaming plans
                                  carry two blocks per stage in half as many stages) */
+    int32_t cluster_sum;      /* split plans with one unit per CTA: the tile's `splits` CTAs
+                                 run as one thread-block cluster and sum their partials
+                                 themselves after the main loop, with no reduction kernel
+                                 (the cluster size, 2..8).  0: the reduction kernel sums the
+                                 split partials, or the plan has none.  It depends on how
+                                 many such clusters the device runs at once, so it is known
+                                 only for the current device (sm_count <= 0); -1 otherwise */
 } dp_plan_info;
 
 /* Fill `info` with the plan for a call on a GPU with `sm_count` SMs

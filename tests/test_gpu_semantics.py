@@ -224,6 +224,50 @@ def test_cluster_sum_matches_reduction_kernel(monkeypatch, op, T, N, K):
     no_device_fault()
 
 
+# (op, T, N, K, forced split count or None for the planner's): clusters of 2 to 8 CTAs,
+# transposed output (the swapped weight gradient) and row-major output, a ragged
+# N = 48 (padding columns), the forward split over K, and the router's BF16x3 tiles
+CLUSTER_CASES = [("wgrad", 16173, 64, 4096, 2), ("wgrad", 16173, 64, 4096, 3), ("wgrad", 16173, 64, 4096, None),
+                 ("wgrad", 4100, 64, 512, 5), ("wgrad", 4100, 64, 512, 6), ("wgrad", 4100, 64, 512, 7),
+                 ("wgrad", 4100, 64, 512, 8), ("wgrad", 4100, 64, 1024, None), ("wgrad", 16173, 128, 4096, None),
+                 ("wgrad", 16173, 48, 5120, None), ("fwd", 64, 1024, 4096, None), ("router_wgrad", 1024, 256, 4096, None)]
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("op,T,N,K,S", CLUSTER_CASES)
+def test_cluster_sum_every_cluster_size(monkeypatch, op, T, N, K, S, out_f32):
+    """A plan with one split unit per CTA adds its partials inside the GEMM's clusters
+    (the plan reports the cluster size): CTA r of the cluster sums its share of the
+    tile's rows over all partials in ascending split order, which gives the reduction
+    kernel's bits, whatever the cluster size, output type or orientation."""
+    router = op.startswith("router")
+    if router and not out_f32:
+        pytest.skip("the router's output is FP32")
+    if S:
+        monkeypatch.setenv("DP_FORCE_SPLITS", str(S))
+    p = dp.plan(op, T, N, K, out_f32=out_f32)
+    assert (p["splits"] == S if S else p["splits"] > 1), p
+    assert p["full_units"] == 0 and not p["cta_pair"] and p["units"] == p["grid"] and p["splits"] <= 8, p
+    if p["cluster_sum"] == 0 and p["splits"] > 4 and p["grid"] > 64:
+        # (clusters live inside one GPC: how many of 5 to 8 CTAs run at once depends on
+        # the device's GPCs; the reduction kernel sums such plans)
+        pytest.skip(f"the device co-schedules too few clusters of {p['splits']} CTAs for {p['grid']} CTAs")
+    assert p["cluster_sum"] == p["splits"], p
+    c = {k: v.to(DEV) for k, v in case_tensors(op, T, N, K).items()}
+    a, b = operands(op, c)
+    kw = {} if router else {"out_dtype": torch.float32 if out_f32 else torch.bfloat16}
+    in_cluster = gpu(op, a, b, **kw)
+    monkeypatch.setenv("DP_FORCE_CLUSTER_SUM", "0")
+    assert dp.plan(op, T, N, K, out_f32=out_f32)["cluster_sum"] == 0
+    by_kernel = gpu(op, a, b, **kw)
+    bits = torch.int32 if out_f32 else torch.int16
+    assert torch.equal(in_cluster.view(bits), by_kernel.view(bits))
+    if T * N * K <= (1 << 31):
+        ref = full_ref(op, *operands(op, case_tensors(op, T, N, K)))
+        assert_budget(as_f64(in_cluster), ref, "f32" if out_f32 else "bf16", f"{op} T={T} S={p['splits']}")
+    no_device_fault()
+
+
 
 def test_dependent_calls_keep_their_order():
     # Consecutive GEMMs overlap only their setup with the previous kernel: a call that

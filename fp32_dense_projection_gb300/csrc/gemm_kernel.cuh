@@ -2,7 +2,8 @@
 //     D[m][n] = sum_k A(m, k) * B(n, k)      (FP32 accumulation in TMEM)
 //
 // One CTA per SM walks a static list of work units (output tile x contraction
-// split).  Roles inside the 256-thread CTA:
+// split).  Roles inside the CTA (256 threads; the router's BF16x3 mode adds the
+// converter warps 2, 3, 8, 9 and, on single CTAs, warp 10):
 //   warp 0      TMA producer: loads 128x64 A and BNx64 B bf16 tiles (128-byte
 //               swizzle) into a shared-memory ring of STAGES block slots, one
 //               or two contraction blocks per ring stage (GemmArgs::kps);
@@ -10,6 +11,8 @@
 //               N=BN, K=16 per instruction), accumulating into one of two TMEM
 //               accumulators so the epilogue of a tile overlaps the next tile's
 //               main loop;
+//   warp 10     BF16x3 on single CTAs: the loads of B's bf16 planes (warp 0 then loads
+//               only A's FP32 staging tiles);
 //   warps 4..7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)...), BF16 round-to-nearest-even or FP32, staged in
 //               shared memory and written by TMA stores or 16-byte stores; for
@@ -152,7 +155,13 @@ struct TileCfg {
   static constexpr int EPI_BYTES = 4 * 4096 * EPI_BUFS;
   // X3: four converter warps (2, 3, 8, 9: one per SM sub-partition) split A
   static constexpr int CONV_WARPS = X3 ? 4 : 0;
-  static constexpr int THREADS = X3 ? 320 : 256;
+  // X3 on single CTAs: B's planes have their own producer (warp B_WARP_ID), so the
+  // thread that loads A's FP32 staging tiles and the one that loads B each wait on one
+  // ring.  (One thread serving both took ~1000 cycles per 32-wide block for two barrier
+  // tests, two expect-tx arrivals and three TMA issues, against ~770 cycles of MMAs.)
+  static constexpr bool B_WARP = X3 && !PAIR;
+  static constexpr int B_WARP_ID = 10;
+  static constexpr int THREADS = X3 ? (B_WARP ? 352 : 320) : 256;
   // full, empty, tmem_full x2, tmem_empty x2, drain (+ staging full / empty for X3)
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SSTAGES;
   static constexpr int SMEM_BYTES =
@@ -629,8 +638,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || (C::B_WARP && warp == C::B_WARP_ID)) {
+    // ------------------------------------------------------------ producer(s)
     if (lane == 0) {
       int stage = 0, sstage = 0;
       uint32_t phase = 0, sphase = 0;
@@ -671,6 +680,18 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         seek(xc, 0);
         seek(bc, 0);
         seek(fc, 0);
+        // (with B_WARP: warp 0 walks A's cursor only, warp B_WARP_ID B's only, and each
+        // tests its one barrier with try_wait, which may suspend the thread briefly,
+        // instead of test_wait's pure poll)
+        if (C::B_WARP) {
+          if (warp == 0)
+            bc.done = true;
+          else
+            xc.done = true;
+        }
+        auto poll = [&](uint32_t bar, uint32_t parity) {
+          return C::B_WARP ? mbar_test(bar, parity) : mbar_peek(bar, parity);
+        };
         // (a pair's peer: one arrival on the leader's full barrier per stage, once this
         // CTA's converters have filled it)
         const bool forward = PAIR && rank != 0;
@@ -686,7 +707,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         while (!xc.done || !bc.done || !fc.done) {
           if (xc.done) issued_x = SSTAGES;  // (fewer blocks than staging slots)
           bool progressed = false;
-          if (!xc.done && mbar_peek(sempty_bar(sstage), sphase ^ 1u)) {
+          if (!xc.done && poll(sempty_bar(sstage), sphase ^ 1u)) {
             const uint32_t xa = sbase + sstage * C::SA_BYTES;
             const uint32_t xf = sfull_bar(sstage);
             const int a_row0 = xc.tm * C::TM + static_cast<int>(rank) * C::BM;
@@ -724,7 +745,7 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             b_ready = true;
           }
           if (b_ready && !bc.done &&
-              (PAIR ? mbar_peek_cluster(empty_bar(stage), phase ^ 1u) : mbar_peek(empty_bar(stage), phase ^ 1u))) {
+              (PAIR ? mbar_peek_cluster(empty_bar(stage), phase ^ 1u) : poll(empty_bar(stage), phase ^ 1u))) {
             const uint32_t sb = base + stage * C::STAGE_BYTES + C::A_BYTES;
             // a pair's B loads all complete on the leader's full barrier
             const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
@@ -882,8 +903,9 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       // epilogue, late enough that its CTAs do not sit on this grid's SMs for the
       // whole main loop (measured on GB300 against a trigger right after setup: the
       // T = 64 forward 10.2 -> 9.7 us, fwd + fwd + bwd at T = 1024, 4096 -> 1024,
-      // 71.1 -> 67.4 us; the large calls unchanged).
-      pdl_launch_dependents();
+      // 71.1 -> 67.4 us; the large calls unchanged).  (With B_WARP: the thread that
+      // loads B, whose loads come last.)
+      if (!C::B_WARP || warp != 0) pdl_launch_dependents();
       // Every load this thread issued has landed before the CTA may exit: on the
       // stage's full barrier, or for a pair (whose loads complete on the leader's
       // barrier) on the empty barrier the leader's MMAs release after reading it.

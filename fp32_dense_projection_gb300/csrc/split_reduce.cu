@@ -8,8 +8,9 @@
 // output type.  The order depends on nothing but the plan, so the result is
 // bitwise repeatable (FlashInfer page "... restore the K1 weight-gradient routes
 // ...": deterministic weight gradients over a fixed split of the 64-token blocks).
-// Every float4 of every split tile has its own thread, which issues the loads of
-// all its splits at once, so the sum costs about one round trip to L2.  It is
+// Every float4 of every split tile (transposed output: every four rows of one) has
+// its own thread, which issues the loads of all its splits at once (or in batches
+// of 8 or 16), so the sum costs about one round trip to L2.  It is
 // launched as a programmatic dependent of the GEMM: its launch overlaps the GEMM's
 // tail and griddepcontrol.wait holds it until the partials are complete and
 // visible.
@@ -29,21 +30,26 @@ struct ReduceArgs {
 
 // Row-major output: one thread per float4 of the split tiles.  Thread t of the (slot,
 // 32-column chunk) handles row t % 128 and float4 column t / 128 of the chunk, so a
-// warp's loads are 512 contiguous bytes of each partial, and loads all splits (up to
+// warp's loads are 512 contiguous bytes of each partial, and loads all splits (8 or
 // 16 at a time) before adding them in order; it stores its 4 values as one 16-byte
 // store (or 8 bytes of bf16).  Transposed output (the swapped weight gradient): one
 // thread per 4 rows of a float4 column (thread t: rows 4(t % 32) .. +3, float4 column
 // t / 32), which it writes as one 16-byte (8-byte) store per output column, next to
 // its neighbouring lanes' rows.  Partial layout: [slot][split][bn/4][128] float4.
 constexpr int kReduceThreads = 128;
-constexpr int kReduceBatch = 16;
 constexpr int kReduceBatchTrans = 4;  // (four rows each: 16 float4 loads in flight)
 
+// TRANS: the transposed output (a.out_trans).  BATCH: row-major partials loaded at a
+// time, 8 for plans of at most 8 splits and 16 above (measured on GB300: 8 is 1-2 us
+// faster for the 7- and 8-way thin weight-gradient sums at T = 65537, 16 is 2-3 us
+// faster for the router forward's 16- and 19-way sums).  Each combination is its own
+// instantiation, so none carries the registers of a larger one.
+template <bool TRANS, int BATCH>
 __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __grid_constant__ ReduceArgs ra) {
   pdl_wait();  // the GEMM's partials are complete and visible
   const GemmArgs& a = ra.g;
   // CTAs per (slot, chunk): 1024 float4, one or four per thread
-  const int per_slice = (a.out_trans ? kBlockM * 8 / 4 : kBlockM * 8) / kReduceThreads;
+  const int per_slice = (TRANS ? kBlockM * 8 / 4 : kBlockM * 8) / kReduceThreads;
   const int cta = static_cast<int>(blockIdx.x);
   const int slice = cta / per_slice;
   const int t = (cta - slice * per_slice) * kReduceThreads + static_cast<int>(threadIdx.x);  // 0..1023 (255)
@@ -62,14 +68,14 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
   tile_coords(a, a.full_units + ptile, &bt, &tm, &tn);
   void* out = out_at(a, bt);
   // row of the slot (the first of four: transposed output), float4 column in the chunk
-  const int row = a.out_trans ? 4 * (t & 31) : t & (kBlockM - 1), j = a.out_trans ? t >> 5 : t >> 7;
+  const int row = TRANS ? 4 * (t & 31) : t & (kBlockM - 1), j = TRANS ? t >> 5 : t >> 7;
   const int64_t m = static_cast<int64_t>(tm) * ra.tile_rows + rank * kBlockM + row;
   const int64_t col = static_cast<int64_t>(tn) * ra.bn + chunk * 32 + 4 * j;
   if (m >= a.gm || col >= a.gn) return;  // (transposed: gm and gn are multiples of 4)
   const size_t pstride = static_cast<size_t>(kBlockM) * ra.bn / 4;  // float4 per partial tile
   const float4* src = a.partials + static_cast<size_t>(slot) * a.splits * pstride +
                       static_cast<size_t>(chunk * 8 + j) * kBlockM + row;
-  if (a.out_trans) {
+  if constexpr (TRANS) {
     float4 acc[4];
     for (int s0 = 0; s0 < nparts; s0 += kReduceBatchTrans) {
       float4 x[kReduceBatchTrans][4];
@@ -89,13 +95,13 @@ __global__ void __launch_bounds__(kReduceThreads) split_reduce_kernel(const __gr
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // splits in ascending order: acc = p_0, then acc += p_s
-  for (int s0 = 0; s0 < nparts; s0 += kReduceBatch) {
-    float4 x[kReduceBatch];
+  for (int s0 = 0; s0 < nparts; s0 += BATCH) {
+    float4 x[BATCH];
 #pragma unroll
-    for (int k = 0; k < kReduceBatch; ++k)
+    for (int k = 0; k < BATCH; ++k)
       if (s0 + k < nparts) x[k] = __ldcg(src + static_cast<size_t>(s0 + k) * pstride);
 #pragma unroll
-    for (int k = 0; k < kReduceBatch; ++k)
+    for (int k = 0; k < BATCH; ++k)
       if (s0 + k < nparts) sum_step(acc, x[k], s0 + k == 0);
   }
   if (a.out_f32) {
@@ -129,14 +135,23 @@ cudaError_t launch_split_reduce(const GemmLaunch& l, int bn, bool pair, int64_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_reduce_kernel, ra);
+  if (l.args.out_trans) return cudaLaunchKernelEx(&cfg, split_reduce_kernel<true, 8>, ra);
+  return l.args.splits > 8 ? cudaLaunchKernelEx(&cfg, split_reduce_kernel<false, 16>, ra)
+                           : cudaLaunchKernelEx(&cfg, split_reduce_kernel<false, 8>, ra);
 }
 
 cudaError_t set_attributes_reduce() {
   // the same shared-memory carveout as the GEMM kernels, so switching between them
   // does not reconfigure the SMs
-  return cudaFuncSetAttribute(split_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = cudaFuncSetAttribute(split_reduce_kernel<false, 8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(split_reduce_kernel<false, 16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(split_reduce_kernel<true, 8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 }  // namespace dp

@@ -11,6 +11,7 @@
 //               N=BN, K=16 per instruction), accumulating into one of two TMEM
 //               accumulators so the epilogue of a tile overlaps the next tile's
 //               main loop;
+//   warp 2      BF16 mode: the loads of B (warp 0 then loads only A);
 //   warp 10     BF16x3 on single CTAs: the loads of B's bf16 planes (warp 0 then loads
 //               only A's FP32 staging tiles);
 //   warps 4..7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
@@ -155,13 +156,16 @@ struct TileCfg {
   static constexpr int EPI_BYTES = 4 * 4096 * EPI_BUFS;
   // X3: four converter warps (2, 3, 8, 9: one per SM sub-partition) split A
   static constexpr int CONV_WARPS = X3 ? 4 : 0;
-  // X3 on single CTAs: B's planes have their own producer (warp B_WARP_ID), so the
-  // thread that loads A's FP32 staging tiles and the one that loads B each wait on one
-  // ring.  (One thread serving both took ~1000 cycles per 32-wide block for two barrier
+  // B's loads have their own producer thread (lane 0 of warp B_WARP_ID): warp 2, idle
+  // otherwise, in BF16 mode; an eleventh warp for BF16x3 on single CTAs, so the thread
+  // that loads A's FP32 staging tiles and the one that loads B each wait on one ring.
+  // (One thread serving both took ~1000 cycles per 32-wide BF16x3 block for two barrier
   // tests, two expect-tx arrivals and three TMA issues, against ~770 cycles of MMAs.)
-  static constexpr bool B_WARP = X3 && !PAIR;
-  static constexpr int B_WARP_ID = 10;
+  // BF16x3 pairs keep one producer thread.
+  static constexpr bool B_WARP = !(X3 && PAIR);
+  static constexpr int B_WARP_ID = X3 ? 10 : 2;
   static constexpr int THREADS = X3 ? (B_WARP ? 352 : 320) : 256;
+  static_assert(X3 || (B_WARP && B_WARP_ID == 2), "BF16 mode: warp 2 loads B");
   // full, empty, tmem_full x2, tmem_empty x2, drain (+ staging full / empty for X3)
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SSTAGES;
   static constexpr int SMEM_BYTES =
@@ -607,7 +611,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
       // X3: the B loads' arrival and one per converter warp; for a pair, the leader's
       // also takes one forwarded arrival from the peer, whose own full barriers only
       // collect its converters
-      mbar_init(full_bar(s), !X3 ? 1 : (PAIR && rank != 0) ? C::CONV_WARPS : 1 + C::CONV_WARPS + (PAIR ? 1 : 0));
+      // (BF16: one expect-tx arrival from each of the A and B producer threads)
+      mbar_init(full_bar(s), !X3 ? 2 : (PAIR && rank != 0) ? C::CONV_WARPS : 1 + C::CONV_WARPS + (PAIR ? 1 : 0));
       mbar_init(empty_bar(s), 1);
     }
     for (int s = 0; s < SSTAGES; ++s) {
@@ -817,6 +822,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
         }
       }
       if (!X3) pdl_wait();  // the previous kernel on the stream (launched as its dependent) is done
+      // (BF16: warp 0 loads A, warp B_WARP_ID loads B, each counting its own bytes)
+      const bool load_a = warp == 0, load_b = warp != 0;
       const int kps = (X3 || args.kps != 2) ? 1 : 2;
       const int nst = STAGES / kps;  // stages of the ring, kps block slots each
       for (int k = 0; !X3 && ok; ++k) {
@@ -839,7 +846,9 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           }
           // a pair's loads all complete on the leader's full barrier
           const uint32_t fb = PAIR ? map_shared_rank(full_bar(stage), 0) : full_bar(stage);
-          if (rank == 0) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * C::STAGE_BYTES * nb);
+          if (rank == 0)
+            mbar_expect_tx(full_bar(stage),
+                           (PAIR ? 2 : 1) * nb * ((load_a ? C::A_BYTES : 0) + (load_b ? C::B_BYTES : 0)));
           // (batched plans: every map has a trailing batch dimension; `hint`: the operand
           // is read once by the launch, loaded with the evict-first policy)
           auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, bool hint) {
@@ -872,7 +881,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             const uint32_t sa = base + (stage * kps + j) * C::STAGE_BYTES;
             const uint32_t sb = sa + C::A_BYTES;
             // MN-major: 64-column groups of 64 contraction rows (8 KB each)
-            if (a_mn && ga.a3d) {
+            if (!load_a) {
+            } else if (a_mn && ga.a3d) {
               load3(sa, mapA, kb * C::BK, a_row0 / 64, ha);
             } else if (a_mn) {
               load(sa, mapA, a_row0, kb * C::BK, ha);
@@ -880,7 +890,8 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
             } else {
               load(sa, mapA, kb * C::BK, a_row0, ha);
             }
-            if (B_MN && ga.b3d) {
+            if (!load_b) {
+            } else if (B_MN && ga.b3d) {
               load3(sb, mapB, kb * C::BK, b_row0 / 64, hb);
             } else if (B_MN) {
 #pragma unroll

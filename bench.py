@@ -196,12 +196,31 @@ def run_profile_case(args, local):
         ev[1].record()
         torch.cuda.synchronize()
         times.append(ev[0].elapsed_time(ev[1]))
+    # each kernel's own duration as CUPTI records it: median of five calls, the 2xL2
+    # buffer zeroed before each (the events above time whole calls, host enqueue included)
+    from torch.profiler import ProfilerActivity, profile
+    flush = torch.empty(2 * torch.cuda.get_device_properties(device).L2_cache_size, dtype=torch.uint8, device=device)
+    with profile(activities=[ProfilerActivity.CUDA]):  # CUPTI warm-up: the first session can miss kernels
+        flush.zero_()
+        torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(5):
+            flush.zero_()
+            call(out)
+        torch.cuda.synchronize()
+    mine = ("gemm_bf16_kernel", "split_reduce_kernel", "split_x3_kernel", "router_ffma_kernel")
+    kern = {}
+    for e in prof.events():
+        if e.device_type == torch.autograd.DeviceType.CUDA and any(k in e.name for k in mine):
+            name = e.name.replace("(anonymous namespace)::", "").split("(")[0].replace("void ", "")
+            kern.setdefault(name, []).append(e.time_range.end - e.time_range.start)
     assert dp.device_error() == 0
     flop = 2.0 * T * N * K * (args.profile_B if batched else 1)
     us = statistics.median(times) * 1e3
     return {"profile_case": op, "T": T, "N": N, "K": K, "B": args.profile_B if batched else 1,
             "out": "f32" if out_dtype == torch.float32 else "bf16",
-            "us": round(us, 2), "tflops": round(flop / us / 1e6, 1), "plan": plan}
+            "us": round(us, 2), "tflops": round(flop / us / 1e6, 1),
+            "kernel_us_cold_l2": {k: round(statistics.median(v), 1) for k, v in kern.items()}, "plan": plan}
 
 
 def run_gpu(args, world, rank, local):
@@ -760,7 +779,8 @@ def main():
     ap.add_argument("--profile-op", default=None,
                     choices=["fwd", "dgrad", "wgrad", "router_fwd", "router_dgrad", "router_wgrad",
                              "fwd_batched", "dgrad_batched", "wgrad_batched"],
-                    help="run only a small single-op case (for ncu captures)")
+                    help="run only a single-op case (for ncu captures); prints each kernel's CUPTI duration "
+                         "after a cold L2 as kernel_us_cold_l2")
     ap.add_argument("--profile-T", type=int, default=4096)
     ap.add_argument("--profile-N", type=int, default=0)
     ap.add_argument("--profile-K", type=int, default=0)

@@ -1214,13 +1214,13 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
     const bool leader = threadIdx.x == 128;
     int local = 0;
     // the epilogue warps (of both CTAs of a pair) release the accumulator on the
-    // leader's barrier
+    // leader's barrier, once their tensor-memory reads have completed (tmem_wait_ld)
     auto release_acc = [&](int a) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (PAIR)
-          mbar_arrive_cluster(map_shared_rank(tempty_bar(a), 0));
+          mbar_arrive_remote(map_shared_rank(tempty_bar(a), 0));
         else
           mbar_arrive(tempty_bar(a));
       }

@@ -315,6 +315,16 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
   return r;
 }
 
+// Arrive on an mbarrier given by its shared::cluster address (possibly the peer's),
+// with the arrive's default release at CTA scope: for an arrival that only reports
+// work the arriving thread has already completed (the epilogue's tensor-memory reads,
+// finished by tcgen05.wait::ld and ordered by tcgen05.fence::before_thread_sync).
+// Measured on GB300: ~65 cycles, where the cluster-scope release below took 2200-2900
+// cycles in an epilogue whose bulk stores were in flight.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(kFfmaThreads, 1) router_ffma_kernel(const __gr
   const int c0 = static_cast<int>(static_cast<int64_t>(s) * args.kchunks / S);
   const int c1 = static_cast<int>(static_cast<int64_t>(s + 1) * args.kchunks / S);
 
+  // (launched as a programmatic dependent of the kernel before it on the stream: its
+  // setup overlaps that kernel's tail, and nothing is read before that kernel is done)
+  pdl_wait();
   const int tid = static_cast<int>(threadIdx.x);
   const int g = tid / C::TG, t = tid - g * C::TG;
   const int ty = t / C::COLS, tx = t - ty * C::COLS;
@@ -253,8 +256,11 @@ cudaError_t launch_t(const FfmaArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kFfmaThreads, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (a.splits > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = static_cast<unsigned>(a.splits);

@@ -52,6 +52,11 @@ __device__ __forceinline__ void locate(const SplitJobs& jobs, uint64_t i, const 
 }
 
 __global__ void __launch_bounds__(kSplitThreads) split_x3_kernel(const __grid_constant__ SplitJobs jobs) {
+  // Launched as a programmatic dependent of the kernel before it (so its launch overlaps
+  // that kernel's tail): it reads nothing until that kernel is done, and only then lets
+  // the GEMM launch, whose staging loads of its FP32 operand start before the GEMM's own
+  // wait -- by then every kernel before this one has completed.
+  pdl_wait();
   pdl_launch_dependents();  // the GEMM may start staging its other operand meanwhile
   // the zero fill of a non-deterministic call's output, one float4 per thread and step
   const uint64_t gstep = static_cast<uint64_t>(gridDim.x) * blockDim.x;
@@ -122,8 +127,17 @@ cudaError_t launch_split_x3(const SplitJob* jobs, int njobs, int sm_count, cudaS
   const int64_t per_block = kSplitThreads * kSplitQuads;
   const int64_t work = std::max<int64_t>(total, p.zquads);
   const int64_t blocks = std::min<int64_t>((work + per_block - 1) / per_block, static_cast<int64_t>(sm_count) * 8);
-  split_x3_kernel<<<static_cast<unsigned>(blocks), kSplitThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_x3_kernel, p);
 }
 
 cudaError_t set_attributes_split() {

@@ -1,10 +1,8 @@
 // dp_gemm_wgrad_noalloc: the weight gradient for callers that cannot allocate.
 //
-// Some callers cannot hand the library a workspace: a framework whose device
-// memory pool is frozen while a training step is captured into a CUDA graph, a
-// serving or real-time runtime that reserves all device memory at start-up, or a
-// plugin whose host forbids cudaMalloc on its hot path because it can
-// synchronise the device.  For them this entry point runs the same weight-gradient
+// Some callers cannot hand the library a workspace: a serving or real-time runtime
+// that reserves all device memory at start-up, or a plugin whose host forbids
+// cudaMalloc on its hot path because it can synchronise the device.  For them this entry point runs the same weight-gradient
 // kernels as dp_gemm_wgrad_ex, with its split partials placed in a scratch array
 // that is part of the library image itself.
 //
@@ -12,8 +10,8 @@
 // that loads this part of the library holds it until the process exits.  In host
 // code its name is only a stand-in for the device symbol, so its device address
 // is looked up once per device, with that device current, via
-// cudaGetSymbolAddress; the first call on each device does this set-up and should
-// therefore come before any stream capture.  Every call shares the one array (the
+// cudaGetSymbolAddress; the first call on each device does this set-up.  Every call
+// shares the one array (the
 // partials need no initial value), so calls that overlap on the GPU (two streams,
 // two threads) race on it.
 #include <cuda_runtime.h>

@@ -155,18 +155,17 @@ dp_status dp_gemm_wgrad_ex(const void* dY, int64_t ldg, const void* X, int64_t l
 
 /* Weight gradient for callers that cannot allocate device memory.  The pages have
  * no counterpart of this entry point; it exists for this library's users.
- * Some callers cannot pass a workspace: a framework whose memory pool is frozen
- * while a step is captured into a CUDA graph, a serving runtime that reserves all
- * device memory at start-up, or a plugin whose host forbids cudaMalloc on its hot
- * path because it can synchronise the device.  This call computes exactly what
+ * Some callers cannot pass a workspace: a serving runtime that reserves all device
+ * memory at start-up, or a plugin whose host forbids cudaMalloc on its hot path
+ * because it can synchronise the device.  This call computes exactly what
  * dp_gemm_wgrad_ex computes (same plan, same kernels, same bits) but keeps its
  * split partials in a 64 MiB scratch array built into the library,
  * which every GPU that loads the library holds until the process exits.  The
  * caller still passes dY, X and dW.  Arguments and errors as dp_gemm_wgrad_ex;
  * a shape whose plan needs more than 64 MiB of scratch returns DP_ERR_WORKSPACE
  * (dp_workspace_size(DP_OP_WGRAD, ...) tells beforehand).  The first call on each
- * device looks up the array's device address and should come before any stream
- * capture.  Every call shares the one array; calls that overlap on the GPU
+ * device looks up the array's device address (with that device current).  Every
+ * call shares the one array; calls that overlap on the GPU
  * (different streams or threads) race on it and must be serialised by the caller.  No cudaMalloc,
  * cudaFree or allocating library routine is called. */
 dp_status dp_gemm_wgrad_noalloc(const void* dY, int64_t ldg, const void* X, int64_t ldx,

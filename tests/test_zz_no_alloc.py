@@ -1,9 +1,8 @@
 """The weight-gradient entry point that allocates nothing.
 
-It serves callers that cannot allocate device memory (a pool frozen during CUDA
-graph capture, a runtime that reserves all memory at start-up, a host that forbids
-cudaMalloc on its hot path): its split scratch is a 64 MiB array inside the
-library.  Called through the C ABI, twice in a row on the same shapes (the second
+It serves callers that cannot allocate device memory (a runtime that reserves all
+memory at start-up, a host that forbids cudaMalloc on its hot path): its split
+scratch is a 64 MiB array inside the library.  Called through the C ABI, twice in a row on the same shapes (the second
 call finds the first call's leftovers in the shared array), its output must match
 the workspace-taking entry point's: within the FP32 budget the parity tests use,
 and in fact bit for bit, since both run the same plan and kernel.
@@ -56,6 +55,23 @@ def test_noalloc_non_deterministic_fp32():
         torch.cuda.synchronize()
         ok, msg = check(got.double().cpu().numpy(), want.double().cpu().numpy(), "f32")
         assert ok, f"call {call}: {msg}"
+    assert dp.device_error() == 0
+
+
+def test_noalloc_back_to_back_calls_on_one_stream():
+    # two calls queued without a synchronisation between them share the scratch array:
+    # the stream orders them, so each output is the workspace entry point's, bit for bit
+    T, N, K = 16173, 64, 4096
+    cases = [inputs.thin_wgrad(T, N, K, seed=s) for s in (8, 9)]
+    dev = [{k: v.to(DEV) for k, v in c.items()} for c in cases]
+    want = [dp.dp_gemm_wgrad(d["dY"], d["X"], out_dtype=torch.float32) for d in dev]
+    torch.cuda.synchronize()
+    got = [torch.full((N, K), float("nan"), dtype=torch.float32, device=DEV) for _ in dev]
+    for d, o in zip(dev, got):
+        dp.dp_gemm_wgrad_noalloc(d["dY"], d["X"], out=o)
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert torch.equal(got[i].view(torch.int32), want[i].view(torch.int32)), f"call {i}"
     assert dp.device_error() == 0
 
 

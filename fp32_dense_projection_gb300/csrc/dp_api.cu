@@ -441,6 +441,18 @@ dp_status prepare_view(const Plan& p, const DeviceState& dev, const void* A, int
                           CU_TENSOR_MAP_SWIZZLE_128B, 0, nb, bso))
                     ? 1
                     : 0;
+  // BF16-mode FP32 whole tiles of one problem whose width is a whole number of 32-column
+  // blocks store two staged blocks (the epilogue warp's two) per TMA store through a
+  // [block][row][32] view of the output (a box cannot clip inside a block, hence the
+  // width rule), when a CTA has several tiles, whose epilogue then paces it (measured on
+  // GB300: router input gradient T = 16384 90.9 -> 86.6 us; a CTA with one tile waits for
+  // both blocks at once and gains nothing).  DP_FORCE_STORE2=0: one block per store.
+  const bool several_tiles = p.units > p.grid / (p.pair ? 2 : 1);
+  a.tma_store2 = (!x3 && a.tma_store && p.out_f32 && nb == 1 && p.gn % 32 == 0 && several_tiles &&
+                  env_int("DP_FORCE_STORE2", 1) != 0 &&
+                  make_map(&a.tmO2, out, p.gm, p.gn, ldo, 32, true, 32, CU_TENSOR_MAP_SWIZZLE_128B, 2))
+                     ? 1
+                     : 0;
   a.epi_single = env_int("DP_FORCE_EPI_SINGLE", 0) != 0 ? 1 : 0;  // (comparisons)
   uint8_t* w = static_cast<uint8_t*>(ws);
   a.partials = p.splits > 1 ? reinterpret_cast<float4*>(w + p.off_partials) : nullptr;

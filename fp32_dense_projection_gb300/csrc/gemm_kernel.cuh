@@ -107,7 +107,12 @@ struct GemmArgs {
   // leading dimension ldo; boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16
   // columns) with the 128-byte swizzle the epilogue stages them in)
   int32_t tma_store;
+  // tma_store2 = 1 (FP32 output of one problem, a whole number of 32-column blocks
+  // wide): two staged 32 x 32 blocks leave in one TMA store, through tmO2, the output as
+  // [32-column block][row][32] with the same swizzle
+  int32_t tma_store2;
   CUtensorMap tmO;
+  CUtensorMap tmO2;
 };
 
 // X3: the FP32 router's BF16x3 mode.  A stage of the MMA ring then holds the bf16
@@ -1266,6 +1271,37 @@ __global__ void __launch_bounds__(TileCfg<BN, PAIR, X3>::THREADS, 1)
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           store_block32(ga, outb, ebuf, lane, m0, n0 + c * 32, v, w.split);
         }
+      } else if (C::EPI_BUFS == 2 && !w.split && ga.tma_store2 && !ga.epi_single) {
+        // FP32 through the [32-column block][row][32] view: both staging blocks of the warp,
+        // side by side, leave as one 3-D box (8 KB per TMA store: issuing a store took
+        // ~280-800 cycles of the ~900 a 4 KB block cost); they are restaged once that
+        // store has read them
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tcol + c * 32, r0);
+          tmem_ld_32x32b_x32(tcol + (c + 1) * 32, r1);
+          tmem_wait_ld();
+          if (c + 2 == BN / 32) release_acc(acc);  // accumulator may be reused
+          if (lane == 0) bulk_wait_group_read0();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r0[j]);
+          stage_block32(ga, ebuf, lane, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r1[j]);
+          stage_block32(ga, ebuf + 4096u, lane, v);
+          fence_proxy_async_shared();
+          __syncwarp();
+          const int32_t z = static_cast<int32_t>((n0 + c * 32) / 32), y = static_cast<int32_t>(m0);
+          if (lane == 0 && y < ga.gm && static_cast<int64_t>(z) * 32 < ga.gn) {
+            tma_store_3d(&ga.tmO2, ebuf, 0, y, z);
+            bulk_commit_group();
+          }
+        }
+        // (a store from both blocks may be in flight: the next staging waits for it)
+        store_pending = false;
+        sbuf = 0;
       } else if (!w.split) {
         // Stage and hand to TMA (which clips rows >= gm, columns >= gn) 4 KB at a
         // time: an FP32 32 x 32 block, or two BF16 32 x 32 blocks side by side (32

@@ -281,6 +281,10 @@ dp_status router_wgrad_ex(const float* dY, int64_t ldg, const float* X, int64_t 
  * the reduction kernel instead of inside the GEMM's clusters; the two give the
  * same bits), DP_FORCE_TMA_STORE (0 / 1: the epilogue's whole-tile TMA stores off
  * / on for every non-transposed output; both store paths give the same bits),
+ * DP_FORCE_STORE2=0 (FP32 whole tiles store one 32 x 32 block per TMA store
+ * instead of two; the same bits), DP_FORCE_EPI_SINGLE=1 (one TMA-store staging
+ * block per epilogue warp instead of two; the same bits), DP_FORCE_EVICT_FIRST=0
+ * (no L2 evict-first policy on the operand a launch reads once; the same bits),
  * DP_FORCE_FUSE (0 / 1 / 2 / 3: dp_gemm_bwd as two calls or as one co-scheduled
  * launch, see dp_gemm_bwd), DP_FORCE_STREAM_K (0: never; 1: a stream-K plan where
  * the shape admits one), DP_FORCE_ATOMIC (calls with deterministic = 0: 0 ordered

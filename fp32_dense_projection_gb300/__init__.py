@@ -478,9 +478,9 @@ OPS = {"fwd": dp_gemm_fwd, "dgrad": dp_gemm_dgrad, "wgrad": dp_gemm_wgrad,
 def dp_gemm_wgrad_noalloc(dY, X, out, out_dtype=None, deterministic=True, stream=None):
     """Weight gradient through the entry point that allocates nothing.
 
-    For callers that cannot allocate device memory (a frozen pool during graph
-    capture, a runtime that pre-reserves all memory, a host that forbids cudaMalloc
-    on its hot path): the split scratch lives in a 64 MiB array inside the library.
+    For callers that cannot allocate device memory (a runtime that pre-reserves all
+    memory, a host that forbids cudaMalloc on its hot path): the split scratch lives
+    in a 64 MiB array inside the library.
     ``out`` must be given (the caller owns every buffer).  Calls on different streams
     must not overlap: they share the one scratch array.
     """
